@@ -1,0 +1,192 @@
+"""Seeded synthetic inputs shared by the CUDA tests, the bench and the oracle tests.
+
+This module only *draws* operands: it holds none of the GEMM's arithmetic.  Every
+tensor is produced on the host from a counter-based generator, so the same
+(seed, index) always gives the same bf16 bit pattern on any machine.
+
+Generator (the pages fix none; this is the plain reading used throughout):
+  * splitmix64 in counter form: x_i = mix(seed + (i + 1) * 0x9E3779B97F4A7C15);
+  * uniform[-1, 1):      u = (x >> 11) * 2**-53,  v = 2u - 1;
+  * normal(0, sigma):    Box-Muller on two consecutive draws of the stream;
+  * rounding to bf16:    round-to-nearest-even straight from the fp64 value
+    (no intermediate fp32 rounding), with no NaN/Inf possible by construction.
+
+Workloads (the shapes of the pages' benchmarks: square cubes, 7B-model MLP
+projections, decode batches) are listed in ``WORKLOADS``.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+SEED_A_BASE = 0x5EED0001
+SEED_B_BASE = 0x5EED1001
+
+
+def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
+    """Draws ``count`` 64-bit words x_start .. x_{start+count-1} of the stream."""
+    idx = np.arange(start + 1, start + 1 + count, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * _GAMMA
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def uniform01(seed: int, start: int, count: int) -> np.ndarray:
+    """fp64 values in [0, 1) with 53 random bits."""
+    return (splitmix64(seed, start, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def uniform_pm1(seed: int, count: int, start: int = 0) -> np.ndarray:
+    """Elements start .. start+count-1 of the uniform[-1, 1) stream."""
+    return uniform01(seed, start, count) * 2.0 - 1.0
+
+
+def normal(seed: int, count: int, sigma: float, start: int = 0) -> np.ndarray:
+    """Box-Muller: draws 2i and 2i+1 give the i-th pair (cos, sin) of variates.
+
+    Element e is the (e % 2)-th member of pair e // 2, so any even ``start``
+    yields exactly the slice of the full stream.
+    """
+    assert start % 2 == 0
+    npairs = (count + 1) // 2
+    u = uniform01(seed, start, 2 * npairs).reshape(npairs, 2)
+    u1 = 1.0 - u[:, 0]  # (0, 1]: log is finite
+    r = np.sqrt(-2.0 * np.log(u1))
+    t = 2.0 * np.pi * u[:, 1]
+    z = np.empty((npairs, 2), dtype=np.float64)
+    z[:, 0] = r * np.cos(t)
+    z[:, 1] = r * np.sin(t)
+    return z.reshape(-1)[:count] * sigma
+
+
+def draws(dist: str, seed: int, start: int, count: int) -> np.ndarray:
+    """fp64 draws for element indices [start, start + count) of one tensor."""
+    if dist == "uniform":
+        return uniform_pm1(seed, count, start)
+    if dist.startswith("normal"):
+        sigma = float(dist.split(":")[1]) if ":" in dist else 1.0
+        return normal(seed, count, sigma, start)
+    raise ValueError(dist)
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp64 to the nearest bf16 (ties to even); returns uint16 bit patterns.
+
+    bf16 keeps 8 significant bits, so an fp64 significand (53 bits) is rounded at
+    bit 45.  Values here are finite and far above the bf16 subnormal range, or zero.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    bits = x.view(np.uint64)
+    lsb = (bits >> np.uint64(45)) & np.uint64(1)
+    bias = np.uint64((1 << 44) - 1) + lsb
+    with np.errstate(over="ignore"):
+        rounded = ((bits + bias) >> np.uint64(45)) << np.uint64(45)
+    f32 = rounded.view(np.float64).astype(np.float32)  # exact: fits in 8 bits
+    return (f32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to fp32 (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def matrix(rows: int, cols: int, dist: str, seed: int, ld: int | None = None,
+           pad_value: int = 0xFFFF) -> np.ndarray:
+    """A rows x ld uint16 matrix whose first ``cols`` columns hold bf16 draws.
+
+    Element (r, c) is draw number r*cols + c of the stream, so the values do not
+    depend on ``ld``; padding columns hold ``pad_value`` (a NaN pattern by default,
+    so a kernel that reads padding shows it).
+    """
+    ld = cols if ld is None else ld
+    assert ld >= cols
+    core = np.empty((rows, cols), dtype=np.uint16)
+    step = max(2, (1 << 24) // max(cols, 1) // 2 * 2)  # rows per chunk (even)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        v = draws(dist, seed, r0 * cols, (r1 - r0) * cols)
+        core[r0:r1] = f64_to_bf16_bits(v).reshape(r1 - r0, cols)
+    if ld == cols:
+        return core
+    out = np.full((rows, ld), pad_value, dtype=np.uint16)
+    out[:, :cols] = core
+    return out
+
+
+def small_int_matrix(rows: int, cols: int, lo: int, hi: int, seed: int) -> np.ndarray:
+    """Integers in [lo, hi] stored as bf16 (exact for |v| <= 256)."""
+    u = uniform01(seed, 0, rows * cols)
+    v = np.floor(u * (hi - lo + 1)).astype(np.int64) + lo
+    return f64_to_bf16_bits(v.astype(np.float64)).reshape(rows, cols)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic GEMM problem C[M,N] = A[M,K] . B[N,K]^T."""
+    name: str
+    M: int
+    N: int
+    K: int
+    dist_a: str
+    dist_b: str
+    cfg: int  # seed offset
+    oracle: str  # "full" or "sampled"
+
+    @property
+    def seed_a(self) -> int:
+        return SEED_A_BASE + self.cfg
+
+    @property
+    def seed_b(self) -> int:
+        return SEED_B_BASE + self.cfg
+
+    def a(self) -> np.ndarray:
+        return matrix(self.M, self.K, self.dist_a, self.seed_a)
+
+    def b(self) -> np.ndarray:
+        return matrix(self.N, self.K, self.dist_b, self.seed_b)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def decode_bytes(self) -> int:
+        """Bytes a skinny GEMM must move at least once: weights, activations, output."""
+        return 2 * (self.N * self.K + self.M * self.K + self.M * self.N)
+
+
+def _decode(m: int, n: int, k: int, cfg: int) -> Workload:
+    tag = "up" if n > k else "down"
+    return Workload(f"dec{m}_{tag}", m, n, k, "normal:1", "normal:0.02", cfg, "full")
+
+
+WORKLOADS = {w.name: w for w in [
+    Workload("sq512", 512, 512, 512, "uniform", "uniform", 0, "full"),
+    Workload("sq2048", 2048, 2048, 2048, "uniform", "uniform", 1, "full"),
+    Workload("sq4096", 4096, 4096, 4096, "uniform", "uniform", 2, "full"),
+    Workload("mlp_up", 4096, 11008, 4096, "normal:1", "normal:0.02", 3, "full"),
+    Workload("mlp_down", 4096, 4096, 11008, "normal:1", "normal:0.02", 4, "full"),
+    _decode(1, 11008, 4096, 5), _decode(2, 11008, 4096, 6),
+    _decode(16, 11008, 4096, 7), _decode(64, 11008, 4096, 8),
+    _decode(1, 4096, 11008, 9), _decode(2, 4096, 11008, 10),
+    _decode(16, 4096, 11008, 11), _decode(64, 4096, 11008, 12),
+    Workload("sq8192", 8192, 8192, 8192, "uniform", "uniform", 13, "sampled"),
+    Workload("sq16384", 16384, 16384, 16384, "uniform", "uniform", 14, "sampled"),
+]}
+
+
+def sample_indices(extent: int, count: int, seed: int) -> np.ndarray:
+    """A sorted, seeded choice of ``count`` distinct indices in [0, extent)."""
+    if count >= extent:
+        return np.arange(extent, dtype=np.int64)
+    keys = splitmix64(seed, 0, extent)
+    return np.sort(np.argsort(keys, kind="stable")[:count]).astype(np.int64)
