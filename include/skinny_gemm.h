@@ -1,0 +1,221 @@
+/*
+ * skinny_gemm.h -- C ABI of the GB300 (sm_103a) bf16 GEMM / skinny-GEMV library.
+ *
+ * Operation (every GEMM entry point):
+ *
+ *     C[m, n] = sum_{k < K} A[m, k] * B[n, k]        0 <= m < M, 0 <= n < N
+ *
+ * with A[m, k] = A[m*lda + k], B[n, k] = B[n*ldb + k], C[m, n] = C[m*ldc + n].
+ * All three are bf16 (stored as 16-bit patterns), products are accumulated in
+ * fp32 and the result is rounded to bf16 with round-to-nearest-even.  B is laid
+ * out like a linear layer's weight [out_features, in_features], so C = A . B^T.
+ * This is the bf16 GEMM with fp32 accumulation of spark-kernels ("the bf16 gemm":
+ * 4096-cubed, the 7B-model 11008-wide MLP shapes and the decode shapes) and the
+ * skinny bf16 GEMV of "The kernels that were there" ("The GEMV": one pass over
+ * the weights for all rows of a small M, fp32 accumulation, bf16 store).
+ *
+ * Conventions shared by all entry points
+ *   - Pointers A, B, C are DEVICE pointers on the current CUDA device; the caller
+ *     owns them.  The library never frees or retains them.
+ *   - Every call only enqueues work on `stream` (never the legacy default stream,
+ *     never a device synchronisation), so calls may be captured in a CUDA graph
+ *     ("The kernels that were there", "The bench that lied": the launch must
+ *     follow the caller's stream).
+ *   - Synchronous argument errors return a non-zero sg_status before anything is
+ *     launched.  Launch failures return SG_ERR_CUDA (see sg_last_cuda_error).
+ *     Kernel-side wait timeouts are reported by sg_check_device_errors.
+ *   - Requirements: M, N, K >= 0; lda >= K, ldb >= K, ldc >= N; A, B, C 16-byte
+ *     aligned and lda, ldb, ldc multiples of 8 elements (16-byte row pitch), else
+ *     SG_ERR_MISALIGNED.  M = 0 or N = 0 is a no-op; K = 0 sets C to zero.
+ *   - C must not overlap A or B.
+ *   - The library keeps one workspace per device (Stream-K / split-K partial sums
+ *     and arrival counters), allocated on the first call that needs it.  That
+ *     first call must not happen during stream capture (SG_ERR_INVALID_ARG is
+ *     returned instead); make one warm-up call first.  Calls that run
+ *     concurrently on different streams of one device share that workspace and
+ *     are not supported.
+ */
+#ifndef SKINNY_GEMM_H
+#define SKINNY_GEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SG_API __attribute__((visibility("default")))
+#else
+#define SG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *sg_stream_t;
+
+typedef enum {
+    SG_OK = 0,
+    SG_ERR_INVALID_ARG = 1,        /* null pointer, negative size, ld too small, M > 64 on gemv */
+    SG_ERR_MISALIGNED = 2,         /* pointer or leading dimension breaks the 16-byte rule */
+    SG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    SG_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+    SG_ERR_TIMEOUT = 5,            /* a kernel gave up on a bounded wait */
+    SG_ERR_OUT_OF_MEMORY = 6       /* workspace allocation failed */
+} sg_status;
+
+/* Skinny-path kernels selectable through gemv_bf16_path. */
+typedef enum {
+    SG_PATH_AUTO = 0,        /* library's choice (see gemv_bf16) */
+    SG_PATH_CUDA_CORE = 1,   /* fp32 FMA stream over the weights, no tensor cores */
+    SG_PATH_TENSOR_CORE = 2, /* tcgen05 with the weight rows on the MMA's M side */
+    SG_PATH_GEMM = 3         /* the general tcgen05 GEMM (plan output only) */
+} sg_path;
+
+/*
+ * gemm_bf16 -- C = A . B^T for any M, N, K (the spec entry point).
+ *
+ * M > 64 runs the persistent tcgen05 GEMM: 128 x 256 output tiles, a TMA-fed
+ * ring of 128-byte-swizzled shared-memory stages, warp-specialised producer /
+ * MMA / epilogue roles, fp32 accumulators in tensor memory, a Stream-K tail
+ * (spark-kernels, "stream-k proper") and a TMA-store epilogue.  M <= 64 is
+ * routed to the skinny path exactly as gemv_bf16 would (spark-kernels, "the
+ * decode kernel": the decode shapes get their own kernel).
+ *
+ * Returns SG_OK or an sg_status code.
+ */
+SG_API int gemm_bf16(const void *A, const void *B, void *C,
+              int64_t M, int64_t N, int64_t K,
+              int64_t lda, int64_t ldb, int64_t ldc, sg_stream_t stream);
+
+/*
+ * gemv_bf16 -- the skinny path, 1 <= M <= 64 (M > 64 or M < 0: SG_ERR_INVALID_ARG).
+ *
+ * Each weight byte of B is read from memory once for all M rows of A
+ * ("The kernels that were there", "The GEMV": the M = 2 kernel loads each weight
+ * once and feeds both rows).  For M <= 8 the kernel is the CUDA-core stream:
+ * 16-byte weight loads coalesced along K, fp32 FMAs, warp-shuffle reductions and
+ * a K split only when there are too few row groups to keep enough bytes in flight
+ * (spark-kernels, "the decode kernel").  For larger M the fp32 FMA rate of the
+ * CUDA cores falls below the weight stream, so the tcgen05 kernel with the weight
+ * rows on the MMA's M side takes over; it reads the weights once as well.
+ */
+SG_API int gemv_bf16(const void *A, const void *B, void *C,
+              int64_t M, int64_t N, int64_t K,
+              int64_t lda, int64_t ldb, int64_t ldc, sg_stream_t stream);
+
+/*
+ * gemv_bf16_path -- gemv_bf16 with the kernel chosen by the caller
+ * (path = SG_PATH_AUTO, SG_PATH_CUDA_CORE or SG_PATH_TENSOR_CORE).  The CUDA-core
+ * kernel holds at most 8 rows of accumulators; larger M is processed in
+ * consecutive launches of 8 rows each.  Same arguments and errors as gemv_bf16;
+ * an unknown path is SG_ERR_INVALID_ARG.
+ */
+SG_API int gemv_bf16_path(const void *A, const void *B, void *C,
+                   int64_t M, int64_t N, int64_t K,
+                   int64_t lda, int64_t ldb, int64_t ldc, int path, sg_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+SG_API const char *sg_status_string(int status);
+
+/* The raw cudaError_t of the most recent SG_ERR_CUDA on this host thread (0 if none). */
+SG_API int sg_last_cuda_error(void);
+
+/*
+ * sg_check_device_errors -- synchronises `stream`, then reads and clears the
+ * current device's kernel error word.  Returns SG_OK, SG_ERR_TIMEOUT (a kernel
+ * gave up on a bounded wait; its output is undefined and the workspace counters
+ * are reset here so later calls are correct), or SG_ERR_CUDA.  If `detail` is not
+ * NULL it receives {code, block, warp, where} of the first recorded error.
+ */
+SG_API int sg_check_device_errors(sg_stream_t stream, uint32_t detail[4]);
+
+/*
+ * sg_set_wait_timeout_ns -- upper bound on any single in-kernel wait (mbarrier
+ * phases).  Default 2e9 ns.  Values below 1e6 are raised to 1e6.  Applies to
+ * launches made after the call, on every device.
+ */
+SG_API void sg_set_wait_timeout_ns(uint64_t ns);
+
+/* --------------------------------------------------------------------------
+ * Planning (host only; no CUDA call is made, usable without a GPU)
+ * -------------------------------------------------------------------------- */
+typedef struct {
+    int32_t path;       /* sg_path the call takes */
+    int32_t tile_m;     /* output rows per tile (MMA M side; weight rows if swapped) */
+    int32_t tile_n;     /* output columns per tile (MMA N side) */
+    int32_t tile_k;     /* K per pipeline stage (64 for tcgen05 paths) */
+    int32_t tiles_m, tiles_n, k_steps;
+    int32_t grid;       /* CTAs launched */
+    int32_t dp_tiles;   /* whole tiles, round-robin over the grid */
+    int32_t sk_tiles;   /* tiles split by Stream-K */
+    int64_t sk_units;   /* sk_tiles * k_steps */
+    int32_t group_m;    /* raster group height */
+    int32_t stages;     /* shared-memory ring depth */
+    int32_t split_k;    /* CUDA-core path: K slices per row group */
+    int32_t rows_per_cta; /* CUDA-core path: weight rows per CTA */
+    double wave_efficiency; /* of one tile per CTA, (ctas/slots)/ceil(ctas/slots) */
+} sg_plan_info;
+
+/*
+ * sg_plan -- the launch plan gemm_bf16 (entry = 0) or gemv_bf16_path (entry = path,
+ * 1 = CUDA core, 2 = tensor core; 0 = the automatic choice) would use for this
+ * shape on a device with `num_sms` SMs.  Returns SG_OK or SG_ERR_INVALID_ARG.
+ */
+SG_API int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
+
+/*
+ * sg_plan_item -- work item `index` of CTA `cta` under a tcgen05 plan from sg_plan:
+ * out = {tile, k0, k1, piece, npieces, slot, sk_index, tile_row, tile_col}.
+ * Returns the CTA's item count, or -1 if cta/index are out of range.
+ */
+SG_API int sg_plan_item(const sg_plan_info *plan, int32_t cta, int32_t index, int32_t out[9]);
+
+/* Wave efficiency (ctas / slots) / ceil(ctas / slots) (UwULLM kernel-dev, budget 4). */
+SG_API double sg_wave_efficiency(int64_t ctas, int64_t slots);
+
+/* --------------------------------------------------------------------------
+ * Roofline microbenchmarks (spark-kernels, "how things are measured": the
+ * card's own peaks are measured, not quoted).  Each runs on `stream`, times
+ * itself with CUDA events and synchronises `stream` before returning.
+ * -------------------------------------------------------------------------- */
+typedef struct {
+    int32_t sm_count;
+    int32_t cc_major, cc_minor;
+    int32_t smem_optin_bytes;   /* max dynamic shared memory per block */
+    int32_t l2_bytes;
+    int64_t global_mem_bytes;
+    int32_t clock_khz;          /* cudaDevAttrClockRate */
+    int32_t mem_clock_khz;
+    int32_t mem_bus_bits;
+} sg_device_info;
+
+/* Device properties of the current device (the pages' rule: query, never hard-code). */
+SG_API int sg_device_query(sg_device_info *out);
+
+/*
+ * sg_bench_tcgen05_peak -- every SM runs one CTA issuing back-to-back
+ * tcgen05.mma.kind::f16 128x256x16 (bf16 in, fp32 accumulate) from operands
+ * resident in shared memory into tensor memory, `iters` MMAs per CTA.
+ * Outputs dense TFLOP/s (2*128*256*16 per MMA) and the SM clock in MHz derived
+ * from clock64 over %globaltimer during the loop.
+ */
+SG_API int sg_bench_tcgen05_peak(int64_t iters, double *tflops, double *sm_mhz, sg_stream_t stream);
+
+/*
+ * sg_bench_copy -- device-to-device cudaMemcpyAsync of `bytes` from src to dst,
+ * `reps` times; *gbps = 2 * bytes / median time (read + write counted).
+ */
+SG_API int sg_bench_copy(void *dst, const void *src, int64_t bytes, int32_t reps, double *gbps, sg_stream_t stream);
+
+/*
+ * sg_bench_read -- a kernel that streams `bytes` (multiple of 16) with 16-byte
+ * loads and reduces them to one word (written to sink, 16 bytes of device memory);
+ * *gbps = bytes / median time over `reps` launches.
+ */
+SG_API int sg_bench_read(const void *src, int64_t bytes, int32_t reps, void *sink, double *gbps, sg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKINNY_GEMM_H */

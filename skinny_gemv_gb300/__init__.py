@@ -1,0 +1,267 @@
+"""Python binding of the GB300 bf16 GEMM / skinny-GEMV C library.
+
+Argument marshalling only: every function here forwards device pointers, sizes
+and the current CUDA stream to ``libskinny_gemm.so`` through ctypes; all of C is
+computed by the library's sm_103a kernels.  PyTorch is used for device memory
+and streams.  If the library has not been built the import of any compute
+function raises -- there is no fallback.
+
+    import torch, skinny_gemv_gb300 as sg
+    C = sg.gemm_bf16(A, B)        # A [M, K], B [N, K] bf16 on cuda -> C [M, N] = A @ B.T
+    C = sg.gemv_bf16(x, W)        # x [M <= 64, K]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from . import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "skinny_gemm.h")
+
+SG_OK = 0
+SG_ERR_INVALID_ARG = 1
+SG_ERR_MISALIGNED = 2
+SG_ERR_UNSUPPORTED_DEVICE = 3
+SG_ERR_CUDA = 4
+SG_ERR_TIMEOUT = 5
+SG_ERR_OUT_OF_MEMORY = 6
+
+PATH_AUTO = 0
+PATH_CUDA_CORE = 1
+PATH_TENSOR_CORE = 2
+PATH_GEMM = 3
+PATH_NAMES = {PATH_AUTO: "auto", PATH_CUDA_CORE: "cuda_core", PATH_TENSOR_CORE: "tensor_core",
+              PATH_GEMM: "gemm"}
+
+
+class SgError(RuntimeError):
+    def __init__(self, status: int, where: str, lib=None):
+        self.status = status
+        msg = lib.sg_status_string(status).decode() if lib is not None else f"status {status}"
+        if status == SG_ERR_CUDA and lib is not None:
+            msg += f" (cudaError {lib.sg_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("tile_k", ctypes.c_int32), ("tiles_m", ctypes.c_int32), ("tiles_n", ctypes.c_int32),
+                ("k_steps", ctypes.c_int32), ("grid", ctypes.c_int32), ("dp_tiles", ctypes.c_int32),
+                ("sk_tiles", ctypes.c_int32), ("sk_units", ctypes.c_int64), ("group_m", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32),
+                ("wave_efficiency", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class DeviceInfo(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int32), ("cc_major", ctypes.c_int32), ("cc_minor", ctypes.c_int32),
+                ("smem_optin_bytes", ctypes.c_int32), ("l2_bytes", ctypes.c_int32),
+                ("global_mem_bytes", ctypes.c_int64), ("clock_khz", ctypes.c_int32),
+                ("mem_clock_khz", ctypes.c_int32), ("mem_bus_bits", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """The loaded ctypes library.  Raises if it is not built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB_PATH):
+        if not build_if_missing:
+            raise RuntimeError(f"CUDA library not built: {_build.LIB_PATH} is missing; "
+                               "run __graft_entry__.build() (nvcc, sm_103a)")
+        _build.build()
+    lib = ctypes.CDLL(_build.LIB_PATH)
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    for name in ("gemm_bf16", "gemv_bf16"):
+        f = getattr(lib, name)
+        f.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, p]
+        f.restype = ctypes.c_int
+    lib.gemv_bf16_path.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
+    lib.gemv_bf16_path.restype = ctypes.c_int
+    lib.sg_status_string.argtypes = [ctypes.c_int]
+    lib.sg_status_string.restype = ctypes.c_char_p
+    lib.sg_last_cuda_error.argtypes = []
+    lib.sg_last_cuda_error.restype = ctypes.c_int
+    lib.sg_check_device_errors.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+    lib.sg_check_device_errors.restype = ctypes.c_int
+    lib.sg_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.sg_set_wait_timeout_ns.restype = None
+    lib.sg_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.sg_plan.restype = ctypes.c_int
+    lib.sg_plan_item.argtypes = [ctypes.POINTER(PlanInfo), i32, i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.sg_plan_item.restype = ctypes.c_int
+    lib.sg_wave_efficiency.argtypes = [i64, i64]
+    lib.sg_wave_efficiency.restype = ctypes.c_double
+    lib.sg_device_query.argtypes = [ctypes.POINTER(DeviceInfo)]
+    lib.sg_device_query.restype = ctypes.c_int
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.sg_bench_tcgen05_peak.argtypes = [i64, dp, dp, p]
+    lib.sg_bench_tcgen05_peak.restype = ctypes.c_int
+    lib.sg_bench_copy.argtypes = [p, p, i64, i32, dp, p]
+    lib.sg_bench_copy.restype = ctypes.c_int
+    lib.sg_bench_read.argtypes = [p, i64, i32, p, dp, p]
+    lib.sg_bench_read.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/skinny_gemm.h."""
+    text = open(HEADER).read()
+    return re.findall(r"^SG_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+
+
+def _check(status: int, where: str) -> None:
+    if status != SG_OK:
+        raise SgError(status, where, load())
+
+
+# ------------------------------------------------------------------ raw pointers
+def gemm_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                  stream: int = 0) -> int:
+    """C-ABI call with raw device pointers; returns the sg_status code."""
+    return load().gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def gemv_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                  stream: int = 0, path: int = PATH_AUTO) -> int:
+    return load().gemv_bf16_path(A, B, C, M, N, K, lda, ldb, ldc, path, stream)
+
+
+# ------------------------------------------------------------------ torch tensors
+def _torch():
+    import torch
+    return torch
+
+
+def _operand(t, name: str):
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_cuda:
+        raise ValueError(f"{name} must be a 2-D bfloat16 CUDA tensor, got {t.dtype} {tuple(t.shape)} {t.device}")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    return t.data_ptr(), max(t.stride(0), t.shape[1])
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _call(fn_name: str, A, B, C=None, stream=None, path: int | None = None):
+    torch = _torch()
+    a_ptr, lda = _operand(A, "A")
+    b_ptr, ldb = _operand(B, "B")
+    M, K = A.shape
+    N, Kb = B.shape
+    if Kb != K:
+        raise ValueError(f"K mismatch: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if C is None:
+        ld = -(-N // 8) * 8  # rows 16-byte aligned, as the library requires
+        C = torch.empty((M, ld), dtype=torch.bfloat16, device=A.device)[:, :N]
+    c_ptr, ldc = _operand(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    s = _stream_handle(stream)
+    lib = load()
+    with torch.cuda.device(A.device):
+        if fn_name == "gemm_bf16":
+            st = lib.gemm_bf16(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc, s)
+        else:
+            st = lib.gemv_bf16_path(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc,
+                                    PATH_AUTO if path is None else path, s)
+    _check(st, fn_name)
+    return C
+
+
+def gemm_bf16(A, B, C=None, stream=None):
+    """C[M, N] = A[M, K] @ B[N, K]^T in bf16 with fp32 accumulation."""
+    return _call("gemm_bf16", A, B, C, stream)
+
+
+def gemv_bf16(A, B, C=None, stream=None, path: int = PATH_AUTO):
+    """The skinny path (1 <= M <= 64); ``path`` picks the kernel (PATH_*)."""
+    return _call("gemv_bf16", A, B, C, stream, path)
+
+
+# ------------------------------------------------------------------ host-only helpers
+def plan(M: int, N: int, K: int, num_sms: int, entry: int = 0) -> dict:
+    info = PlanInfo()
+    _check(load().sg_plan(M, N, K, num_sms, entry, ctypes.byref(info)), "sg_plan")
+    d = info.as_dict()
+    d["_struct"] = info
+    return d
+
+
+def plan_items(info: dict) -> list[list[tuple]]:
+    """All work items of a tcgen05 plan, per CTA: (tile, k0, k1, piece, npieces, slot, sk_index, tm, tn)."""
+    lib = load()
+    out = (ctypes.c_int32 * 9)()
+    st = info["_struct"]
+    items = []
+    for cta in range(info["grid"]):
+        row = []
+        n = lib.sg_plan_item(ctypes.byref(st), cta, 0, out)
+        for i in range(max(n, 0)):
+            lib.sg_plan_item(ctypes.byref(st), cta, i, out)
+            row.append(tuple(out))
+        items.append(row)
+    return items
+
+
+def wave_efficiency(ctas: int, slots: int) -> float:
+    return load().sg_wave_efficiency(ctas, slots)
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load().sg_set_wait_timeout_ns(ns)
+
+
+def check_device_errors(stream=None):
+    """Synchronises the stream; returns (status, detail[4]) of kernel wait timeouts."""
+    detail = (ctypes.c_uint32 * 4)()
+    st = load().sg_check_device_errors(_stream_handle(stream), detail)
+    return st, list(detail)
+
+
+def device_query() -> dict:
+    info = DeviceInfo()
+    _check(load().sg_device_query(ctypes.byref(info)), "sg_device_query")
+    return {name: getattr(info, name) for name, _ in info._fields_}
+
+
+def bench_tcgen05_peak(iters: int, stream=None) -> tuple[float, float]:
+    tf, mhz = ctypes.c_double(), ctypes.c_double()
+    _check(load().sg_bench_tcgen05_peak(iters, ctypes.byref(tf), ctypes.byref(mhz), _stream_handle(stream)),
+           "sg_bench_tcgen05_peak")
+    return tf.value, mhz.value
+
+
+def bench_copy(dst, src, reps: int = 20, stream=None) -> float:
+    g = ctypes.c_double()
+    nbytes = src.numel() * src.element_size()
+    _check(load().sg_bench_copy(dst.data_ptr(), src.data_ptr(), nbytes, reps, ctypes.byref(g),
+                                _stream_handle(stream)), "sg_bench_copy")
+    return g.value
+
+
+def bench_read(src, sink, reps: int = 20, stream=None) -> float:
+    g = ctypes.c_double()
+    nbytes = src.numel() * src.element_size()
+    _check(load().sg_bench_read(src.data_ptr(), nbytes, reps, sink.data_ptr(), ctypes.byref(g),
+                                _stream_handle(stream)), "sg_bench_read")
+    return g.value

@@ -1,0 +1,616 @@
+// Host side of the C ABI declared in include/skinny_gemm.h: argument checks,
+// per-device state (properties, workspace, error word), tensor-map encoding,
+// launch planning and dispatch.  Nothing here computes any part of C: every
+// output element is produced by the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/skinny_gemm.h"
+#include "sg_internal.h"
+#include "sg_ptx.cuh"
+#include "sg_sched.cuh"
+
+namespace sg {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return SG_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------- device state
+constexpr int kMaxDevices = 64;
+constexpr size_t kPartialBytes = size_t(64) << 20;  // Stream-K / split-K fp32 partials
+constexpr size_t kNumCounters = 16384;
+constexpr int kCcRowsPerWarp = 4;
+constexpr int kCcWarps = 8;
+
+struct DeviceState {
+  bool props_ready = false;
+  int sm_count = 0, cc_major = 0, cc_minor = 0, smem_optin = 0, l2_bytes = 0;
+  void* workspace = nullptr;  // [partials | counters | error word]
+  float* partials = nullptr;
+  uint32_t* counters = nullptr;
+  DeviceError* err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+int current_device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return SG_ERR_UNSUPPORTED_DEVICE;
+  DeviceState& d = g_devices[dev];
+  if (!d.props_ready) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d.props_ready) {
+      int v[5];
+      const cudaDeviceAttr attrs[5] = {cudaDevAttrMultiProcessorCount, cudaDevAttrComputeCapabilityMajor,
+                                       cudaDevAttrComputeCapabilityMinor, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                       cudaDevAttrL2CacheSize};
+      for (int i = 0; i < 5; ++i) {
+        e = cudaDeviceGetAttribute(&v[i], attrs[i], dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+      }
+      d.sm_count = v[0];
+      d.cc_major = v[1];
+      d.cc_minor = v[2];
+      d.smem_optin = v[3];
+      d.l2_bytes = v[4];
+      d.props_ready = true;
+    }
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3) return SG_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return SG_OK;
+}
+
+// Allocates the workspace on first use.  Refused while `stream` is capturing.
+int ensure_workspace(DeviceState& d, cudaStream_t stream) {
+  if (d.workspace) return SG_OK;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (d.workspace) return SG_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (cap != cudaStreamCaptureStatusNone) return SG_ERR_INVALID_ARG;
+  const size_t bytes = kPartialBytes + kNumCounters * sizeof(uint32_t) + 256;
+  void* p = nullptr;
+  e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();
+    return SG_ERR_OUT_OF_MEMORY;
+  }
+  uint8_t* base = static_cast<uint8_t*>(p);
+  e = cudaMemsetAsync(base + kPartialBytes, 0, bytes - kPartialBytes, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return cuda_fail(e);
+  }
+  d.partials = reinterpret_cast<float*>(base);
+  d.counters = reinterpret_cast<uint32_t*>(base + kPartialBytes);
+  d.err = reinterpret_cast<DeviceError*>(base + kPartialBytes + kNumCounters * sizeof(uint32_t));
+  d.workspace = p;
+  return SG_OK;
+}
+
+// ----------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  uint64_t cols, rows, ld;
+  uint32_t box_cols, box_rows, swizzle;
+  int dev;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && cols == o.cols && rows == o.rows && ld == o.ld && box_cols == o.box_cols &&
+           box_rows == o.box_rows && swizzle == o.swizzle && dev == o.dev;
+  }
+};
+
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+};
+
+constexpr int kMapCacheSize = 64;
+std::mutex g_map_mutex;
+MapEntry g_map_cache[kMapCacheSize];
+int g_map_used = 0, g_map_next = 0;
+
+// A 2-D bf16 tensor of `rows` rows x `cols` columns with a row pitch of `ld`
+// elements, read or written in boxes of box_rows x box_cols.
+int make_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
+             uint32_t box_cols, CUtensorMapSwizzle swz, int dev) {
+  const MapKey key{ptr, cols, rows, ld, box_cols, box_rows, static_cast<uint32_t>(swz), dev};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int i = 0; i < g_map_used; ++i)
+      if (g_map_cache[i].key == key) {
+        *out = g_map_cache[i].map;
+        return SG_OK;
+      }
+  }
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  *out = m;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  MapEntry& slot = g_map_cache[g_map_used < kMapCacheSize ? g_map_used++ : (g_map_next++ % kMapCacheSize)];
+  slot.key = key;
+  slot.map = m;
+  return SG_OK;
+}
+
+// ----------------------------------------------------------------- planning
+void fill_sched(sg_plan_info* o, const Schedule& s) {
+  o->tiles_m = s.tiles_m;
+  o->tiles_n = s.tiles_n;
+  o->k_steps = s.k_steps;
+  o->grid = s.grid;
+  o->dp_tiles = s.dp_tiles;
+  o->sk_tiles = s.sk_tiles;
+  o->sk_units = s.sk_units;
+  o->group_m = s.group_m;
+}
+
+Schedule sched_from_plan(const sg_plan_info& o) {
+  Schedule s{};
+  s.tiles_m = o.tiles_m;
+  s.tiles_n = o.tiles_n;
+  s.k_steps = o.k_steps;
+  s.grid = o.grid;
+  s.dp_tiles = o.dp_tiles;
+  s.sk_tiles = o.sk_tiles;
+  s.sk_units = o.sk_units;
+  s.group_m = o.group_m;
+  return s;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+  std::memset(o, 0, sizeof *o);
+  o->path = SG_PATH_GEMM;
+  o->tile_m = kBM;
+  o->tile_n = kGemmBN;
+  o->tile_k = kBK;
+  o->stages = kGemmStages;
+  const int32_t tm = static_cast<int32_t>(ceil_div(M, kBM)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN));
+  const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
+  const Schedule s = make_schedule(tm, tn, ks, sms, 4, std::min<int32_t>(tm, 8));
+  fill_sched(o, s);
+  o->split_k = 1;
+  o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, sms);
+}
+
+int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+
+void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+  std::memset(o, 0, sizeof *o);
+  o->path = SG_PATH_TENSOR_CORE;
+  o->tile_m = kBM;
+  o->tile_n = skinny_bn(M);
+  o->tile_k = kBK;
+  o->stages = kSkinnyStages;
+  const int32_t tm = static_cast<int32_t>(ceil_div(N, kBM));
+  const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
+  const Schedule s = make_schedule(tm, 1, ks, sms, 8, 1);
+  fill_sched(o, s);
+  o->split_k = 1;
+  o->wave_efficiency = wave_efficiency(tm, sms);
+}
+
+void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+  std::memset(o, 0, sizeof *o);
+  o->path = SG_PATH_CUDA_CORE;
+  o->rows_per_cta = kCcRowsPerWarp * kCcWarps;
+  o->tile_m = o->rows_per_cta;
+  o->tile_n = static_cast<int32_t>(std::min<int64_t>(M, 8));
+  o->tile_k = 8;
+  const int64_t ctas = ceil_div(N, o->rows_per_cta);
+  int64_t split = 1;
+  if (ctas < 2 * sms && K >= 2048) {
+    split = std::min<int64_t>(ceil_div(2 * sms, ctas), K / 1024);
+    split = std::max<int64_t>(split, 1);
+  }
+  int64_t k_slice = ceil_div(ceil_div(K, split), 8) * 8;
+  if (k_slice < 8) k_slice = 8;
+  split = ceil_div(K, k_slice);
+  if (split < 1) split = 1;
+  const int64_t mrows = std::min<int64_t>(M, 8);
+  if (split > 1 && (static_cast<size_t>(split) * mrows * N * 4 > kPartialBytes ||
+                    static_cast<size_t>(ctas) > kNumCounters)) {
+    split = 1;
+    k_slice = ceil_div(K, 8) * 8;
+  }
+  o->split_k = static_cast<int32_t>(split);
+  o->tiles_m = static_cast<int32_t>(ctas);
+  o->tiles_n = 1;
+  o->k_steps = static_cast<int32_t>(k_slice);  // elements per K slice
+  o->grid = static_cast<int32_t>(ctas * split);
+  o->wave_efficiency = wave_efficiency(o->grid, sms);
+}
+
+int choose_skinny_path(int64_t M) { return M <= 8 ? SG_PATH_CUDA_CORE : SG_PATH_TENSOR_CORE; }
+
+// ----------------------------------------------------------------- validation
+int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+             int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return SG_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return SG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return SG_OK;
+  if (!C || (K > 0 && (!A || !B))) return SG_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldc < N) return SG_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (misaligned(C) || (K > 0 && (misaligned(A) || misaligned(B)))) return SG_ERR_MISALIGNED;
+  if ((lda & 7) || (ldb & 7) || (ldc & 7)) return SG_ERR_MISALIGNED;
+  return SG_OK;
+}
+
+TcParams base_params(DeviceState& d, int64_t M, int64_t N, int64_t K, int64_t ldc, void* C) {
+  TcParams p{};
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.ldc = ldc;
+  p.C = C;
+  p.partials = d.partials;
+  p.counters = d.counters;
+  p.err = d.err;
+  p.timeout_ns = g_timeout_ns.load();
+  return p;
+}
+
+int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
+  sg_plan_info plan;
+  plan_tc_gemm(M, N, K, d.sm_count, &plan);
+  CUtensorMap ta, tb, tc;
+  int st = make_map(&ta, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tb, B, N, K, ldb, kGemmBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, dev);
+  if (st != SG_OK) return st;
+  TcParams p = base_params(d, M, N, K, ldc, C);
+  p.sched = sched_from_plan(plan);
+  cudaError_t e = launch_tc_gemm(ta, tb, tc, p, stream);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
+int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
+  sg_plan_info plan;
+  plan_tc_skinny(M, N, K, d.sm_count, &plan);
+  CUtensorMap tw, tx;
+  int st = make_map(&tw, B, N, K, ldb, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st != SG_OK) return st;
+  TcParams p = base_params(d, M, N, K, ldc, C);
+  p.sched = sched_from_plan(plan);
+  cudaError_t e = launch_tc_skinny(plan.tile_n, tw, tx, p, stream);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
+int run_cc(DeviceState& d, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+           int64_t ldb, int64_t ldc, cudaStream_t stream) {
+  // At most 8 activation rows per launch; larger M runs as consecutive row blocks.
+  for (int64_t m0 = 0; m0 < M; m0 += 8) {
+    const int64_t mb = std::min<int64_t>(8, M - m0);
+    sg_plan_info plan;
+    plan_cc(mb, N, K, d.sm_count, &plan);
+    CcParams p{};
+    p.A = static_cast<const uint16_t*>(A) + m0 * lda;
+    p.B = static_cast<const uint16_t*>(B);
+    p.C = static_cast<uint16_t*>(C) + m0 * ldc;
+    p.M = static_cast<int32_t>(mb);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.lda = lda;
+    p.ldb = ldb;
+    p.ldc = ldc;
+    p.rows_per_cta = plan.rows_per_cta;
+    p.split_k = plan.split_k;
+    p.k_slice = plan.k_steps;
+    p.partials = d.partials;
+    p.counters = d.counters;
+    cudaError_t e = launch_cc_gemv(p, plan.tiles_m, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return SG_OK;
+}
+
+int skinny_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                    int64_t ldb, int64_t ldc, int path, cudaStream_t stream) {
+  DeviceState* d = nullptr;
+  int dev = 0;
+  int st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, stream);
+    return e == cudaSuccess ? SG_OK : cuda_fail(e);
+  }
+  st = ensure_workspace(*d, stream);
+  if (st != SG_OK) return st;
+  if (path == SG_PATH_AUTO) path = choose_skinny_path(M);
+  if (path == SG_PATH_CUDA_CORE) return run_cc(*d, A, B, C, M, N, K, lda, ldb, ldc, stream);
+  return run_tc_skinny(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, stream);
+}
+
+}  // namespace
+}  // namespace sg
+
+using namespace sg;
+
+extern "C" {
+
+int gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              int64_t ldc, sg_stream_t stream) {
+  int st = validate(A, B, C, M, N, K, lda, ldb, ldc);
+  if (st != SG_OK || M == 0 || N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M <= 64) return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, s);
+  DeviceState* d = nullptr;
+  int dev = 0;
+  st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, s);
+    return e == cudaSuccess ? SG_OK : cuda_fail(e);
+  }
+  st = ensure_workspace(*d, s);
+  if (st != SG_OK) return st;
+  return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, s);
+}
+
+int gemv_bf16_path(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                   int64_t ldb, int64_t ldc, int path, sg_stream_t stream) {
+  if (path < SG_PATH_AUTO || path > SG_PATH_TENSOR_CORE) return SG_ERR_INVALID_ARG;
+  if (M > 64) return SG_ERR_INVALID_ARG;
+  int st = validate(A, B, C, M, N, K, lda, ldb, ldc);
+  if (st != SG_OK || M == 0 || N == 0) return st;
+  return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, path, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemv_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              int64_t ldc, sg_stream_t stream) {
+  return gemv_bf16_path(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, stream);
+}
+
+const char* sg_status_string(int status) {
+  switch (status) {
+    case SG_OK: return "SG_OK";
+    case SG_ERR_INVALID_ARG: return "SG_ERR_INVALID_ARG: invalid argument";
+    case SG_ERR_MISALIGNED: return "SG_ERR_MISALIGNED: pointer or leading dimension not 16-byte aligned";
+    case SG_ERR_UNSUPPORTED_DEVICE: return "SG_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3 (sm_103a)";
+    case SG_ERR_CUDA: return "SG_ERR_CUDA: a CUDA call failed (see sg_last_cuda_error)";
+    case SG_ERR_TIMEOUT: return "SG_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    case SG_ERR_OUT_OF_MEMORY: return "SG_ERR_OUT_OF_MEMORY: workspace allocation failed";
+    default: return "unknown sg_status";
+  }
+}
+
+int sg_last_cuda_error(void) { return g_last_cuda_error; }
+
+void sg_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns < 1000000ull ? 1000000ull : ns); }
+
+int sg_check_device_errors(sg_stream_t stream, uint32_t detail[4]) {
+  DeviceState* d = nullptr;
+  int dev = 0;
+  int st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (detail) std::memset(detail, 0, 4 * sizeof(uint32_t));
+  if (!d->workspace) return SG_OK;
+  DeviceError h{};
+  e = cudaMemcpyAsync(&h, d->err, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (h.code == 0) return SG_OK;
+  if (detail) {
+    detail[0] = h.code;
+    detail[1] = h.block;
+    detail[2] = h.role;
+    detail[3] = h.where;
+  }
+  // Clear the error word and every arrival counter an aborted launch may have left.
+  e = cudaMemsetAsync(d->counters, 0, kNumCounters * sizeof(uint32_t) + sizeof(DeviceError), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return SG_ERR_TIMEOUT;
+}
+
+int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info* out) {
+  if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
+  if (entry < 0 || entry > SG_PATH_TENSOR_CORE) return SG_ERR_INVALID_ARG;
+  if (entry == 0 && M > 64) {
+    plan_tc_gemm(M, N, K, num_sms, out);
+    return SG_OK;
+  }
+  if (M > 64) return SG_ERR_INVALID_ARG;
+  const int path = entry == 0 ? choose_skinny_path(M) : entry;
+  if (path == SG_PATH_CUDA_CORE)
+    plan_cc(std::min<int64_t>(std::max<int64_t>(M, 1), 8), N, K, num_sms, out);
+  else
+    plan_tc_skinny(M, N, K, num_sms, out);
+  return SG_OK;
+}
+
+int sg_plan_item(const sg_plan_info* plan, int32_t cta, int32_t index, int32_t out[9]) {
+  if (!plan || !out || plan->path == SG_PATH_CUDA_CORE) return -1;
+  const Schedule s = sched_from_plan(*plan);
+  if (cta < 0 || cta >= s.grid) return -1;
+  const int32_t n = item_count(s, cta);
+  if (index < 0 || index >= n) return -1;
+  const WorkItem w = get_item(s, cta, index);
+  int32_t tm, tn;
+  tile_coords(s, w.tile, tm, tn);
+  const int32_t vals[9] = {w.tile, w.k0, w.k1, w.piece, w.npieces, w.slot, w.sk_index, tm, tn};
+  std::memcpy(out, vals, sizeof vals);
+  return n;
+}
+
+double sg_wave_efficiency(int64_t ctas, int64_t slots) { return wave_efficiency(ctas, slots); }
+
+int sg_device_query(sg_device_info* out) {
+  if (!out) return SG_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int clk = 0, mclk = 0, bus = 0;
+  cudaDeviceGetAttribute(&clk, cudaDevAttrClockRate, dev);
+  cudaDeviceGetAttribute(&mclk, cudaDevAttrMemoryClockRate, dev);
+  cudaDeviceGetAttribute(&bus, cudaDevAttrGlobalMemoryBusWidth, dev);
+  out->sm_count = prop.multiProcessorCount;
+  out->cc_major = prop.major;
+  out->cc_minor = prop.minor;
+  out->smem_optin_bytes = static_cast<int32_t>(prop.sharedMemPerBlockOptin);
+  out->l2_bytes = prop.l2CacheSize;
+  out->global_mem_bytes = static_cast<int64_t>(prop.totalGlobalMem);
+  out->clock_khz = clk;
+  out->mem_clock_khz = mclk;
+  out->mem_bus_bits = bus;
+  return SG_OK;
+}
+
+int sg_bench_tcgen05_peak(int64_t iters, double* tflops, double* sm_mhz, sg_stream_t stream) {
+  if (iters < 16 || !tflops || !sm_mhz) return SG_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  int dev = 0;
+  int st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = ensure_workspace(*d, s);
+  if (st != SG_OK) return st;
+  const int grid = d->sm_count;
+  unsigned long long* buf = nullptr;
+  cudaError_t e = cudaMalloc(&buf, 2 * grid * sizeof(unsigned long long));
+  if (e != cudaSuccess) return cuda_fail(e);
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  e = launch_tc_peak(std::min<int64_t>(iters, 1024), grid, buf, buf + grid, d->err, s);  // warm-up
+  if (e == cudaSuccess) e = cudaEventRecord(e0, s);
+  if (e == cudaSuccess) e = launch_tc_peak(iters, grid, buf, buf + grid, d->err, s);
+  if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  std::vector<unsigned long long> h(2 * grid);
+  if (e == cudaSuccess) e = cudaMemcpy(h.data(), buf, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaFree(buf);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const double flops = 2.0 * kBM * 256 * 16 * static_cast<double>(iters) * grid;
+  *tflops = flops / (ms * 1e-3) / 1e12;
+  double mhz = 0;
+  for (int i = 0; i < grid; ++i) mhz += static_cast<double>(h[i]) / static_cast<double>(h[grid + i]) * 1e3;
+  *sm_mhz = mhz / grid;
+  return SG_OK;
+}
+
+namespace {
+double median_of(std::vector<float>& v) {
+  std::sort(v.begin(), v.end());
+  return v.size() % 2 ? v[v.size() / 2] : 0.5 * (v[v.size() / 2 - 1] + v[v.size() / 2]);
+}
+}  // namespace
+
+int sg_bench_copy(void* dst, const void* src, int64_t bytes, int32_t reps, double* gbps, sg_stream_t stream) {
+  if (!dst || !src || bytes <= 0 || reps < 1 || !gbps) return SG_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  std::vector<float> t;
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);  // warm-up
+  for (int i = 0; i < reps && e == cudaSuccess; ++i) {
+    float ms = 0;
+    e = cudaEventRecord(e0, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    t.push_back(ms);
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *gbps = 2.0 * static_cast<double>(bytes) / (median_of(t) * 1e-3) / 1e9;
+  return SG_OK;
+}
+
+int sg_bench_read(const void* src, int64_t bytes, int32_t reps, void* sink, double* gbps, sg_stream_t stream) {
+  if (!src || !sink || bytes < 16 || (bytes % 16) || reps < 1 || !gbps) return SG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) return SG_ERR_MISALIGNED;
+  DeviceState* d = nullptr;
+  int st = current_device_state(&d, nullptr);
+  if (st != SG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int grid = d->sm_count * 4;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  std::vector<float> t;
+  cudaError_t e = launch_read_stream(src, bytes, sink, grid, s);  // warm-up
+  for (int i = 0; i < reps && e == cudaSuccess; ++i) {
+    float ms = 0;
+    e = cudaEventRecord(e0, s);
+    if (e == cudaSuccess) e = launch_read_stream(src, bytes, sink, grid, s);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    t.push_back(ms);
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *gbps = static_cast<double>(bytes) / (median_of(t) * 1e-3) / 1e9;
+  return SG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,392 @@
+// Persistent tcgen05 GEMM for sm_103a: C[M,N] = A[M,K] . B[N,K]^T, bf16 in,
+// fp32 accumulate in tensor memory, bf16 out.
+//
+// One CTA per SM, 6 warps with fixed roles:
+//   warp 0     TMA producer: per k-step waits for a free ring stage, arms its
+//              `full` barrier with the stage's byte count and issues two tiled
+//              cp.async.bulk.tensor loads (A box 64 x 128, B box 64 x BN, 128-byte
+//              swizzle, zero fill outside the matrices);
+//   warp 1     allocates tensor memory; one thread issues tcgen05.mma
+//              (128 x BN x 16 per instruction, 4 per stage) and commits each stage
+//              back to its `empty` barrier and each finished accumulator to
+//              `tmem_full`;
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, Stream-K partials,
+//              fp32 -> bf16 (round to nearest even), 64-byte-swizzled staging and
+//              TMA stores (clipped at M and N), then release the accumulator.
+// Two accumulators (2 x BN TMEM columns) let the epilogue of one tile overlap the
+// main loop of the next.
+//
+// This is spark-kernels' variant 5 ("the copies were the problem, not the power":
+// a producer warp with cp.async.bulk.tensor boxes, 128-byte swizzle, a full and an
+// empty barrier per stage, no block-wide barrier in the k-loop) on the Stream-K
+// schedule of variant 4 ("stream-k proper"), with the sm_100-class tensor cores:
+// operands go TMA -> shared memory -> tcgen05.mma without a trip through
+// registers, and the accumulator lives in tensor memory instead of registers.
+//
+// The swapped variant (SWAP = true) serves the skinny path: the weights B take
+// the MMA's 128-row M side and the few activation rows of A its N side (16, 32 or
+// 64), so every weight byte is loaded once for all rows; its epilogue writes
+// C[m, n] = D[n, m] with direct coalesced stores.
+#include <cuda_bf16.h>
+
+#include "sg_internal.h"
+#include "sg_ptx.cuh"
+#include "sg_sched.cuh"
+
+namespace sg {
+namespace {
+
+template <int BN, int STAGES, bool SWAP>
+struct TcLayout {
+  static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kStagingBufBytes = 32 * 64;  // 32 rows x 32 bf16
+  static constexpr int kStagingBufs = 2;            // per epilogue warp
+  static constexpr int kAOff = 0;
+  static constexpr int kBOff = STAGES * kABytes;
+  static constexpr int kStagingOff = kBOff + STAGES * kBBytes;
+  static constexpr int kStagingBytes = SWAP ? 0 : kEpiWarps * kStagingBufs * kStagingBufBytes;
+  static constexpr int kBarOff = kStagingOff + kStagingBytes;
+  // full[S], empty[S], tmem_full[2], tmem_empty[2], teardown
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, sk flag
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+  static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
+  static constexpr int kChunk = SWAP ? 16 : 32;  // accumulator columns per tcgen05.ld
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+  static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+template <int BN, int STAGES, bool SWAP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  using L = TcLayout<BN, STAGES, SWAP>;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tmem_full = bars + 2 * STAGES;
+  uint64_t* tmem_empty = bars + 2 * STAGES + 2;
+  uint64_t* teardown = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
+  volatile uint32_t* sk_last = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 8);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const Schedule& sched = p.sched;
+  const int cta = blockIdx.x;
+  const int nitems = item_count(sched, cta);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], L::kEpiWarps);
+    }
+    mbar_init(teardown, 1);
+    *abort_flag = 0;
+    *sk_last = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (!SWAP) tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; i < nitems && ok; ++i) {
+        const WorkItem w = get_item(sched, cta, i);
+        int32_t tm, tn;
+        tile_coords(sched, w.tile, tm, tn);
+        for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
+          const uint32_t s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, abort_flag)) {
+            if (!*abort_flag) record_error(p.err, kDevTimeoutEmpty, s);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+          tma_load_2d(smem + L::kAOff + s * L::kABytes, &tmA, ks * kBK, tm * kBM, &full[s]);
+          tma_load_2d(smem + L::kBOff + s * L::kBBytes, &tmB, ks * kBK, tn * BN, &full[s]);
+        }
+      }
+      if (!ok) {
+        // Unwinding: let the loads already issued land before the CTA exits.
+        const uint32_t inflight = it < STAGES ? it : STAGES;
+        for (uint32_t j = 0; j < inflight; ++j) {
+          const uint32_t jt = it - 1 - j;
+          volatile uint32_t never = 0;
+          mbar_wait(&full[jt % STAGES], (jt / STAGES) & 1u, p.timeout_ns, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; i < nitems && ok; ++i) {
+        const WorkItem w = get_item(sched, cta, i);
+        const uint32_t b = static_cast<uint32_t>(i) & 1u;
+        const uint32_t use = static_cast<uint32_t>(i) >> 1;
+        if (!mbar_wait(&tmem_empty[b], (use & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kDevTimeoutTmemEmpty, i);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * BN;
+        for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
+          const uint32_t s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, p.timeout_ns, abort_flag)) {
+            if (!*abort_flag) record_error(p.err, kDevTimeoutFull, s);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes);
+          const uint32_t b_addr = smem_u32(smem + L::kBOff + s * L::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // +32 bytes per 16 bf16 of K inside the 128-byte swizzle row
+            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
+                        (ks > w.k0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        tc_commit(&tmem_full[b]);  // accumulator b is complete
+      }
+      if (!ok || *abort_flag) {
+        // Unwinding: wait for every MMA issued so far before TMEM is freed.
+        tc_commit(teardown);
+        volatile uint32_t never = 0;
+        if (!mbar_wait(teardown, 0, p.timeout_ns, &never)) record_error(p.err, kDevTimeoutTeardown, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int epi_tid = threadIdx.x - 64;  // 0..127
+    uint32_t store_count = 0;
+    uint8_t* staging = smem + L::kStagingOff + q * L::kStagingBufs * L::kStagingBufBytes;
+
+    // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
+    auto emit_chunk = [&](const float* v, int tm, int tn, int j) {
+      if constexpr (!SWAP) {
+        const int col0 = tn * BN + j * 32;
+        const int row0 = tm * kBM + q * 32;
+        const uint32_t buf = store_count & 1u;
+        if (lane == 0) bulk_wait_group_read<1>();  // buffer `buf` no longer read by TMA
+        __syncwarp();
+        const uint32_t base = smem_u32(staging + buf * L::kStagingBufBytes) + lane * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t phys = static_cast<uint32_t>(c) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+          st_shared_v4(base + phys * 16, pack_bf16x2(v[8 * c + 0], v[8 * c + 1]),
+                       pack_bf16x2(v[8 * c + 2], v[8 * c + 3]), pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                       pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (row0 < p.M && col0 < p.N) tma_store_2d(&tmC, staging + buf * L::kStagingBufBytes, col0, row0);
+          bulk_commit_group();
+        }
+        ++store_count;
+      } else {
+        // D[n][m]: this thread's row is weight row n, columns are activation rows m.
+        const int n = tm * kBM + row;
+        if (n < p.N) {
+          __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C);
+#pragma unroll
+          for (int e = 0; e < L::kChunk; ++e) {
+            const int m = tn * BN + j * L::kChunk + e;
+            if (m < p.M) c[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(v[e]);
+          }
+        }
+      }
+    };
+
+    auto load_chunk = [&](uint32_t taddr, float* v) {
+      if constexpr (L::kChunk == 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+      } else {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(taddr, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+      }
+    };
+
+    constexpr int kChunks = BN / L::kChunk;
+    constexpr int kQuads = L::kChunk / 4;
+    for (int i = 0; i < nitems; ++i) {
+      const WorkItem w = get_item(sched, cta, i);
+      int32_t tm, tn;
+      tile_coords(sched, w.tile, tm, tn);
+      const uint32_t b = static_cast<uint32_t>(i) & 1u;
+      const uint32_t use = static_cast<uint32_t>(i) >> 1;
+      if (!mbar_wait(&tmem_full[b], use & 1u, p.timeout_ns, abort_flag)) {
+        if (!*abort_flag) record_error(p.err, kDevTimeoutTmemFull, i);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + lane_off + b * BN;
+      float v[L::kChunk];
+      if (w.npieces == 1) {
+        for (int j = 0; j < kChunks; ++j) {
+          load_chunk(tacc + j * L::kChunk, v);
+          emit_chunk(v, tm, tn, j);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[b]);
+      } else {
+        // Stream-K piece: publish this piece's fp32 partial, then count arrivals.
+        float4* slot = reinterpret_cast<float4*>(p.partials + static_cast<int64_t>(w.slot) * kBM * BN);
+        for (int j = 0; j < kChunks; ++j) {
+          load_chunk(tacc + j * L::kChunk, v);
+#pragma unroll
+          for (int q4 = 0; q4 < kQuads; ++q4)
+            slot[(j * kQuads + q4) * kBM + row] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[b]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (epi_tid == 0) {
+          const uint32_t before = atomicAdd(&p.counters[w.sk_index], 1u);
+          *sk_last = (before == static_cast<uint32_t>(w.npieces - 1)) ? 1u : 0u;
+        }
+        named_bar_sync(1, 128);
+        if (*sk_last) {
+          // Last arrival: sum all pieces in k order, then store.
+          __threadfence();
+          for (int j = 0; j < kChunks; ++j) {
+            float acc[L::kChunk];
+            for (int pj = 0; pj < w.npieces; ++pj) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  p.partials + static_cast<int64_t>(piece_slot(sched, w.sk_index, pj)) * kBM * BN);
+#pragma unroll
+              for (int q4 = 0; q4 < kQuads; ++q4) {
+                const float4 x = __ldcg(&src[(j * kQuads + q4) * kBM + row]);
+                if (pj == 0) {
+                  acc[4 * q4] = x.x; acc[4 * q4 + 1] = x.y; acc[4 * q4 + 2] = x.z; acc[4 * q4 + 3] = x.w;
+                } else {
+                  acc[4 * q4] += x.x; acc[4 * q4 + 1] += x.y; acc[4 * q4 + 2] += x.z; acc[4 * q4 + 3] += x.w;
+                }
+              }
+            }
+            emit_chunk(acc, tm, tn, j);
+          }
+          if (epi_tid == 0) atomicExch(&p.counters[w.sk_index], 0u);
+        }
+      }
+    }
+    if constexpr (!SWAP) {
+      if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+template <int BN, int STAGES, bool SWAP>
+cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
+                           cudaStream_t stream) {
+  using L = TcLayout<BN, STAGES, SWAP>;
+  auto kern = tc_gemm_kernel<BN, STAGES, SWAP>;
+  static bool configured = false;  // the attribute is per function, process-wide
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<p.sched.grid, kTcThreads, L::kAlloc, stream>>>(a, b, c, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_smem_bytes(int bn, bool swapped) {
+  if (!swapped) return TcLayout<kGemmBN, kGemmStages, false>::kAlloc;
+  switch (bn) {
+    case 16: return TcLayout<16, kSkinnyStages, true>::kAlloc;
+    case 32: return TcLayout<32, kSkinnyStages, true>::kAlloc;
+    default: return TcLayout<64, kSkinnyStages, true>::kAlloc;
+  }
+}
+
+cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                           const TcParams& p, cudaStream_t stream) {
+  return launch_variant<kGemmBN, kGemmStages, false>(tmA, tmB, tmC, p, stream);
+}
+
+cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
+                             cudaStream_t stream) {
+  switch (bn) {
+    case 16: return launch_variant<16, kSkinnyStages, true>(tmW, tmX, tmX, p, stream);
+    case 32: return launch_variant<32, kSkinnyStages, true>(tmW, tmX, tmX, p, stream);
+    case 64: return launch_variant<64, kSkinnyStages, true>(tmW, tmX, tmX, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sg

@@ -1,0 +1,67 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sg_sched.cuh"
+
+namespace sg {
+
+struct DeviceError;
+
+constexpr int kBM = 128;  // MMA M (tile rows; weight rows on the swapped path)
+constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
+constexpr int kGemmBN = 256;
+constexpr int kGemmStages = 4;
+constexpr int kSkinnyStages = 8;
+constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+
+// Everything a tcgen05 launch needs besides its tensor maps.
+struct TcParams {
+  int32_t M, N, K;       // C is M x N (output terms)
+  int64_t ldc;           // elements
+  void* C;               // used by the swapped epilogue's direct stores
+  Schedule sched;
+  float* partials;       // Stream-K slots, 2 * grid of them
+  uint32_t* counters;    // one arrival counter per Stream-K tile
+  DeviceError* err;
+  uint64_t timeout_ns;
+};
+
+// Non-swapped GEMM: A-operand = A (rows M), B-operand = B (rows N), BN = 256.
+cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                           const TcParams& p, cudaStream_t stream);
+
+// Swapped skinny GEMM: A-operand = weights B (rows N), B-operand = activations A
+// (rows M <= bn), bn in {16, 32, 64}.
+cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
+                             cudaStream_t stream);
+
+// Shared-memory bytes a launch of each variant needs (for the plan and checks).
+int tc_smem_bytes(int bn, bool swapped);
+
+// CUDA-core skinny kernel.
+struct CcParams {
+  const uint16_t* A;
+  const uint16_t* B;
+  uint16_t* C;
+  int32_t M, N, K;
+  int64_t lda, ldb, ldc;
+  int32_t rows_per_cta;  // weight rows per CTA (warps * rows per warp)
+  int32_t split_k;       // K slices; > 1 uses the partial/counter fixup
+  int32_t k_slice;       // k elements per slice (multiple of 8)
+  float* partials;       // split_k * M * N fp32 when split_k > 1
+  uint32_t* counters;    // one per CTA row group
+};
+
+cudaError_t launch_cc_gemv(const CcParams& p, int grid_rows, cudaStream_t stream);
+
+// Microbenchmark kernels.
+cudaError_t launch_tc_peak(int64_t iters, int grid, unsigned long long* cycles, unsigned long long* ns,
+                           DeviceError* err, cudaStream_t stream);
+cudaError_t launch_read_stream(const void* src, int64_t bytes, void* sink, int grid, cudaStream_t stream);
+
+}  // namespace sg

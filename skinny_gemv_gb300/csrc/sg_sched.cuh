@@ -1,0 +1,176 @@
+// Persistent tile schedule with a Stream-K tail (host + device).
+//
+// The output is cut into tiles_m x tiles_n tiles; each tile needs k_steps steps of
+// BK = 64 along K.  A persistent grid of `grid` CTAs (one per SM) walks:
+//
+//   1. data-parallel tiles [0, dp_tiles): CTA c takes tiles c, c + grid, ...
+//      (whole tiles, no partial sums);
+//   2. Stream-K tiles [dp_tiles, dp_tiles + sk_tiles): their flattened
+//      (tile, k-step) space of sk_units = sk_tiles * k_steps units is cut into
+//      `grid` contiguous ranges, range c = [c*U/grid, (c+1)*U/grid).
+//
+// This is the schedule of spark-kernels, "stream-k proper": a resident grid, the
+// last waves' (tile, k-step) space cut into equal contiguous ranges so that no CTA
+// idles at the end, and (UwULLM kernel-dev, budget 4) wave efficiency
+// (ctas/SMs)/ceil(ctas/SMs) as the quantity it repairs.
+//
+// A tile covered by more than one range is finished by whichever of its pieces
+// arrives last (an arrival counter per tile); that piece sums every piece's fp32
+// partial in increasing k order, so the result does not depend on timing.  The
+// counter is reset by the finishing piece, so nothing is cleared between launches.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define SG_HD __host__ __device__ __forceinline__
+#else
+#define SG_HD inline
+#endif
+
+namespace sg {
+
+struct Schedule {
+  int32_t tiles_m;   // tiles along the output rows (MMA M side)
+  int32_t tiles_n;   // tiles along the output columns (MMA N side)
+  int32_t k_steps;   // ceil(K / 64)
+  int32_t grid;      // persistent CTAs launched
+  int32_t dp_tiles;  // whole tiles handed out round-robin
+  int32_t sk_tiles;  // tiles split by Stream-K
+  int64_t sk_units;  // sk_tiles * k_steps
+  int32_t group_m;   // raster group height in tiles (L2 locality)
+  int32_t pad;
+};
+
+struct WorkItem {
+  int32_t tile;      // linear tile index in raster order
+  int32_t k0, k1;    // k-step range [k0, k1) of this piece
+  int32_t piece;     // index of this piece among the tile's pieces (k order)
+  int32_t npieces;   // 1 = whole tile
+  int32_t slot;      // partial-sum slot of this piece (2*cta + which)
+  int32_t sk_index;  // tile index inside the Stream-K region (arrival counter)
+};
+
+SG_HD int64_t sk_range_begin(const Schedule& s, int64_t c) { return (c * s.sk_units) / s.grid; }
+
+// The CTA whose range holds Stream-K unit u: the largest c with begin(c) <= u.
+SG_HD int64_t sk_owner(const Schedule& s, int64_t u) {
+  return ((u + 1) * s.grid + s.sk_units - 1) / s.sk_units - 1;
+}
+
+// Slot of CTA c's piece of SK tile t: 0 if the piece is the first item of c's
+// range (the range starts inside tile t), else 1.
+SG_HD int32_t sk_slot(const Schedule& s, int64_t c, int64_t t) {
+  const int64_t first_tile = sk_range_begin(s, c) / s.k_steps;
+  return static_cast<int32_t>(2 * c + (first_tile == t ? 0 : 1));
+}
+
+SG_HD int32_t dp_count(const Schedule& s, int32_t c) {
+  return c < s.dp_tiles ? (s.dp_tiles - 1 - c) / s.grid + 1 : 0;
+}
+
+// Number of work items of CTA c.
+SG_HD int32_t item_count(const Schedule& s, int32_t c) {
+  int32_t n = dp_count(s, c);
+  if (s.sk_tiles > 0) {
+    const int64_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
+    if (u1 > u0) n += static_cast<int32_t>((u1 - 1) / s.k_steps - u0 / s.k_steps + 1);
+  }
+  return n;
+}
+
+// The i-th work item of CTA c (0 <= i < item_count(s, c)).
+SG_HD WorkItem get_item(const Schedule& s, int32_t c, int32_t i) {
+  WorkItem w;
+  const int32_t ndp = dp_count(s, c);
+  if (i < ndp) {
+    w.tile = c + i * s.grid;
+    w.k0 = 0;
+    w.k1 = s.k_steps;
+    w.piece = 0;
+    w.npieces = 1;
+    w.slot = -1;
+    w.sk_index = -1;
+    return w;
+  }
+  const int64_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
+  const int64_t t = u0 / s.k_steps + (i - ndp);
+  const int64_t tb = t * s.k_steps, te = tb + s.k_steps;
+  w.tile = static_cast<int32_t>(s.dp_tiles + t);
+  w.k0 = static_cast<int32_t>((u0 > tb ? u0 : tb) - tb);
+  w.k1 = static_cast<int32_t>((u1 < te ? u1 : te) - tb);
+  const int64_t first = sk_owner(s, tb), last = sk_owner(s, te - 1);
+  w.piece = static_cast<int32_t>(c - first);
+  w.npieces = static_cast<int32_t>(last - first + 1);
+  w.slot = w.npieces > 1 ? sk_slot(s, c, t) : -1;
+  w.sk_index = static_cast<int32_t>(t);
+  return w;
+}
+
+// Slot of piece j of Stream-K tile t (t counted inside the Stream-K region).
+SG_HD int32_t piece_slot(const Schedule& s, int64_t t, int32_t j) {
+  const int64_t c = sk_owner(s, t * s.k_steps) + j;
+  return sk_slot(s, c, t);
+}
+
+// Grouped raster order: groups of group_m tile-rows, column-major inside a group,
+// so the tiles in flight share A rows and B columns in L2.
+SG_HD void tile_coords(const Schedule& s, int32_t tile, int32_t& tm, int32_t& tn) {
+  const int32_t per_group = s.group_m * s.tiles_n;
+  const int32_t g = tile / per_group;
+  const int32_t first_m = g * s.group_m;
+  const int32_t rows = (s.tiles_m - first_m) < s.group_m ? (s.tiles_m - first_m) : s.group_m;
+  const int32_t r = tile - g * per_group;
+  tm = first_m + r % rows;
+  tn = r / rows;
+}
+
+// Wave efficiency (UwULLM kernel-dev, budget 4): (ctas / slots) / ceil(ctas / slots).
+SG_HD double wave_efficiency(int64_t ctas, int64_t slots) {
+  if (ctas <= 0 || slots <= 0) return 0.0;
+  const int64_t waves = (ctas + slots - 1) / slots;
+  return static_cast<double>(ctas) / static_cast<double>(slots) / static_cast<double>(waves);
+}
+
+// Builds the schedule.  min_units_per_cta bounds how thinly a tile may be split
+// (a piece's fp32 partial costs about as much as a few k-steps of loads).
+inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps, int32_t num_ctas,
+                              int32_t min_units_per_cta, int32_t group_m) {
+  Schedule s{};
+  s.tiles_m = tiles_m;
+  s.tiles_n = tiles_n;
+  s.k_steps = k_steps;
+  s.group_m = group_m < 1 ? 1 : group_m;
+  const int64_t T = static_cast<int64_t>(tiles_m) * tiles_n;
+  const int64_t G = num_ctas < 1 ? 1 : num_ctas;
+  if (T >= G) {
+    const int64_t rem = T % G;
+    s.grid = static_cast<int32_t>(G);
+    if (rem == 0 || k_steps < 2) {
+      s.dp_tiles = static_cast<int32_t>(T);
+      s.sk_tiles = 0;
+    } else {
+      // Stream-K over the last full wave plus the remainder: 1 < waves < 2.
+      s.sk_tiles = static_cast<int32_t>(rem + G);
+      s.dp_tiles = static_cast<int32_t>(T - s.sk_tiles);
+    }
+  } else {
+    // Fewer tiles than CTAs: every tile is split along K.
+    const int64_t units = T * k_steps;
+    const int64_t per = min_units_per_cta < 1 ? 1 : min_units_per_cta;
+    int64_t g = units / per;
+    if (g > G) g = G;
+    if (g < T) g = T;
+    s.grid = static_cast<int32_t>(g);
+    s.dp_tiles = 0;
+    s.sk_tiles = static_cast<int32_t>(T);
+    if (g == T) {  // one CTA per tile: plain data-parallel
+      s.dp_tiles = static_cast<int32_t>(T);
+      s.sk_tiles = 0;
+    }
+  }
+  s.sk_units = static_cast<int64_t>(s.sk_tiles) * k_steps;
+  return s;
+}
+
+}  // namespace sg

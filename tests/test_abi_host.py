@@ -1,0 +1,196 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every symbol
+the header declares, rejects bad arguments before touching CUDA, and its launch
+planner produces schedules that cover every (tile, k-step) exactly once."""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+import skinny_gemv_gb300 as sg
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sg._build.build()
+    return sg.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = sg.declared_symbols()
+    assert len(names) >= 14
+    for n in ["gemm_bf16", "gemv_bf16", "gemv_bf16_path", "sg_status_string", "sg_last_cuda_error",
+              "sg_check_device_errors", "sg_plan", "sg_bench_tcgen05_peak", "sg_bench_copy",
+              "sg_bench_read", "sg_device_query"]:
+        assert n in names
+    exported = set()
+    import subprocess
+    out = subprocess.check_output(["nm", "-D", "--defined-only", sg.library_path()]).decode()
+    for line in out.splitlines():
+        parts = line.split()
+        if len(parts) == 3 and parts[1] == "T":
+            exported.add(parts[2])
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.sg_status_string(code).decode()
+        assert s.startswith("SG_")
+    assert lib.sg_status_string(99).decode() == "unknown sg_status"
+
+
+@pytest.mark.parametrize("args,code", [
+    # (A, B, C, M, N, K, lda, ldb, ldc)
+    ((16, 16, 16, -1, 8, 8, 8, 8, 8), sg.SG_ERR_INVALID_ARG),
+    ((16, 16, 16, 8, -1, 8, 8, 8, 8), sg.SG_ERR_INVALID_ARG),
+    ((16, 16, 16, 8, 8, -8, 8, 8, 8), sg.SG_ERR_INVALID_ARG),
+    ((0, 16, 16, 8, 8, 8, 8, 8, 8), sg.SG_ERR_INVALID_ARG),       # null A
+    ((16, 0, 16, 8, 8, 8, 8, 8, 8), sg.SG_ERR_INVALID_ARG),       # null B
+    ((16, 16, 0, 8, 8, 8, 8, 8, 8), sg.SG_ERR_INVALID_ARG),       # null C
+    ((16, 16, 16, 8, 8, 16, 8, 16, 8), sg.SG_ERR_INVALID_ARG),    # lda < K
+    ((16, 16, 16, 8, 8, 16, 16, 8, 8), sg.SG_ERR_INVALID_ARG),    # ldb < K
+    ((16, 16, 16, 8, 16, 8, 8, 8, 8), sg.SG_ERR_INVALID_ARG),     # ldc < N
+    ((18, 16, 16, 8, 8, 8, 8, 8, 8), sg.SG_ERR_MISALIGNED),       # A not 16-B aligned
+    ((16, 24, 16, 8, 8, 8, 8, 8, 8), sg.SG_ERR_MISALIGNED),       # B not 16-B aligned
+    ((16, 16, 16, 8, 8, 12, 12, 16, 8), sg.SG_ERR_MISALIGNED),    # lda % 8
+    ((16, 16, 16, 8, 8, 8, 8, 8, 12), sg.SG_ERR_MISALIGNED),      # ldc % 8
+])
+def test_argument_errors_before_any_cuda_call(lib, args, code):
+    assert lib.gemm_bf16(*args, None) == code
+    assert lib.gemv_bf16(*args, None) == code
+
+
+def test_empty_problems_are_noops(lib):
+    # M = 0 or N = 0: nothing to do, no CUDA call, even with null pointers
+    assert lib.gemm_bf16(None, None, None, 0, 8, 8, 8, 8, 8, None) == sg.SG_OK
+    assert lib.gemm_bf16(None, None, None, 8, 0, 8, 8, 8, 8, None) == sg.SG_OK
+    assert lib.gemv_bf16(None, None, None, 0, 8, 8, 8, 8, 8, None) == sg.SG_OK
+
+
+def test_gemv_rejects_large_m_and_bad_path(lib):
+    assert lib.gemv_bf16(16, 16, 16, 65, 8, 8, 8, 8, 8, None) == sg.SG_ERR_INVALID_ARG
+    assert lib.gemv_bf16_path(16, 16, 16, 4, 8, 8, 8, 8, 8, 7, None) == sg.SG_ERR_INVALID_ARG
+
+
+def _golden_rows(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split(None, 4))
+    return rows
+
+
+def test_wave_efficiency_matches_printed_values(lib):
+    rows = _golden_rows("wave_efficiency.txt")
+    assert len(rows) >= 5
+    for ctas, slots, want, tol, *_ in rows:
+        got = sg.wave_efficiency(int(ctas), int(slots))
+        assert abs(got - float(want)) <= float(tol), (ctas, slots, got, want)
+    # the two-factor product the page prints: 86.1% x 95.7% = 82.4%
+    assert abs(sg.wave_efficiency(1024, 170) * 0.957 - 0.824) < 0.001
+
+
+def test_waves_of_the_rtx5090_example():
+    for tiles, slots, waves in (r[:3] for r in _golden_rows("waves.txt")):
+        assert round(int(tiles) / int(slots), 2) == float(waves)
+    # tiles of a 4096^2 output in 128 x 128 tiles
+    assert (4096 // 128) ** 2 == 1024
+
+
+def _check_plan_coverage(info):
+    items = sg.plan_items(info)
+    T = info["tiles_m"] * info["tiles_n"]
+    KS = info["k_steps"]
+    cover = np.zeros((T, KS), dtype=np.int32)
+    pieces = {}
+    for cta, row in enumerate(items):
+        assert len(row) >= 1, f"CTA {cta} has no work"
+        first_sk = sum(1 for it in row if it[0] < info["dp_tiles"])
+        for idx, (tile, k0, k1, piece, npieces, slot, sk, tm, tn) in enumerate(row):
+            assert 0 <= tile < T and 0 <= k0 < k1 <= KS
+            assert 0 <= tm < info["tiles_m"] and 0 <= tn < info["tiles_n"]
+            cover[tile, k0:k1] += 1
+            if npieces > 1:
+                assert slot in (2 * cta, 2 * cta + 1)
+                # slot 0 of a CTA is its first Stream-K item, slot 1 its last
+                assert (slot == 2 * cta) == (idx == first_sk)
+                assert idx in (first_sk, len(row) - 1)
+                pieces.setdefault(tile, []).append((k0, k1, piece, npieces, cta, slot))
+            else:
+                assert (k0, k1) == (0, KS) and slot == -1
+    assert np.all(cover == 1), "every (tile, k-step) exactly once"
+    # (tile row, tile col) is a bijection of tile indices
+    coords = {(it[7], it[8]) for row in items for it in row}
+    assert len(coords) == T
+    for tile, ps in pieces.items():
+        ps.sort()
+        n = ps[0][3]
+        assert len(ps) == n and [p[2] for p in ps] == list(range(n))
+        assert ps[0][0] == 0 and ps[-1][1] == KS
+        assert all(ps[i][1] == ps[i + 1][0] for i in range(n - 1))
+        assert [p[4] for p in ps] == list(range(ps[0][4], ps[0][4] + n)), "consecutive CTAs"
+        assert len({p[5] for p in ps}) == n
+    return items
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (2048, 2048, 2048), (512, 512, 512),
+                                   (4096, 11008, 4096), (4096, 4096, 11008), (8192, 8192, 8192),
+                                   (65, 257, 4104), (1000, 3000, 200), (129, 8, 64)])
+@pytest.mark.parametrize("sms", [148, 152, 170])
+def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms):
+    info = sg.plan(M, N, K, sms, 0)
+    assert info["path"] == sg.PATH_GEMM
+    assert info["tile_m"] == 128 and info["tile_n"] == 256 and info["tile_k"] == 64
+    assert info["tiles_m"] == -(-M // 128) and info["tiles_n"] == -(-N // 256)
+    assert info["grid"] <= sms
+    T = info["tiles_m"] * info["tiles_n"]
+    assert info["dp_tiles"] + info["sk_tiles"] == T
+    if T >= sms and T % sms:
+        assert sms < info["sk_tiles"] < 2 * sms  # Stream-K over one wave plus the remainder
+    _check_plan_coverage(info)
+
+
+@pytest.mark.parametrize("M", [1, 2, 9, 16, 17, 33, 64])
+@pytest.mark.parametrize("N,K", [(11008, 4096), (4096, 11008), (300, 700), (128, 64)])
+def test_skinny_tensor_core_plan(lib, M, N, K):
+    info = sg.plan(M, N, K, 152, sg.PATH_TENSOR_CORE)
+    assert info["path"] == sg.PATH_TENSOR_CORE
+    assert info["tile_n"] == (16 if M <= 16 else 32 if M <= 32 else 64)
+    assert info["tiles_n"] == 1 and info["tiles_m"] == -(-N // 128)
+    items = _check_plan_coverage(info)
+    # the weights are read once: each weight tile's k-steps are covered exactly once
+    assert sum(k1 - k0 for row in items for (_, k0, k1, *_) in row) == info["tiles_m"] * info["k_steps"]
+
+
+def test_auto_path_choice(lib):
+    assert sg.plan(2, 4096, 4096, 152, 0)["path"] == sg.PATH_CUDA_CORE
+    assert sg.plan(8, 4096, 4096, 152, 0)["path"] == sg.PATH_CUDA_CORE
+    assert sg.plan(9, 4096, 4096, 152, 0)["path"] == sg.PATH_TENSOR_CORE
+    assert sg.plan(64, 4096, 4096, 152, 0)["path"] == sg.PATH_TENSOR_CORE
+    assert sg.plan(65, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM
+
+
+@pytest.mark.parametrize("N,K", [(11008, 4096), (4096, 11008), (256, 8192), (100, 24)])
+def test_cuda_core_plan(lib, N, K):
+    info = sg.plan(2, N, K, 152, sg.PATH_CUDA_CORE)
+    assert info["rows_per_cta"] == 32
+    assert info["tiles_m"] == -(-N // 32)
+    k_slice = info["k_steps"]
+    assert k_slice % 8 == 0 and info["split_k"] == -(-K // k_slice)
+    assert info["grid"] == info["tiles_m"] * info["split_k"]
+    if info["tiles_m"] >= 2 * 152:
+        assert info["split_k"] == 1
+
+
+def test_plan_rejects_bad_arguments(lib):
+    out = sg.PlanInfo()
+    assert lib.sg_plan(-1, 8, 8, 152, 0, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
+    assert lib.sg_plan(8, 8, 8, 0, 0, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
+    assert lib.sg_plan(65, 8, 8, 152, sg.PATH_CUDA_CORE, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
