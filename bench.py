@@ -1,0 +1,540 @@
+#!/usr/bin/env python3
+"""Benchmark of the bf16 GEMM library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+One step is one gemm_bf16 call on the headline workload: C = A . B^T with
+M = N = K = 4096, A and B uniform[-1, 1] rounded to bf16 from the seeded
+generator (fp32 accumulation, bf16 output).  The timed region runs exactly K
+steps back to back on one stream, inputs already resident in HBM; the inputs
+rotate over enough copies (each at its own address) that the working set is
+several times the L2, so no step reads its operands from L2 left by the one
+before.  The JSON line (printed by rank 0) carries:
+
+  value / ms_per_step  whole-job TFLOP/s (2*M*N*K per step, all ranks) over the
+                       max-over-ranks time of the K steps
+  roofline             the GEMM kernel's achieved TFLOP/s (mean CUDA-event
+                       duration of its launches) against the measured bf16 peak
+  e2e                  the same metric with host buffers: each step copies A and
+                       B from pinned host memory, calls gemm_bf16 and copies C back
+  cpu_baseline         the fp64 oracle on a bounded row sample, on the host cores
+  rows                 the other workloads (2048^3, the 7B MLP projections,
+                       8192^3, the decode shapes M = 1, 2, 16, 64) and the
+                       measured tcgen05 peak / copy / read roofs
+  clocks               nvidia-smi SM clock samples taken during the timed region
+
+--impl reference times the oracle itself (the reference arm): each step is the
+fp64 oracle on a 64-row sample of the same 4096^3 workload, on the host cores.
+
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU:
+the problem does not need to be sharded, and no data moves between ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TFLOPS and % of measured tcgen05 peak; decode GB/s and % of HBM roof (1×GB300)"
+HEADLINE = "sq4096"
+REF_ROWS_PER_STEP = 64
+CPU_SAMPLE_ROWS = 2048
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def tflops(M: int, N: int, K: int, seconds: float) -> float:
+    """Dense throughput with the requested dims: 2*M*N*K / time (gemm3 benchmarks page,
+    "Throughput and precision")."""
+    return 2.0 * M * N * K / seconds / 1e12
+
+
+def decode_bytes(M: int, N: int, K: int) -> int:
+    """Bytes a skinny GEMM must move once: bf16 weights, activations and output."""
+    return 2 * (N * K + M * K + M * N)
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group("gloo")
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    """Max of a float over all ranks (control plane only; gloo)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str | None, interval_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", str(interval_ms)]
+        if device_id:
+            self.cmd += ["-i", device_id]
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)  # let the first samples arrive
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self) -> dict:
+        sms, maxes, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms), "power_w_max": max(power) if power else None}
+
+
+def device_id_for_smi(torch, dev: int) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "skinny_gemv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(PROFILES, "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}:{workload}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def host_bits_to_device(torch, bits, device):
+    import numpy as np
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def copies(t, n: int):
+    return [t] + [t.clone() for _ in range(n - 1)]
+
+
+def rotation_count(bytes_per_set: int, l2: int) -> int:
+    """Input sets needed so that the rotation spans at least four L2 capacities."""
+    return max(2, math.ceil(4 * l2 / max(bytes_per_set, 1)) + 1)
+
+
+def time_launches(torch, stream, fns, steps: int, warmup: int):
+    """Runs fns[i % len(fns)] for warmup + steps; returns (total_ms, per-launch ms list)
+    of the timed steps, with CUDA events on `stream`."""
+    for i in range(warmup):
+        fns[i % len(fns)]()
+    stream.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        fns[(warmup + i) % len(fns)]()
+        ends[i].record(stream)
+    t1.record(stream)
+    t1.synchronize()
+    return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+# ---------------------------------------------------------------- the reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import synthetic as syn
+    import oracle
+    w = syn.WORKLOADS[HEADLINE]
+    A = w.a()
+    B = w.b()
+    threads = oracle.default_threads()
+    rows_per = REF_ROWS_PER_STEP
+    used = threads
+
+    def step(i):
+        nonlocal used
+        r0 = (i * rows_per) % w.M
+        _, used = oracle.gemm(A[r0:r0 + rows_per], B, threads=threads, return_threads=True)
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t
+    value = tflops(rows_per, w.N, w.K, dt / args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded uniform[-1,1] -> bf16)",
+        "config": {"workload": f"{HEADLINE}: bf16 GEMM C[4096,4096] = A[4096,4096] . B[4096,4096]^T",
+                   "sample": f"{rows_per} rows of C per step (all 4096 columns, full K)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": used, "kind": "oracle",
+                         "sample": f"{rows_per} x 4096 outputs of the 4096^3 GEMM per step, fp64"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import skinny_gemv_gb300 as sg
+    import synthetic as syn
+
+    dist = init_dist(world)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    sg.load()
+    info = sg.device_query()
+    l2 = info["l2_bytes"]
+    peaks = measured_peaks()
+    stream = torch.cuda.Stream(device)
+    w = syn.WORKLOADS[HEADLINE]
+    M, N, K = w.M, w.N, w.K
+
+    with torch.cuda.stream(stream):
+        A0 = host_bits_to_device(torch, w.a(), device)
+        B0 = host_bits_to_device(torch, w.b(), device)
+        nrot = rotation_count(A0.numel() * 2 + B0.numel() * 2, l2)
+        As, Bs = copies(A0, nrot), copies(B0, nrot)
+        Cs = [torch.empty((M, N), dtype=torch.bfloat16, device=device) for _ in range(nrot)]
+    stream.synchronize()
+    fns = [(lambda a=a, b=b, c=c: sg.gemm_bf16(a, b, c, stream=stream)) for a, b, c in zip(As, Bs, Cs)]
+
+    check = None
+    if not args.no_check:
+        check = sanity_gate(torch, sg, w, As[0], Bs[0], Cs[0], stream)
+
+    sampler = ClockSampler(device_id_for_smi(torch, local))
+    barrier(dist)
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        fns[i % nrot]()
+    torch.cuda.synchronize()
+    barrier(dist)
+    with sampler:
+        torch.cuda.synchronize()
+        total_ms, per_launch = time_launches(torch, stream, fns, args.steps, 0)
+        torch.cuda.synchronize()
+    barrier(dist)
+    total_ms = max_over_ranks(dist, total_ms)
+    st, detail = sg.check_device_errors(stream)
+    if st != sg.SG_OK:
+        raise RuntimeError(f"device error {st} {detail}")
+
+    value = tflops(M, N, K, total_ms / 1e3 / args.steps) * world
+    kernel_ms = statistics.fmean(per_launch)
+    achieved = tflops(M, N, K, kernel_ms / 1e3)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(torch, sg, w, A0, B0, stream, args, dist, world)
+
+    rows = []
+    micro = {}
+    cpu = None
+    if rank == 0 and not args.quick:
+        rows = measure_rows(torch, sg, syn, stream, l2, peaks, args)
+        micro = measure_micro(torch, sg, stream)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(syn, w)
+
+    if rank != 0:
+        return 0
+    plan = sg.plan(M, N, K, info["sm_count"], 0)
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded splitmix64 uniform[-1,1] rounded to bf16)",
+        "config": {
+            "workload": f"{HEADLINE}: bf16 GEMM C[4096,4096] = A[4096,4096] . B[4096,4096]^T, fp32 accumulate, bf16 out",
+            "M": M, "N": N, "K": K, "accumulate": "f32",
+            "l2": f"inputs larger than L2: {nrot} rotating copies of A, B, C "
+                  f"({nrot * 3 * M * K * 2 / 2**20:.0f} MiB vs {l2 / 2**20:.0f} MiB L2), no flush",
+            "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}", "grid": plan["grid"],
+            "dp_tiles": plan["dp_tiles"], "sk_tiles": plan["sk_tiles"],
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "roofline": {
+            "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": recorded_traffic("tc_gemm_kernel", HEADLINE),
+            "kernel": "tc_gemm_kernel<256,4,false>", "kernel_ms": kernel_ms,
+            "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peaks['source']}, burst: cuBLAS 8192^3)",
+            "algorithmic": f"2*M*N*K = {2 * M * N * K / 1e9:.1f} GFLOP per launch",
+        },
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": sampler.summary(),
+        "gpu_launches": args.steps,
+        "correctness": check,
+        "rows": rows,
+        "microbench": micro,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def sanity_gate(torch, sg, w, A, B, C, stream):
+    """Guards the timing against a broken build: 256 sampled rows of the headline
+    output must agree with an fp32 matmul of the same rows on the device, within
+    the parity tests' tolerance.  (Parity proper is the test suite's job.)"""
+    sg.gemm_bf16(A, B, C, stream=stream)
+    stream.synchronize()
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1)
+    rows = torch.randperm(w.M, generator=g)[:256].to(A.device)
+    ref = (A[rows].float() @ B.float().t()).double()
+    got = C[rows].double()
+    diff = (got - ref).abs()
+    bound = 1e-2 * ref.abs() + 2e-3 * math.sqrt(w.K)
+    n_over = int((diff > bound).sum().item())
+    rel_fro = float(torch.linalg.norm(got - ref) / torch.linalg.norm(ref))
+    if n_over or rel_fro > 4e-3 or not torch.isfinite(got).all():
+        raise RuntimeError(f"headline output fails the sanity gate: n_over={n_over} rel_fro={rel_fro}")
+    return {"vs": "device fp32 matmul, 256 sampled rows", "max_abs": float(diff.max().item()),
+            "rel_fro": rel_fro, "n_over": n_over}
+
+
+def measure_e2e(torch, sg, w, A0, B0, stream, args, dist, world):
+    """Host buffers in, host buffer out: per step H2D of A and B from pinned memory,
+    gemm_bf16, D2H of C into pinned memory."""
+    M, N, K = w.M, w.N, w.K
+    hA = A0.cpu().pin_memory()
+    hB = B0.cpu().pin_memory()
+    hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    dA = torch.empty_like(A0)
+    dB = torch.empty_like(B0)
+    dC = torch.empty((M, N), dtype=torch.bfloat16, device=A0.device)
+
+    def step():
+        with torch.cuda.stream(stream):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            sg.gemm_bf16(dA, dB, dC, stream=stream)
+            hC.copy_(dC, non_blocking=True)
+
+    steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        step()
+    stream.synchronize()
+    barrier(dist)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    t1.synchronize()
+    ms = max_over_ranks(dist, t0.elapsed_time(t1)) / steps
+    return {"value": tflops(M, N, K, ms / 1e3) * world, "unit": "TFLOPS", "ms_per_step": ms,
+            "steps": steps, "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N}
+
+
+def measure_rows(torch, sg, syn, stream, l2, peaks, args):
+    """Other workloads of the pages, timed the same way (inputs rotated past L2).
+    Inputs are drawn on the device from seeded generators with the workloads'
+    distributions; the parity tests check these shapes on the host generator's inputs."""
+    out = []
+    gen = torch.Generator(device=stream.device)
+    steps = 20 if args.quick else 50
+
+    def draw(rows, cols, dist, seed):
+        gen.manual_seed(seed)
+        if dist == "uniform":
+            t = torch.rand((rows, cols), generator=gen, device=stream.device, dtype=torch.float32) * 2 - 1
+        else:
+            sigma = float(dist.split(":")[1])
+            t = torch.randn((rows, cols), generator=gen, device=stream.device, dtype=torch.float32) * sigma
+        return t.to(torch.bfloat16)
+
+    names = ["sq2048", "mlp_up", "mlp_down", "sq8192"] + [n for n in syn.WORKLOADS if n.startswith("dec")]
+    for name in names:
+        w = syn.WORKLOADS[name]
+        with torch.cuda.stream(stream):
+            A = draw(w.M, w.K, w.dist_a, w.seed_a)
+            B = draw(w.N, w.K, w.dist_b, w.seed_b)
+            per_set = 2 * (w.M * w.K + w.N * w.K)
+            nrot = rotation_count(per_set, l2)
+            As = copies(A, nrot) if w.M > 64 else [A] * nrot
+            Bs = copies(B, nrot)
+            C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=stream.device)
+        stream.synchronize()
+        paths = [("gemm_bf16", None)]
+        if w.M <= 64:
+            paths = [("gemm_bf16", None), ("gemv_bf16/cuda_core", sg.PATH_CUDA_CORE),
+                     ("gemv_bf16/tensor_core", sg.PATH_TENSOR_CORE)]
+        for label, path in paths:
+            if path is None:
+                fns = [(lambda a=a, b=b: sg.gemm_bf16(a, b, C, stream=stream)) for a, b in zip(As, Bs)]
+            else:
+                fns = [(lambda a=a, b=b, p=path: sg.gemv_bf16(a, b, C, stream=stream, path=p))
+                       for a, b in zip(As, Bs)]
+            total, per = time_launches(torch, stream, fns, steps, 5)
+            med = statistics.median(per)
+            row = {"workload": name, "entry": label, "M": w.M, "N": w.N, "K": w.K,
+                   "us_median": med * 1e3, "us_back_to_back": total / steps * 1e3}
+            if w.M > 64:
+                row["tflops"] = tflops(w.M, w.N, w.K, med / 1e3)
+                row["frac_of_peak"] = row["tflops"] / peaks["bf16_tflops"]
+            else:
+                gbs = decode_bytes(w.M, w.N, w.K) / (med / 1e3) / 1e9
+                row["gbs"] = gbs
+                row["frac_of_hbm"] = gbs / peaks["hbm_gbs"]
+                row["gbs_back_to_back"] = decode_bytes(w.M, w.N, w.K) / (total / steps / 1e3) / 1e9
+            out.append(row)
+        del As, Bs, A, B, C
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_micro(torch, sg, stream):
+    tf, mhz = sg.bench_tcgen05_peak(4_000_000, stream=stream)
+    n = 1 << 31
+    src = torch.ones(n, dtype=torch.uint8, device=stream.device)
+    dst = torch.empty_like(src)
+    sink = torch.zeros(4, dtype=torch.int32, device=stream.device)
+    copy = sg.bench_copy(dst, src, reps=10, stream=stream)
+    read = sg.bench_read(src, sink, reps=10, stream=stream)
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"tcgen05_peak_tflops": tf, "tcgen05_peak_sm_mhz": mhz, "copy_gbs": copy, "read_gbs": read}
+
+
+def cpu_baseline(syn, w):
+    import oracle
+    A = w.a()[:CPU_SAMPLE_ROWS]
+    B = w.b()
+    t = time.perf_counter()
+    _, used = oracle.gemm(A, B, return_threads=True)
+    dt = time.perf_counter() - t
+    return {"value": tflops(CPU_SAMPLE_ROWS, w.N, w.K, dt), "unit": "TFLOPS", "cores": used, "kind": "oracle",
+            "sample": f"first {CPU_SAMPLE_ROWS} of 4096 rows of the 4096^3 GEMM (fp64), {dt:.1f} s"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline only: skip the extra rows and microbenchmarks")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-check", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
