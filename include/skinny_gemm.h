@@ -114,6 +114,39 @@ SG_API int gemv_bf16_path(const void *A, const void *B, void *C,
                    int64_t M, int64_t N, int64_t K,
                    int64_t lda, int64_t ldb, int64_t ldc, int path, sg_stream_t stream);
 
+/*
+ * gemv_bf16_noalloc -- gemv_bf16 on the CUDA-core kernel (SG_PATH_CUDA_CORE),
+ * for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this entry point exists for integration, not for the method.
+ *
+ * Who needs it: gemv_bf16 allocates its split-K workspace with cudaMalloc on
+ * the first call.  Some callers cannot allow that: an engine whose device memory
+ * belongs to its own pool allocator (where a raw cudaMalloc fails or fragments
+ * the pool), a plug-in inside a host framework that forbids raw allocations, or
+ * code that must not pay the implicit device synchronisation of cudaMalloc.
+ * This call makes no cudaMalloc, cudaFree or other allocating call.  Its scratch
+ * (split-K fp32 partial sums and arrival counters) is a fixed array in the
+ * library's device image, SG_NOALLOC_PARTIAL_BYTES + 4 * SG_NOALLOC_COUNTERS
+ * bytes, which every GPU that loads the library holds until the process exits.
+ *
+ * Arguments, layout and errors are those of gemv_bf16 (1 <= M <= 64; results
+ * equal gemv_bf16_path(..., SG_PATH_CUDA_CORE, ...)).  A call whose K split would
+ * need more partial sums or counters than the array holds returns
+ * SG_ERR_INVALID_ARG before launching anything.
+ *
+ * The first call on each device looks up the array's device address (it must be
+ * made with that device current), so make that first call before any stream
+ * capture.  Every call shares the one array and finds the previous call's
+ * contents in it; each call clears the counters it uses before its kernel runs.
+ * Calls whose kernels overlap on the GPU (different streams, or different host
+ * threads) race on the array and may return wrong results: serialise them.
+ */
+#define SG_NOALLOC_PARTIAL_BYTES (1u << 20)
+#define SG_NOALLOC_COUNTERS 4096u
+SG_API int gemv_bf16_noalloc(const void *A, const void *B, void *C,
+                             int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc, sg_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 SG_API const char *sg_status_string(int status);
 

@@ -84,7 +84,7 @@ def load(build_if_missing: bool = False):
         _build.build()
     lib = ctypes.CDLL(_build.LIB_PATH)
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
-    for name in ("gemm_bf16", "gemv_bf16"):
+    for name in ("gemm_bf16", "gemv_bf16", "gemv_bf16_noalloc"):
         f = getattr(lib, name)
         f.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, p]
         f.restype = ctypes.c_int
@@ -181,6 +181,8 @@ def _call(fn_name: str, A, B, C=None, stream=None, path: int | None = None):
     with torch.cuda.device(A.device):
         if fn_name == "gemm_bf16":
             st = lib.gemm_bf16(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc, s)
+        elif fn_name == "gemv_bf16_noalloc":
+            st = lib.gemv_bf16_noalloc(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc, s)
         else:
             st = lib.gemv_bf16_path(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc,
                                     PATH_AUTO if path is None else path, s)
@@ -196,6 +198,12 @@ def gemm_bf16(A, B, C=None, stream=None):
 def gemv_bf16(A, B, C=None, stream=None, path: int = PATH_AUTO):
     """The skinny path (1 <= M <= 64); ``path`` picks the kernel (PATH_*)."""
     return _call("gemv_bf16", A, B, C, stream, path)
+
+
+def gemv_bf16_noalloc(A, B, C=None, stream=None):
+    """The CUDA-core skinny path with its scratch in the library's fixed device
+    array instead of an allocated workspace (for callers that cannot allocate)."""
+    return _call("gemv_bf16_noalloc", A, B, C, stream)
 
 
 # ------------------------------------------------------------------ host-only helpers

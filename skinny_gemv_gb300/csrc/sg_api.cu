@@ -376,6 +376,9 @@ int skinny_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N,
 }
 
 }  // namespace
+
+void set_last_cuda_error(int e) { g_last_cuda_error = e; }
+
 }  // namespace sg
 
 using namespace sg;

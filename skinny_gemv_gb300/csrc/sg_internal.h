@@ -59,6 +59,9 @@ struct CcParams {
 
 cudaError_t launch_cc_gemv(const CcParams& p, int grid_rows, cudaStream_t stream);
 
+// Records a CUDA error for sg_last_cuda_error() (this host thread).
+void set_last_cuda_error(int e);
+
 // Microbenchmark kernels.
 cudaError_t launch_tc_peak(int64_t iters, int grid, unsigned long long* cycles, unsigned long long* ns,
                            DeviceError* err, cudaStream_t stream);

@@ -36,6 +36,10 @@ def test_exports_every_declared_symbol(lib):
     assert not missing, missing
     for n in names:
         assert hasattr(lib, n)
+        # every entry point has a full ctypes prototype: without one, ctypes would
+        # pass 64-bit pointers and sizes as 32-bit ints
+        assert getattr(lib, n).argtypes is not None, f"{n} has no argtypes"
+        assert getattr(lib, n).restype is not None or n == "sg_set_wait_timeout_ns", n
 
 
 def test_status_strings(lib):
