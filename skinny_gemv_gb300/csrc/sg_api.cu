@@ -32,8 +32,7 @@ int cuda_fail(cudaError_t e) {
 constexpr int kMaxDevices = 64;
 constexpr size_t kPartialBytes = size_t(64) << 20;  // Stream-K / split-K fp32 partials
 constexpr size_t kNumCounters = 16384;
-constexpr int kCcRowsPerWarp = 4;
-constexpr int kCcWarps = 8;
+constexpr int64_t kCcMaxRowsPerCta = 256;
 
 struct DeviceState {
   bool props_ready = false;
@@ -217,7 +216,7 @@ void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   o->stages = kGemmStages;
   const int32_t tm = static_cast<int32_t>(ceil_div(M, kBM)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN));
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
-  const Schedule s = make_schedule(tm, tn, ks, sms, 4, std::min<int32_t>(tm, 8));
+  const Schedule s = make_schedule(tm, tn, ks, sms, 4, std::min<int32_t>(tm, 8), false);
   fill_sched(o, s);
   o->split_k = 1;
   o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, sms);
@@ -230,45 +229,47 @@ void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   o->path = SG_PATH_TENSOR_CORE;
   o->tile_m = kBM;
   o->tile_n = skinny_bn(M);
-  o->tile_k = kBK;
-  o->stages = kSkinnyStages;
+  o->tile_k = kBK * kSkinnyKsub;
+  o->stages = skinny_stages(o->tile_n);
   const int32_t tm = static_cast<int32_t>(ceil_div(N, kBM));
-  const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
-  const Schedule s = make_schedule(tm, 1, ks, sms, 8, 1);
+  const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK * kSkinnyKsub));
+  const Schedule s = make_schedule(tm, 1, ks, sms, 2, 1, true);
   fill_sched(o, s);
   o->split_k = 1;
   o->wave_efficiency = wave_efficiency(tm, sms);
 }
 
+// CUDA-core plan: two CTAs per SM, each owning a contiguous block of weight rows
+// (at most kCcMaxRowsPerCta); K is split across CTAs only when there are fewer
+// row blocks than that.
 void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
   o->path = SG_PATH_CUDA_CORE;
-  o->rows_per_cta = kCcRowsPerWarp * kCcWarps;
-  o->tile_m = o->rows_per_cta;
-  o->tile_n = static_cast<int32_t>(std::min<int64_t>(M, 8));
-  o->tile_k = 8;
-  const int64_t ctas = ceil_div(N, o->rows_per_cta);
+  const int64_t target = 2 * static_cast<int64_t>(sms);
+  int64_t rows_grid = std::min<int64_t>(N, target);
+  rows_grid = std::max<int64_t>(rows_grid, ceil_div(N, kCcMaxRowsPerCta));
   int64_t split = 1;
-  if (ctas < 2 * sms && K >= 2048) {
-    split = std::min<int64_t>(ceil_div(2 * sms, ctas), K / 1024);
-    split = std::max<int64_t>(split, 1);
-  }
+  if (rows_grid < target && K >= 2048) split = std::max<int64_t>(1, std::min<int64_t>(ceil_div(target, rows_grid), K / 1024));
   int64_t k_slice = ceil_div(ceil_div(K, split), 8) * 8;
   if (k_slice < 8) k_slice = 8;
   split = ceil_div(K, k_slice);
   if (split < 1) split = 1;
   const int64_t mrows = std::min<int64_t>(M, 8);
   if (split > 1 && (static_cast<size_t>(split) * mrows * N * 4 > kPartialBytes ||
-                    static_cast<size_t>(ctas) > kNumCounters)) {
+                    static_cast<size_t>(rows_grid) > kNumCounters)) {
     split = 1;
     k_slice = ceil_div(K, 8) * 8;
   }
+  o->rows_per_cta = static_cast<int32_t>(ceil_div(N, rows_grid));
+  o->tile_m = o->rows_per_cta;
+  o->tile_n = static_cast<int32_t>(mrows);
+  o->tile_k = 8;
   o->split_k = static_cast<int32_t>(split);
-  o->tiles_m = static_cast<int32_t>(ctas);
+  o->tiles_m = static_cast<int32_t>(rows_grid);
   o->tiles_n = 1;
   o->k_steps = static_cast<int32_t>(k_slice);  // elements per K slice
-  o->grid = static_cast<int32_t>(ctas * split);
-  o->wave_efficiency = wave_efficiency(o->grid, sms);
+  o->grid = static_cast<int32_t>(rows_grid * split);
+  o->wave_efficiency = wave_efficiency(o->grid, 2 * static_cast<int64_t>(sms));
 }
 
 int choose_skinny_path(int64_t M) { return M <= 8 ? SG_PATH_CUDA_CORE : SG_PATH_TENSOR_CORE; }
@@ -347,12 +348,12 @@ int run_cc(DeviceState& d, const void* A, const void* B, void* C, int64_t M, int
     p.lda = lda;
     p.ldb = ldb;
     p.ldc = ldc;
-    p.rows_per_cta = plan.rows_per_cta;
+    p.grid_rows = plan.tiles_m;
     p.split_k = plan.split_k;
     p.k_slice = plan.k_steps;
     p.partials = d.partials;
     p.counters = d.counters;
-    cudaError_t e = launch_cc_gemv(p, plan.tiles_m, stream);
+    cudaError_t e = launch_cc_gemv(p, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return SG_OK;

@@ -36,10 +36,13 @@
 namespace sg {
 namespace {
 
-template <int BN, int STAGES, bool SWAP>
+// KSUB: consecutive 64-wide k boxes per pipeline stage (one schedule k-step).
+template <int BN, int STAGES, bool SWAP, int KSUB>
 struct TcLayout {
-  static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kASub = kBM * kBK * 2;  // 16 KB: one 128 x 64 box
+  static constexpr int kBSub = BN * kBK * 2;
+  static constexpr int kABytes = KSUB * kASub;
+  static constexpr int kBBytes = KSUB * kBSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiWarps = 4;
   static constexpr int kStagingBufBytes = 32 * 64;  // 32 rows x 32 bf16
@@ -74,11 +77,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, int KSUB>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using L = TcLayout<BN, STAGES, SWAP>;
+  using L = TcLayout<BN, STAGES, SWAP, KSUB>;
+  const int kboxes = (p.K + kBK - 1) / kBK;  // 64-wide k boxes that hold data
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -145,9 +149,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], L::kStageBytes);
-          tma_load_2d(smem + L::kAOff + s * L::kABytes, &tmA, ks * kBK, tm * kBM, &full[s]);
-          tma_load_2d(smem + L::kBOff + s * L::kBBytes, &tmB, ks * kBK, tn * BN, &full[s]);
+          const int nsub = min(KSUB, kboxes - ks * KSUB);  // boxes past K are skipped
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nsub * (L::kASub + L::kBSub)));
+          for (int j = 0; j < nsub; ++j) {
+            const int kx = (ks * KSUB + j) * kBK;
+            tma_load_2d(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, tm * kBM, &full[s]);
+            tma_load_2d(smem + L::kBOff + s * L::kBBytes + j * L::kBSub, &tmB, kx, tn * BN, &full[s]);
+          }
         }
       }
       if (!ok) {
@@ -186,13 +194,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes);
-          const uint32_t b_addr = smem_u32(smem + L::kBOff + s * L::kBBytes);
+          const int nsub = min(KSUB, kboxes - ks * KSUB);
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes + j * L::kASub);
+            const uint32_t b_addr = smem_u32(smem + L::kBOff + s * L::kBBytes + j * L::kBSub);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // +32 bytes per 16 bf16 of K inside the 128-byte swizzle row
-            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
-                        (ks > w.k0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // +32 bytes per 16 bf16 of K inside the 128-byte swizzle row
+              tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
+                          (ks > w.k0 || j > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -276,7 +287,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tile_coords(sched, w.tile, tm, tn);
       const uint32_t b = static_cast<uint32_t>(i) & 1u;
       const uint32_t use = static_cast<uint32_t>(i) >> 1;
-      if (!mbar_wait(&tmem_full[b], use & 1u, p.timeout_ns, abort_flag)) {
+      // An accumulator is ready after its k-steps have run: allow 20 us per k-step
+      // on top of the base bound (a k-step normally takes about 0.3 us).
+      const uint64_t limit = p.timeout_ns + static_cast<uint64_t>(w.k1 - w.k0) * 20000ull;
+      if (!mbar_wait(&tmem_full[b], use & 1u, limit, abort_flag)) {
         if (!*abort_flag) record_error(p.err, kDevTimeoutTmemFull, i);
         *abort_flag = 1;
         break;
@@ -316,16 +330,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __threadfence();
           for (int j = 0; j < kChunks; ++j) {
             float acc[L::kChunk];
-            for (int pj = 0; pj < w.npieces; ++pj) {
-              const float4* src = reinterpret_cast<const float4*>(
+            // Two pieces per batch: 2 x kQuads independent loads in flight.
+            for (int pj = 0; pj < w.npieces; pj += 2) {
+              const bool pair = pj + 1 < w.npieces;
+              const float4* s0 = reinterpret_cast<const float4*>(
                   p.partials + static_cast<int64_t>(piece_slot(sched, w.sk_index, pj)) * kBM * BN);
+              const float4* s1 = reinterpret_cast<const float4*>(
+                  p.partials + static_cast<int64_t>(piece_slot(sched, w.sk_index, pair ? pj + 1 : pj)) * kBM * BN);
+              float4 x0[kQuads], x1[kQuads];
+#pragma unroll
+              for (int q4 = 0; q4 < kQuads; ++q4) x0[q4] = __ldcg(&s0[(j * kQuads + q4) * kBM + row]);
+              if (pair) {
+#pragma unroll
+                for (int q4 = 0; q4 < kQuads; ++q4) x1[q4] = __ldcg(&s1[(j * kQuads + q4) * kBM + row]);
+              }
 #pragma unroll
               for (int q4 = 0; q4 < kQuads; ++q4) {
-                const float4 x = __ldcg(&src[(j * kQuads + q4) * kBM + row]);
+                float* a4 = &acc[4 * q4];
                 if (pj == 0) {
-                  acc[4 * q4] = x.x; acc[4 * q4 + 1] = x.y; acc[4 * q4 + 2] = x.z; acc[4 * q4 + 3] = x.w;
+                  a4[0] = x0[q4].x; a4[1] = x0[q4].y; a4[2] = x0[q4].z; a4[3] = x0[q4].w;
                 } else {
-                  acc[4 * q4] += x.x; acc[4 * q4 + 1] += x.y; acc[4 * q4 + 2] += x.z; acc[4 * q4 + 3] += x.w;
+                  a4[0] += x0[q4].x; a4[1] += x0[q4].y; a4[2] += x0[q4].z; a4[3] += x0[q4].w;
+                }
+                if (pair) {  // k order: piece pj, then pj + 1
+                  a4[0] += x1[q4].x; a4[1] += x1[q4].y; a4[2] += x1[q4].z; a4[3] += x1[q4].w;
                 }
               }
             }
@@ -348,11 +376,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, int KSUB>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
                            cudaStream_t stream) {
-  using L = TcLayout<BN, STAGES, SWAP>;
-  auto kern = tc_gemm_kernel<BN, STAGES, SWAP>;
+  using L = TcLayout<BN, STAGES, SWAP, KSUB>;
+  auto kern = tc_gemm_kernel<BN, STAGES, SWAP, KSUB>;
   static bool configured = false;  // the attribute is per function, process-wide
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
@@ -366,25 +394,25 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
 }  // namespace
 
 int tc_smem_bytes(int bn, bool swapped) {
-  if (!swapped) return TcLayout<kGemmBN, kGemmStages, false>::kAlloc;
+  if (!swapped) return TcLayout<kGemmBN, kGemmStages, false, 1>::kAlloc;
   switch (bn) {
-    case 16: return TcLayout<16, kSkinnyStages, true>::kAlloc;
-    case 32: return TcLayout<32, kSkinnyStages, true>::kAlloc;
-    default: return TcLayout<64, kSkinnyStages, true>::kAlloc;
+    case 16: return TcLayout<16, skinny_stages(16), true, kSkinnyKsub>::kAlloc;
+    case 32: return TcLayout<32, skinny_stages(32), true, kSkinnyKsub>::kAlloc;
+    default: return TcLayout<64, skinny_stages(64), true, kSkinnyKsub>::kAlloc;
   }
 }
 
 cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const TcParams& p, cudaStream_t stream) {
-  return launch_variant<kGemmBN, kGemmStages, false>(tmA, tmB, tmC, p, stream);
+  return launch_variant<kGemmBN, kGemmStages, false, 1>(tmA, tmB, tmC, p, stream);
 }
 
 cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
                              cudaStream_t stream) {
   switch (bn) {
-    case 16: return launch_variant<16, kSkinnyStages, true>(tmW, tmX, tmX, p, stream);
-    case 32: return launch_variant<32, kSkinnyStages, true>(tmW, tmX, tmX, p, stream);
-    case 64: return launch_variant<64, kSkinnyStages, true>(tmW, tmX, tmX, p, stream);
+    case 16: return launch_variant<16, skinny_stages(16), true, kSkinnyKsub>(tmW, tmX, tmX, p, stream);
+    case 32: return launch_variant<32, skinny_stages(32), true, kSkinnyKsub>(tmW, tmX, tmX, p, stream);
+    case 64: return launch_variant<64, skinny_stages(64), true, kSkinnyKsub>(tmW, tmX, tmX, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,21 +1,25 @@
 // CUDA-core skinny GEMM (decode GEMV) for M <= 8 activation rows.
 //
-// C[m, n] = sum_k A[m, k] B[n, k]: each warp owns R consecutive weight rows n and
-// streams them along K with 16-byte (8 x bf16) loads, adjacent lanes on adjacent
-// 16-byte vectors so one warp instruction reads 512 contiguous bytes of a row.
-// Every loaded weight vector is multiplied against all M activation rows before
-// the next one is loaded, so each weight byte crosses the memory bus once
-// ("The kernels that were there", "The GEMV": parallel over output columns, warps
-// stride K with adjacent threads on adjacent weights, 128-bit loads, fp32
-// accumulation, bf16 store; the M = 2 kernel feeds both rows from one load).
-// Per-lane fp32 partials are combined with warp shuffles.
+// C[m, n] = sum_k A[m, k] B[n, k].  The grid is grid_rows x split_k CTAs.  CTA
+// (b, s) owns the contiguous weight rows [b*N/grid_rows, (b+1)*N/grid_rows), so
+// every CTA streams one contiguous block of B, and K slice s.  Inside the CTA the 8
+// warps split the slice along K; each warp walks the CTA's rows R at a time with
+// 16-byte (8 x bf16) non-caching loads, adjacent lanes on adjacent 16-byte vectors
+// (512 contiguous bytes per row per warp instruction).  Every loaded weight vector
+// is multiplied against all M activation rows before the next is loaded, so each
+// weight byte crosses the memory bus once ("The kernels that were there", "The
+// GEMV": parallel over output columns, warps stride K with adjacent threads on
+// adjacent weights, 128-bit loads, fp32 accumulation, bf16 store; the M = 2
+// kernel feeds both rows from one load).  Lane partials are combined with warp
+// shuffles, and the 8 warps' partials are summed in warp order through shared
+// memory, so the result does not depend on timing.
 //
-// When there are too few row groups to keep enough bytes in flight, K is cut
-// into split_k slices (blockIdx.y).  Each slice writes fp32 partials; the last
-// slice of a row group to finish (an arrival counter) sums the slices in slice
-// order, stores bf16 and resets the counter, so the result is the same every
-// run and nothing needs clearing between calls (spark-kernels, "the decode
-// kernel": split K only when the strips are too few, and keep it to one launch).
+// When there are too few rows to give every SM two CTAs, K is also split across
+// CTAs (split_k > 1).  Each slice writes fp32 partials, and the last slice of a
+// row block to finish (an arrival counter) sums the slices in slice order, stores
+// bf16 and resets the counter.  Nothing needs clearing between calls, and a call
+// is one launch (spark-kernels, "the decode kernel": split K only when the strips
+// are too few).
 #include <cuda_bf16.h>
 
 #include "sg_internal.h"
@@ -24,7 +28,6 @@ namespace sg {
 namespace {
 
 constexpr int kCcWarps = 8;
-constexpr int kCcUnroll = 4;
 
 __device__ __forceinline__ uint4 ld_stream_v4(const uint16_t* p) {
   uint4 v;
@@ -45,64 +48,68 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
-template <int MT, int R>
-__global__ void __launch_bounds__(kCcWarps * 32) cc_gemv_kernel(const CcParams p) {
+// MT: activation rows held (>= M); R: weight rows per warp pass; U: 16-byte
+// vectors per lane per row in flight.
+template <int MT, int R, int U>
+__global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParams p) {
+  extern __shared__ float red[];  // [rows of this CTA][MT][kCcWarps]
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int n0 = blockIdx.x * p.rows_per_cta + warp * R;
+  const int row_lo = static_cast<int>((static_cast<int64_t>(blockIdx.x) * p.N) / p.grid_rows);
+  const int row_hi = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * p.N) / p.grid_rows);
   const int slice = blockIdx.y;
   const int kb = slice * p.k_slice;
   const int ke = min(p.K, kb + p.k_slice);
-  const int kvec_end = kb + ((max(ke - kb, 0)) / 8) * 8;
+  const int nvec = max(ke - kb, 0) / 8;  // whole 16-byte vectors in this slice
+  const int v_lo = kb / 8 + (warp * nvec) / kCcWarps;
+  const int v_hi = kb / 8 + ((warp + 1) * nvec) / kCcWarps;
+  const int tail_k = kb + nvec * 8;  // [tail_k, ke): fewer than 8 elements, warp 0
 
-  float acc[R][MT];
+  for (int r0 = row_lo; r0 < row_hi; r0 += R) {
+    float acc[R][MT];
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
-
-  bool row_ok[R];
-  const uint16_t* brow[R];
+      for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+    const uint16_t* brow[R];
+    bool row_ok[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    row_ok[r] = (n0 + r) < p.N;
-    brow[r] = p.B + static_cast<int64_t>(row_ok[r] ? n0 + r : 0) * p.ldb;
-  }
-
-  for (int k = kb + lane * 8; k < kvec_end; k += 32 * 8 * kCcUnroll) {
-    uint4 wv[kCcUnroll][R];
-#pragma unroll
-    for (int u = 0; u < kCcUnroll; ++u) {
-      const int kk = k + u * 256;
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-        wv[u][r] = (kk < kvec_end && row_ok[r]) ? ld_stream_v4(brow[r] + kk) : make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < R; ++r) {
+      row_ok[r] = r0 + r < row_hi;
+      brow[r] = p.B + static_cast<int64_t>(row_ok[r] ? r0 + r : r0) * p.ldb;
     }
+    for (int v = v_lo + lane; v < v_hi; v += 32 * U) {
+      uint4 wv[U][R];
 #pragma unroll
-    for (int u = 0; u < kCcUnroll; ++u) {
-      const int kk = k + u * 256;
-      if (kk < kvec_end) {
+      for (int u = 0; u < U; ++u) {
+        const int vv = v + 32 * u;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < p.M) {
-            float a[8];
-            bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(m) * p.lda + kk)), a);
+        for (int r = 0; r < R; ++r)
+          wv[u][r] = (vv < v_hi && row_ok[r]) ? ld_stream_v4(brow[r] + 8 * vv) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-              float w[8];
-              bf16x8_to_f32(wv[u][r], w);
+      for (int u = 0; u < U; ++u) {
+        const int vv = v + 32 * u;
+        if (vv < v_hi) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc[r][m] = fmaf(w[e], a[e], acc[r][m]);
+          for (int m = 0; m < MT; ++m) {
+            if (m < p.M) {
+              float a[8];
+              bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(m) * p.lda + 8 * vv)), a);
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                float w[8];
+                bf16x8_to_f32(wv[u][r], w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[r][m] = fmaf(w[e], a[e], acc[r][m]);
+              }
             }
           }
         }
       }
     }
-  }
-  // K tail (fewer than 8 elements): one element per lane.
-  {
-    const int k = kvec_end + lane;
-    if (k < ke) {
+    if (warp == 0 && tail_k + lane < ke) {  // K tail: one element per lane
+      const int k = tail_k + lane;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const float w = row_ok[r] ? bf16_to_f32(brow[r][k]) : 0.f;
@@ -111,37 +118,36 @@ __global__ void __launch_bounds__(kCcWarps * 32) cc_gemv_kernel(const CcParams p
           if (m < p.M) acc[r][m] = fmaf(w, bf16_to_f32(p.A[static_cast<int64_t>(m) * p.lda + k]), acc[r][m]);
       }
     }
-  }
-  // Warp reduction: every lane ends with the full sums.
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float v = acc[r][m];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-      acc[r][m] = v;
-    }
-
-  __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.C);
-  if (p.split_k == 1) {
-    // Lane (r * MT + m) stores element (m, n0 + r).
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
-        if (lane == r * MT + m && m < p.M && row_ok[r])
-          C[static_cast<int64_t>(m) * p.ldc + n0 + r] = __float2bfloat16_rn(acc[r][m]);
-    return;
+      for (int m = 0; m < MT; ++m) {
+        float v = acc[r][m];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        if (lane == 0 && row_ok[r]) red[((r0 + r - row_lo) * MT + m) * kCcWarps + warp] = v;
+      }
   }
+  __syncthreads();
 
-  // Split K: publish this slice's partials, the last slice to arrive finishes.
+  // Sum the warps' partials in warp order.
+  const int rows = row_hi - row_lo;
+  __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.C);
   float* part = p.partials + static_cast<int64_t>(slice) * p.M * p.N;
+  for (int e = threadIdx.x; e < rows * p.M; e += blockDim.x) {
+    const int r = e / p.M, m = e % p.M;
+    const float* src = red + (r * MT + m) * kCcWarps;
+    float s = src[0];
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-      if (lane == r * MT + m && m < p.M && row_ok[r]) part[static_cast<int64_t>(m) * p.N + n0 + r] = acc[r][m];
+    for (int w = 1; w < kCcWarps; ++w) s += src[w];
+    if (p.split_k == 1)
+      C[static_cast<int64_t>(m) * p.ldc + row_lo + r] = __float2bfloat16_rn(s);
+    else
+      part[static_cast<int64_t>(m) * p.N + row_lo + r] = s;
+  }
+  if (p.split_k == 1) return;
+
+  // Split K across CTAs: the last slice of this row block to arrive finishes.
   __threadfence();
   __syncthreads();
   __shared__ uint32_t is_last;
@@ -152,41 +158,45 @@ __global__ void __launch_bounds__(kCcWarps * 32) cc_gemv_kernel(const CcParams p
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  const int rows = p.rows_per_cta;
-  const int nb = blockIdx.x * rows;
   for (int e = threadIdx.x; e < rows * p.M; e += blockDim.x) {
-    const int m = e / rows;
-    const int n = nb + e % rows;
-    if (n >= p.N) continue;
+    const int r = e / p.M, m = e % p.M;
+    const int n = row_lo + r;
     float s = 0.f;
-    for (int sl = 0; sl < p.split_k; ++sl)
-      s = (sl == 0) ? __ldcg(p.partials + (static_cast<int64_t>(sl) * p.M + m) * p.N + n)
-                    : s + __ldcg(p.partials + (static_cast<int64_t>(sl) * p.M + m) * p.N + n);
+    for (int sl = 0; sl < p.split_k; ++sl) {
+      const float x = __ldcg(p.partials + (static_cast<int64_t>(sl) * p.M + m) * p.N + n);
+      s = (sl == 0) ? x : s + x;
+    }
     C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(s);
   }
   if (threadIdx.x == 0) atomicExch(&p.counters[blockIdx.x], 0u);
 }
 
-template <int MT>
-cudaError_t launch_mt(const CcParams& p, int grid_rows, cudaStream_t stream) {
-  dim3 grid(grid_rows, p.split_k);
-  const int R = p.rows_per_cta / kCcWarps;
-  switch (R) {
-    case 1: cc_gemv_kernel<MT, 1><<<grid, kCcWarps * 32, 0, stream>>>(p); break;
-    case 2: cc_gemv_kernel<MT, 2><<<grid, kCcWarps * 32, 0, stream>>>(p); break;
-    case 4: cc_gemv_kernel<MT, 4><<<grid, kCcWarps * 32, 0, stream>>>(p); break;
-    default: return cudaErrorInvalidValue;
+template <int MT, int R, int U>
+cudaError_t launch_one(const CcParams& p, cudaStream_t stream) {
+  const int rows_max = (p.N + p.grid_rows - 1) / p.grid_rows;
+  const size_t smem = static_cast<size_t>(rows_max) * MT * kCcWarps * sizeof(float);
+  auto kern = cc_gemv_kernel<MT, R, U>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
   }
+  dim3 grid(p.grid_rows, p.split_k);
+  kern<<<grid, kCcWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_cc_gemv(const CcParams& p, int grid_rows, cudaStream_t stream) {
-  if (p.M <= 1) return launch_mt<1>(p, grid_rows, stream);
-  if (p.M <= 2) return launch_mt<2>(p, grid_rows, stream);
-  if (p.M <= 4) return launch_mt<4>(p, grid_rows, stream);
-  if (p.M <= 8) return launch_mt<8>(p, grid_rows, stream);
+int cc_smem_bytes(int64_t M, int64_t N, int grid_rows) {
+  const int64_t mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+  return static_cast<int>(((N + grid_rows - 1) / grid_rows) * mt * kCcWarps * sizeof(float));
+}
+
+cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream) {
+  if (p.M <= 1) return launch_one<1, 8, 2>(p, stream);
+  if (p.M <= 2) return launch_one<2, 8, 2>(p, stream);
+  if (p.M <= 4) return launch_one<4, 4, 2>(p, stream);
+  if (p.M <= 8) return launch_one<8, 2, 2>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -16,7 +16,13 @@ constexpr int kBM = 128;  // MMA M (tile rows; weight rows on the swapped path)
 constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
 constexpr int kGemmBN = 256;
 constexpr int kGemmStages = 4;
-constexpr int kSkinnyStages = 8;
+// Skinny (swapped) path: each stage holds kSkinnyKsub consecutive 64-wide k boxes
+// of 128 weight rows, so a weight row is read kSkinnyKsub * 128 contiguous bytes
+// at a time; the ring takes as many stages as fit in 224 KB of shared memory.
+constexpr int kSkinnyKsub = 4;
+constexpr int skinny_stages(int bn) {
+  return (224 * 1024) / (kSkinnyKsub * (kBM + bn) * kBK * 2) < 2 ? 2 : (224 * 1024) / (kSkinnyKsub * (kBM + bn) * kBK * 2);
+}
 constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
 // Everything a tcgen05 launch needs besides its tensor maps.
@@ -50,14 +56,17 @@ struct CcParams {
   uint16_t* C;
   int32_t M, N, K;
   int64_t lda, ldb, ldc;
-  int32_t rows_per_cta;  // weight rows per CTA (warps * rows per warp)
+  int32_t grid_rows;     // CTAs along N; CTA b owns rows [b*N/grid_rows, (b+1)*N/grid_rows)
   int32_t split_k;       // K slices; > 1 uses the partial/counter fixup
   int32_t k_slice;       // k elements per slice (multiple of 8)
   float* partials;       // split_k * M * N fp32 when split_k > 1
   uint32_t* counters;    // one per CTA row group
 };
 
-cudaError_t launch_cc_gemv(const CcParams& p, int grid_rows, cudaStream_t stream);
+cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream);
+
+// Dynamic shared memory of the CUDA-core kernel for M rows over grid_rows row blocks.
+int cc_smem_bytes(int64_t M, int64_t N, int grid_rows);
 
 // Records a CUDA error for sg_last_cuda_error() (this host thread).
 void set_last_cuda_error(int e);

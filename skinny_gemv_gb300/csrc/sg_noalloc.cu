@@ -128,12 +128,12 @@ extern "C" int gemv_bf16_noalloc(const void* A, const void* B, void* C, int64_t 
     p.lda = lda;
     p.ldb = ldb;
     p.ldc = ldc;
-    p.rows_per_cta = plan.rows_per_cta;
+    p.grid_rows = plan.tiles_m;
     p.split_k = plan.split_k;
     p.k_slice = plan.k_steps;
     p.partials = partials;
     p.counters = counters;
-    e = launch_cc_gemv(p, plan.tiles_m, s);
+    e = launch_cc_gemv(p, s);
     if (e != cudaSuccess) {
       set_last_cuda_error(static_cast<int>(e));
       return SG_ERR_CUDA;

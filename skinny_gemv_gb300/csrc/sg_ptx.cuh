@@ -86,16 +86,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Returns false if
-// the deadline passed or *abort became non-zero first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline_ns,
+// *abort became non-zero, or if more than timeout_ns of %globaltimer time has
+// passed since the first unsuccessful try AND at least kMinSpins tries were made
+// (time the kernel spends stopped, e.g. under a profiler's replay, is not
+// counted as waiting unless the loop kept spinning through it).
+constexpr uint32_t kMinSpins = 1u << 18;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
                                           volatile uint32_t* abort) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait(a, parity)) return true;
     if ((spin & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() > deadline_ns) return false;
+      if (spin >= kMinSpins && globaltimer_ns() - t0 > timeout_ns) return false;
     }
   }
 }

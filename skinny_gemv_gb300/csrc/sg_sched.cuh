@@ -3,11 +3,17 @@
 // The output is cut into tiles_m x tiles_n tiles; each tile needs k_steps steps of
 // BK = 64 along K.  A persistent grid of `grid` CTAs (one per SM) walks:
 //
-//   1. data-parallel tiles [0, dp_tiles): CTA c takes tiles c, c + grid, ...
-//      (whole tiles, no partial sums);
-//   2. Stream-K tiles [dp_tiles, dp_tiles + sk_tiles): their flattened
+//   1. Stream-K tiles [0, sk_tiles): their flattened
 //      (tile, k-step) space of sk_units = sk_tiles * k_steps units is cut into
-//      `grid` contiguous ranges, range c = [c*U/grid, (c+1)*U/grid).
+//      `grid` contiguous ranges, range c = [c*U/grid, (c+1)*U/grid);
+//   2. data-parallel tiles [sk_tiles, sk_tiles + dp_tiles): CTA c takes tiles
+//      sk_tiles + c, sk_tiles + c + grid, ...
+//      (whole tiles, no partial sums).
+//
+// The Stream-K pieces come first so that the partial-sum exchange of a split
+// tile overlaps the main loop of the CTA's later whole tiles instead of being
+// exposed at the end of the launch.  Both phases walk the grouped raster in
+// order, so the tiles in flight at any time are neighbours.
 //
 // This is the schedule of spark-kernels, "stream-k proper": a resident grid, the
 // last waves' (tile, k-step) space cut into equal contiguous ranges so that no CTA
@@ -69,22 +75,23 @@ SG_HD int32_t dp_count(const Schedule& s, int32_t c) {
   return c < s.dp_tiles ? (s.dp_tiles - 1 - c) / s.grid + 1 : 0;
 }
 
-// Number of work items of CTA c.
-SG_HD int32_t item_count(const Schedule& s, int32_t c) {
-  int32_t n = dp_count(s, c);
-  if (s.sk_tiles > 0) {
-    const int64_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
-    if (u1 > u0) n += static_cast<int32_t>((u1 - 1) / s.k_steps - u0 / s.k_steps + 1);
-  }
-  return n;
+// Number of Stream-K pieces of CTA c.
+SG_HD int32_t sk_count(const Schedule& s, int32_t c) {
+  if (s.sk_tiles <= 0) return 0;
+  const int64_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
+  return u1 > u0 ? static_cast<int32_t>((u1 - 1) / s.k_steps - u0 / s.k_steps + 1) : 0;
 }
 
-// The i-th work item of CTA c (0 <= i < item_count(s, c)).
+// Number of work items of CTA c.
+SG_HD int32_t item_count(const Schedule& s, int32_t c) { return sk_count(s, c) + dp_count(s, c); }
+
+// The i-th work item of CTA c (0 <= i < item_count(s, c)): its Stream-K pieces
+// first, then its whole tiles.
 SG_HD WorkItem get_item(const Schedule& s, int32_t c, int32_t i) {
   WorkItem w;
-  const int32_t ndp = dp_count(s, c);
-  if (i < ndp) {
-    w.tile = c + i * s.grid;
+  const int32_t nsk = sk_count(s, c);
+  if (i >= nsk) {
+    w.tile = s.sk_tiles + c + (i - nsk) * s.grid;
     w.k0 = 0;
     w.k1 = s.k_steps;
     w.piece = 0;
@@ -94,9 +101,9 @@ SG_HD WorkItem get_item(const Schedule& s, int32_t c, int32_t i) {
     return w;
   }
   const int64_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
-  const int64_t t = u0 / s.k_steps + (i - ndp);
+  const int64_t t = u0 / s.k_steps + i;
   const int64_t tb = t * s.k_steps, te = tb + s.k_steps;
-  w.tile = static_cast<int32_t>(s.dp_tiles + t);
+  w.tile = static_cast<int32_t>(t);
   w.k0 = static_cast<int32_t>((u0 > tb ? u0 : tb) - tb);
   w.k1 = static_cast<int32_t>((u1 < te ? u1 : te) - tb);
   const int64_t first = sk_owner(s, tb), last = sk_owner(s, te - 1);
@@ -132,10 +139,18 @@ SG_HD double wave_efficiency(int64_t ctas, int64_t slots) {
   return static_cast<double>(ctas) / static_cast<double>(slots) / static_cast<double>(waves);
 }
 
-// Builds the schedule.  min_units_per_cta bounds how thinly a tile may be split
-// (a piece's fp32 partial costs about as much as a few k-steps of loads).
+// Builds the schedule.
+//
+// tiles >= CTAs: whole-tile waves, with the last full wave plus the remainder cut
+//   by Stream-K when the tile count is not a multiple of the CTA count.
+// tiles < CTAs, memory-bound (fill_grid): every tile is split along K so that
+//   all `num_ctas` CTAs stream an equal share (at least min_units_per_cta k-steps
+//   each); the weight stream needs every SM's load bandwidth.
+// tiles < CTAs, compute-bound (!fill_grid): Stream-K only pays when a tile can be
+//   split at least two ways (s = floor(CTAs / tiles) >= 2): one tile per CTA
+//   loses (1 - tiles/CTAs) of a tile's time at most, less than a fixup costs.
 inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps, int32_t num_ctas,
-                              int32_t min_units_per_cta, int32_t group_m) {
+                              int32_t min_units_per_cta, int32_t group_m, bool fill_grid) {
   Schedule s{};
   s.tiles_m = tiles_m;
   s.tiles_n = tiles_n;
@@ -143,6 +158,7 @@ inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps,
   s.group_m = group_m < 1 ? 1 : group_m;
   const int64_t T = static_cast<int64_t>(tiles_m) * tiles_n;
   const int64_t G = num_ctas < 1 ? 1 : num_ctas;
+  const int64_t per = min_units_per_cta < 1 ? 1 : min_units_per_cta;
   if (T >= G) {
     const int64_t rem = T % G;
     s.grid = static_cast<int32_t>(G);
@@ -155,18 +171,24 @@ inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps,
       s.dp_tiles = static_cast<int32_t>(T - s.sk_tiles);
     }
   } else {
-    // Fewer tiles than CTAs: every tile is split along K.
     const int64_t units = T * k_steps;
-    const int64_t per = min_units_per_cta < 1 ? 1 : min_units_per_cta;
-    int64_t g = units / per;
-    if (g > G) g = G;
+    int64_t g;
+    if (fill_grid) {
+      g = units / per;
+      if (g > G) g = G;
+    } else {
+      const int64_t split = G / T;  // >= 1
+      g = split >= 2 ? T * split : T;
+      if (g > units / per) g = units / per;
+    }
     if (g < T) g = T;
     s.grid = static_cast<int32_t>(g);
-    s.dp_tiles = 0;
-    s.sk_tiles = static_cast<int32_t>(T);
     if (g == T) {  // one CTA per tile: plain data-parallel
       s.dp_tiles = static_cast<int32_t>(T);
       s.sk_tiles = 0;
+    } else {
+      s.dp_tiles = 0;
+      s.sk_tiles = static_cast<int32_t>(T);
     }
   }
   s.sk_units = static_cast<int64_t>(s.sk_tiles) * k_steps;

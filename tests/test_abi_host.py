@@ -116,7 +116,9 @@ def _check_plan_coverage(info):
     pieces = {}
     for cta, row in enumerate(items):
         assert len(row) >= 1, f"CTA {cta} has no work"
-        first_sk = sum(1 for it in row if it[0] < info["dp_tiles"])
+        n_sk = sum(1 for it in row if it[0] < info["sk_tiles"])
+        # Stream-K pieces (tiles [0, sk_tiles)) come first, then whole tiles
+        assert all(it[0] < info["sk_tiles"] for it in row[:n_sk])
         for idx, (tile, k0, k1, piece, npieces, slot, sk, tm, tn) in enumerate(row):
             assert 0 <= tile < T and 0 <= k0 < k1 <= KS
             assert 0 <= tm < info["tiles_m"] and 0 <= tn < info["tiles_n"]
@@ -124,8 +126,8 @@ def _check_plan_coverage(info):
             if npieces > 1:
                 assert slot in (2 * cta, 2 * cta + 1)
                 # slot 0 of a CTA is its first Stream-K item, slot 1 its last
-                assert (slot == 2 * cta) == (idx == first_sk)
-                assert idx in (first_sk, len(row) - 1)
+                assert (slot == 2 * cta) == (idx == 0)
+                assert idx in (0, n_sk - 1)
                 pieces.setdefault(tile, []).append((k0, k1, piece, npieces, cta, slot))
             else:
                 assert (k0, k1) == (0, KS) and slot == -1
@@ -181,16 +183,21 @@ def test_auto_path_choice(lib):
     assert sg.plan(65, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM
 
 
-@pytest.mark.parametrize("N,K", [(11008, 4096), (4096, 11008), (256, 8192), (100, 24)])
+@pytest.mark.parametrize("N,K", [(11008, 4096), (4096, 11008), (256, 8192), (100, 24), (1 << 20, 64)])
 def test_cuda_core_plan(lib, N, K):
     info = sg.plan(2, N, K, 152, sg.PATH_CUDA_CORE)
-    assert info["rows_per_cta"] == 32
-    assert info["tiles_m"] == -(-N // 32)
+    blocks = info["tiles_m"]
+    # two CTAs per SM unless there are fewer rows; at most 256 rows per CTA
+    assert blocks == max(min(N, 304), -(-N // 256))
+    assert info["rows_per_cta"] == -(-N // blocks) <= 256
     k_slice = info["k_steps"]
     assert k_slice % 8 == 0 and info["split_k"] == -(-K // k_slice)
-    assert info["grid"] == info["tiles_m"] * info["split_k"]
-    if info["tiles_m"] >= 2 * 152:
+    assert info["grid"] == blocks * info["split_k"]
+    if blocks >= 304:
         assert info["split_k"] == 1
+    # every row belongs to exactly one block: [b*N/blocks, (b+1)*N/blocks)
+    bounds = [(b * N) // blocks for b in range(blocks + 1)]
+    assert bounds[0] == 0 and bounds[-1] == N and all(x < y for x, y in zip(bounds, bounds[1:]))
 
 
 def test_plan_rejects_bad_arguments(lib):
