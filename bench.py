@@ -13,8 +13,9 @@ before.  The JSON line (printed by rank 0) carries:
 
   value / ms_per_step  whole-job TFLOP/s (2*M*N*K per step, all ranks) over the
                        max-over-ranks time of the K steps
-  roofline             the GEMM kernel's achieved TFLOP/s (mean CUDA-event
-                       duration of its launches) against the measured bf16 peak
+  roofline             the GEMM kernel's achieved TFLOP/s (CUDA-event time of
+                       the K back-to-back launches / K) against the measured
+                       bf16 peak
   e2e                  the same metric with host buffers: each step copies A and
                        B from pinned host memory, calls gemm_bf16 and copies C back
   cpu_baseline         the fp64 oracle on a bounded row sample, on the host cores
@@ -215,24 +216,38 @@ def rotation_count(bytes_per_set: int, l2: int) -> int:
     return max(2, math.ceil(4 * l2 / max(bytes_per_set, 1)) + 1)
 
 
-def time_launches(torch, stream, fns, steps: int, warmup: int):
-    """Runs fns[i % len(fns)] for warmup + steps; returns (total_ms, per-launch ms list)
-    of the timed steps, with CUDA events on `stream`."""
+def build_graphs(torch, stream, fns, steps: int, graph_chunk: int = 500, offset: int = 0):
+    """Captures fns[(offset + i) % len(fns)] for i < steps into CUDA graphs of at
+    most graph_chunk launches each (one launch per step)."""
+    graphs = []
+    for c0 in range(0, steps, graph_chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(c0, min(steps, c0 + graph_chunk)):
+                fns[(offset + i) % len(fns)]()
+        graphs.append(g)
+    stream.synchronize()
+    return graphs
+
+
+def time_launches(torch, stream, fns, steps: int, warmup: int, graph_chunk: int = 500):
+    """Runs fns[i % len(fns)] `warmup` times eagerly, then captures the `steps`
+    timed calls into CUDA graphs (at most graph_chunk launches each) and replays
+    them back to back on `stream`, bracketed by CUDA events on that stream.
+    Graph replay keeps host launch overhead out of the device timeline, so
+    short kernels are timed as they run back to back.  Returns total ms."""
     for i in range(warmup):
         fns[i % len(fns)]()
     stream.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    graphs = build_graphs(torch, stream, fns, steps, graph_chunk, offset=warmup)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(steps):
-        starts[i].record(stream)
-        fns[(warmup + i) % len(fns)]()
-        ends[i].record(stream)
+    for g in graphs:
+        g.replay()
     t1.record(stream)
     t1.synchronize()
-    return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return t0.elapsed_time(t1)
 
 
 # ---------------------------------------------------------------- the reference arm
@@ -314,18 +329,27 @@ def run_ours(args, world, rank, local):
         fns[i % nrot]()
     torch.cuda.synchronize()
     barrier(dist)
+    graphs = build_graphs(torch, stream, fns, args.steps)
     with sampler:
         torch.cuda.synchronize()
-        total_ms, per_launch = time_launches(torch, stream, fns, args.steps, 0)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for g in graphs:
+            g.replay()
+        t1.record(stream)
+        t1.synchronize()
+        total_ms = t0.elapsed_time(t1)
         torch.cuda.synchronize()
     barrier(dist)
-    total_ms = max_over_ranks(dist, total_ms)
     st, detail = sg.check_device_errors(stream)
     if st != sg.SG_OK:
         raise RuntimeError(f"device error {st} {detail}")
 
+    local_ms = total_ms
+    total_ms = max_over_ranks(dist, total_ms)
     value = tflops(M, N, K, total_ms / 1e3 / args.steps) * world
-    kernel_ms = statistics.fmean(per_launch)
+    kernel_ms = local_ms / args.steps  # mean launch duration, back to back
     achieved = tflops(M, N, K, kernel_ms / 1e3)
 
     e2e = None
@@ -355,14 +379,16 @@ def run_ours(args, world, rank, local):
             "M": M, "N": N, "K": K, "accumulate": "f32",
             "l2": f"inputs larger than L2: {nrot} rotating copies of A, B, C "
                   f"({nrot * 3 * M * K * 2 / 2**20:.0f} MiB vs {l2 / 2**20:.0f} MiB L2), no flush",
-            "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}", "grid": plan["grid"],
+            "tile": f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
+            "ctas": plan["grid"] * plan["cluster_size"], "cluster": plan["cluster_size"],
             "dp_tiles": plan["dp_tiles"], "sk_tiles": plan["sk_tiles"],
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "roofline": {
             "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": recorded_traffic("tc_gemm_kernel", HEADLINE),
-            "kernel": "tc_gemm_kernel<256,4,false>", "kernel_ms": kernel_ms,
+            "kernel": ("tc_gemm_kernel<256,6,pair>" if plan["path"] == sg.PATH_GEMM_PAIR
+                       else "tc_gemm_kernel<256,4,single>"), "kernel_ms": kernel_ms,
             "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peaks['source']}, burst: cuBLAS 8192^3)",
             "algorithmic": f"2*M*N*K = {2 * M * N * K / 1e9:.1f} GFLOP per launch",
         },
@@ -473,10 +499,9 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args):
             else:
                 fns = [(lambda a=a, b=b, p=path: sg.gemv_bf16(a, b, C, stream=stream, path=p))
                        for a, b in zip(As, Bs)]
-            total, per = time_launches(torch, stream, fns, steps, 5)
-            med = statistics.median(per)
-            row = {"workload": name, "entry": label, "M": w.M, "N": w.N, "K": w.K,
-                   "us_median": med * 1e3, "us_back_to_back": total / steps * 1e3}
+            total = time_launches(torch, stream, fns, steps, 5)
+            med = total / steps  # ms per launch, graph replay back to back
+            row = {"workload": name, "entry": label, "M": w.M, "N": w.N, "K": w.K, "us": med * 1e3}
             if w.M > 64:
                 row["tflops"] = tflops(w.M, w.N, w.K, med / 1e3)
                 row["frac_of_peak"] = row["tflops"] / peaks["bf16_tflops"]
@@ -484,7 +509,6 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args):
                 gbs = decode_bytes(w.M, w.N, w.K) / (med / 1e3) / 1e9
                 row["gbs"] = gbs
                 row["frac_of_hbm"] = gbs / peaks["hbm_gbs"]
-                row["gbs_back_to_back"] = decode_bytes(w.M, w.N, w.K) / (total / steps / 1e3) / 1e9
             out.append(row)
         del As, Bs, A, B, C
         torch.cuda.empty_cache()

@@ -68,7 +68,8 @@ typedef enum {
     SG_PATH_AUTO = 0,        /* library's choice (see gemv_bf16) */
     SG_PATH_CUDA_CORE = 1,   /* fp32 FMA stream over the weights, no tensor cores */
     SG_PATH_TENSOR_CORE = 2, /* tcgen05 with the weight rows on the MMA's M side */
-    SG_PATH_GEMM = 3         /* the general tcgen05 GEMM (plan output only) */
+    SG_PATH_GEMM = 3,        /* tcgen05 GEMM, one CTA per 128 x 256 tile */
+    SG_PATH_GEMM_PAIR = 4    /* tcgen05 GEMM, a 2-CTA cluster per 256 x 256 tile */
 } sg_path;
 
 /*
@@ -147,6 +148,19 @@ SG_API int gemv_bf16_noalloc(const void *A, const void *B, void *C,
                              int64_t M, int64_t N, int64_t K,
                              int64_t lda, int64_t ldb, int64_t ldc, sg_stream_t stream);
 
+/*
+ * gemm_bf16_path -- gemm_bf16 with the kernel chosen by the caller:
+ * SG_PATH_AUTO (gemm_bf16's choice), SG_PATH_GEMM (one CTA per 128 x 256 tile),
+ * SG_PATH_GEMM_PAIR (a cluster of two CTAs on two SMs per 256 x 256 tile, each
+ * CTA loading half of the A rows and half of the B rows of the tile), or, for
+ * M <= 64, SG_PATH_CUDA_CORE / SG_PATH_TENSOR_CORE as in gemv_bf16_path.  Any M
+ * is accepted by the two GEMM kernels.  Same arguments and errors as gemm_bf16;
+ * an unknown path, or a skinny path with M > 64, is SG_ERR_INVALID_ARG.
+ */
+SG_API int gemm_bf16_path(const void *A, const void *B, void *C,
+                          int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc, int path, sg_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 SG_API const char *sg_status_string(int status);
 
@@ -187,12 +201,15 @@ typedef struct {
     int32_t split_k;    /* CUDA-core path: K slices per row group */
     int32_t rows_per_cta; /* CUDA-core path: weight rows per CTA */
     double wave_efficiency; /* of one tile per CTA, (ctas/slots)/ceil(ctas/slots) */
+    int32_t cluster_size; /* CTAs per schedule unit: 2 for SG_PATH_GEMM_PAIR, else 1 */
+    int32_t reserved;
 } sg_plan_info;
 
 /*
- * sg_plan -- the launch plan gemm_bf16 (entry = 0) or gemv_bf16_path (entry = path,
- * 1 = CUDA core, 2 = tensor core; 0 = the automatic choice) would use for this
- * shape on a device with `num_sms` SMs.  Returns SG_OK or SG_ERR_INVALID_ARG.
+ * sg_plan -- the launch plan gemm_bf16_path would use for this shape and `entry`
+ * (an sg_path; 0 = gemm_bf16's automatic choice) on a device with `num_sms` SMs.
+ * For the paired GEMM, `grid` counts clusters (each of cluster_size CTAs).
+ * Returns SG_OK or SG_ERR_INVALID_ARG.
  */
 SG_API int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
 

@@ -33,8 +33,9 @@ PATH_AUTO = 0
 PATH_CUDA_CORE = 1
 PATH_TENSOR_CORE = 2
 PATH_GEMM = 3
+PATH_GEMM_PAIR = 4
 PATH_NAMES = {PATH_AUTO: "auto", PATH_CUDA_CORE: "cuda_core", PATH_TENSOR_CORE: "tensor_core",
-              PATH_GEMM: "gemm"}
+              PATH_GEMM: "gemm", PATH_GEMM_PAIR: "gemm_pair"}
 
 
 class SgError(RuntimeError):
@@ -52,7 +53,8 @@ class PlanInfo(ctypes.Structure):
                 ("k_steps", ctypes.c_int32), ("grid", ctypes.c_int32), ("dp_tiles", ctypes.c_int32),
                 ("sk_tiles", ctypes.c_int32), ("sk_units", ctypes.c_int64), ("group_m", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32),
-                ("wave_efficiency", ctypes.c_double)]
+                ("wave_efficiency", ctypes.c_double), ("cluster_size", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -88,8 +90,10 @@ def load(build_if_missing: bool = False):
         f = getattr(lib, name)
         f.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, p]
         f.restype = ctypes.c_int
-    lib.gemv_bf16_path.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
-    lib.gemv_bf16_path.restype = ctypes.c_int
+    for name in ("gemv_bf16_path", "gemm_bf16_path"):
+        f = getattr(lib, name)
+        f.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
+        f.restype = ctypes.c_int
     lib.sg_status_string.argtypes = [ctypes.c_int]
     lib.sg_status_string.restype = ctypes.c_char_p
     lib.sg_last_cuda_error.argtypes = []
@@ -130,9 +134,9 @@ def _check(status: int, where: str) -> None:
 
 # ------------------------------------------------------------------ raw pointers
 def gemm_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
-                  stream: int = 0) -> int:
+                  stream: int = 0, path: int = PATH_AUTO) -> int:
     """C-ABI call with raw device pointers; returns the sg_status code."""
-    return load().gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, stream)
+    return load().gemm_bf16_path(A, B, C, M, N, K, lda, ldb, ldc, path, stream)
 
 
 def gemv_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
@@ -180,7 +184,8 @@ def _call(fn_name: str, A, B, C=None, stream=None, path: int | None = None):
     lib = load()
     with torch.cuda.device(A.device):
         if fn_name == "gemm_bf16":
-            st = lib.gemm_bf16(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc, s)
+            st = lib.gemm_bf16_path(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc,
+                                    PATH_AUTO if path is None else path, s)
         elif fn_name == "gemv_bf16_noalloc":
             st = lib.gemv_bf16_noalloc(a_ptr, b_ptr, c_ptr, M, N, K, lda, ldb, ldc, s)
         else:
@@ -190,9 +195,10 @@ def _call(fn_name: str, A, B, C=None, stream=None, path: int | None = None):
     return C
 
 
-def gemm_bf16(A, B, C=None, stream=None):
-    """C[M, N] = A[M, K] @ B[N, K]^T in bf16 with fp32 accumulation."""
-    return _call("gemm_bf16", A, B, C, stream)
+def gemm_bf16(A, B, C=None, stream=None, path: int = PATH_AUTO):
+    """C[M, N] = A[M, K] @ B[N, K]^T in bf16 with fp32 accumulation; ``path``
+    picks the kernel (PATH_AUTO, PATH_GEMM, PATH_GEMM_PAIR, or a skinny PATH_*)."""
+    return _call("gemm_bf16", A, B, C, stream, path)
 
 
 def gemv_bf16(A, B, C=None, stream=None, path: int = PATH_AUTO):

@@ -207,20 +207,26 @@ Schedule sched_from_plan(const sg_plan_info& o) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+// tcgen05 GEMM plan.  pair: 256 x 256 tiles on clusters of two CTAs (the
+// schedule counts clusters); else 128 x 256 tiles, one CTA each.
+void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
-  o->path = SG_PATH_GEMM;
-  o->tile_m = kBM;
+  o->path = pair ? SG_PATH_GEMM_PAIR : SG_PATH_GEMM;
+  o->tile_m = pair ? 2 * kBM : kBM;
   o->tile_n = kGemmBN;
   o->tile_k = kBK;
-  o->stages = kGemmStages;
-  const int32_t tm = static_cast<int32_t>(ceil_div(M, kBM)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN));
+  o->stages = pair ? kPairStages : kGemmStages;
+  o->cluster_size = pair ? 2 : 1;
+  const int32_t units = pair ? std::max(1, sms / 2) : sms;
+  const int32_t tm = static_cast<int32_t>(ceil_div(M, o->tile_m)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN));
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
-  const Schedule s = make_schedule(tm, tn, ks, sms, 4, std::min<int32_t>(tm, 8), false);
+  const Schedule s = make_schedule(tm, tn, ks, units, 4, std::min<int32_t>(tm, pair ? 4 : 8), false);
   fill_sched(o, s);
   o->split_k = 1;
-  o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, sms);
+  o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, units);
 }
+
+bool auto_pair(int64_t M) { return M >= 2 * kBM; }
 
 int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
@@ -231,6 +237,7 @@ void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   o->tile_n = skinny_bn(M);
   o->tile_k = kBK * kSkinnyKsub;
   o->stages = skinny_stages(o->tile_n);
+  o->cluster_size = 1;
   const int32_t tm = static_cast<int32_t>(ceil_div(N, kBM));
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK * kSkinnyKsub));
   const Schedule s = make_schedule(tm, 1, ks, sms, 2, 1, true);
@@ -245,6 +252,7 @@ void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
 void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
   o->path = SG_PATH_CUDA_CORE;
+  o->cluster_size = 1;
   const int64_t target = 2 * static_cast<int64_t>(sms);
   int64_t rows_grid = std::min<int64_t>(N, target);
   rows_grid = std::max<int64_t>(rows_grid, ceil_div(N, kCcMaxRowsPerCta));
@@ -303,17 +311,18 @@ TcParams base_params(DeviceState& d, int64_t M, int64_t N, int64_t K, int64_t ld
 }
 
 int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
+                int64_t lda, int64_t ldb, int64_t ldc, bool pair, cudaStream_t stream) {
   sg_plan_info plan;
-  plan_tc_gemm(M, N, K, d.sm_count, &plan);
+  plan_tc_gemm(M, N, K, d.sm_count, pair, &plan);
   CUtensorMap ta, tb, tc;
+  const uint32_t b_rows = pair ? kGemmBN / 2 : kGemmBN;  // B rows each CTA loads per tile
   int st = make_map(&ta, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
-  if (st == SG_OK) st = make_map(&tb, B, N, K, ldb, kGemmBN, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tb, B, N, K, ldb, b_rows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, dev);
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
-  cudaError_t e = launch_tc_gemm(ta, tb, tc, p, stream);
+  cudaError_t e = pair ? launch_tc_gemm_pair(ta, tb, tc, p, stream) : launch_tc_gemm(ta, tb, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
@@ -386,12 +395,16 @@ using namespace sg;
 
 extern "C" {
 
-int gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-              int64_t ldc, sg_stream_t stream) {
+int gemm_bf16_path(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                   int64_t ldb, int64_t ldc, int path, sg_stream_t stream) {
+  if (path < SG_PATH_AUTO || path > SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
+  if ((path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE) && M > 64) return SG_ERR_INVALID_ARG;
   int st = validate(A, B, C, M, N, K, lda, ldb, ldc);
   if (st != SG_OK || M == 0 || N == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (M <= 64) return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, s);
+  if (path == SG_PATH_AUTO && M <= 64) return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, s);
+  if (path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE)
+    return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, path, s);
   DeviceState* d = nullptr;
   int dev = 0;
   st = current_device_state(&d, &dev);
@@ -402,7 +415,13 @@ int gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
   }
   st = ensure_workspace(*d, s);
   if (st != SG_OK) return st;
-  return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, s);
+  const bool pair = path == SG_PATH_GEMM_PAIR || (path == SG_PATH_AUTO && auto_pair(M));
+  return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, pair, s);
+}
+
+int gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              int64_t ldc, sg_stream_t stream) {
+  return gemm_bf16_path(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, stream);
 }
 
 int gemv_bf16_path(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -466,13 +485,13 @@ int sg_check_device_errors(sg_stream_t stream, uint32_t detail[4]) {
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info* out) {
   if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
-  if (entry < 0 || entry > SG_PATH_TENSOR_CORE) return SG_ERR_INVALID_ARG;
-  if (entry == 0 && M > 64) {
-    plan_tc_gemm(M, N, K, num_sms, out);
+  if (entry < SG_PATH_AUTO || entry > SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
+  if (entry == SG_PATH_GEMM || entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && M > 64)) {
+    plan_tc_gemm(M, N, K, num_sms, entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && auto_pair(M)), out);
     return SG_OK;
   }
   if (M > 64) return SG_ERR_INVALID_ARG;
-  const int path = entry == 0 ? choose_skinny_path(M) : entry;
+  const int path = entry == SG_PATH_AUTO ? choose_skinny_path(M) : entry;
   if (path == SG_PATH_CUDA_CORE)
     plan_cc(std::min<int64_t>(std::max<int64_t>(M, 1), 8), N, K, num_sms, out);
   else

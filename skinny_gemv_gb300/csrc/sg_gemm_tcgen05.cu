@@ -23,6 +23,12 @@
 // operands go TMA -> shared memory -> tcgen05.mma without a trip through
 // registers, and the accumulator lives in tensor memory instead of registers.
 //
+// The paired variant (PAIR = true) runs on clusters of two CTAs on two SMs: one
+// 256 x 256 output tile per pair, each CTA loading its 128 rows of A and 128 rows
+// of B (32 KB per stage, 6 stages) and holding its 128 x 256 half of the
+// accumulator; the even CTA issues tcgen05.mma.cta_group::2 for both.  Per SM this
+// moves 2/3 of the bytes of the 128 x 256 single-CTA tile for the same FLOPs.
+//
 // The swapped variant (SWAP = true) serves the skinny path: the weights B take
 // the MMA's 128-row M side and the few activation rows of A its N side (16, 32 or
 // 64), so every weight byte is loaded once for all rows; its epilogue writes
@@ -37,10 +43,12 @@ namespace sg {
 namespace {
 
 // KSUB: consecutive 64-wide k boxes per pipeline stage (one schedule k-step).
-template <int BN, int STAGES, bool SWAP, int KSUB>
+// PAIR: B's rows are split between the two CTAs of a pair (BN / 2 each).
+template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
 struct TcLayout {
+  static constexpr int kBRowsPerCta = PAIR ? BN / 2 : BN;
   static constexpr int kASub = kBM * kBK * 2;  // 16 KB: one 128 x 64 box
-  static constexpr int kBSub = BN * kBK * 2;
+  static constexpr int kBSub = kBRowsPerCta * kBK * 2;
   static constexpr int kABytes = KSUB * kASub;
   static constexpr int kBBytes = KSUB * kBSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -59,8 +67,11 @@ struct TcLayout {
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
   static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
   static constexpr int kChunk = SWAP ? 16 : 32;  // accumulator columns per tcgen05.ld
+  // epilogue arrivals that free an accumulator: 4 warps, of both CTAs when paired
+  static constexpr uint32_t kTmemEmptyCount = PAIR ? 2 * kEpiWarps : kEpiWarps;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
   static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
+  static_assert(!(PAIR && SWAP), "the paired variant is the non-swapped GEMM");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -77,13 +88,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int BN, int STAGES, bool SWAP, int KSUB>
+template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using L = TcLayout<BN, STAGES, SWAP, KSUB>;
+  using L = TcLayout<BN, STAGES, SWAP, KSUB, PAIR>;
+  constexpr int kTileRows = PAIR ? 2 * kBM : kBM;  // output rows per tile (the MMA's M)
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, BN);
   const int kboxes = (p.K + kBK - 1) / kBK;  // 64-wide k boxes that hold data
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -100,8 +112,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const Schedule& sched = p.sched;
-  const int cta = blockIdx.x;
-  const int nitems = item_count(sched, cta);
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = the pair's MMA issuer
+  const int unit = PAIR ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+  const int nitems = item_count(sched, unit);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -110,7 +123,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], L::kEpiWarps);
+      mbar_init(&tmem_empty[b], L::kTmemEmptyCount);
     }
     mbar_init(teardown, 1);
     *abort_flag = 0;
@@ -123,11 +136,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!SWAP) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, L::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, L::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, L::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -137,9 +156,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int i = 0; i < nitems && ok; ++i) {
-        const WorkItem w = get_item(sched, cta, i);
+        const WorkItem w = get_item(sched, unit, i);
         int32_t tm, tn;
         tile_coords(sched, w.tile, tm, tn);
+        const int arow = tm * kTileRows + static_cast<int>(rank) * kBM;
+        const int brow = tn * BN + static_cast<int>(rank) * L::kBRowsPerCta;
         for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -150,15 +171,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           const int nsub = min(KSUB, kboxes - ks * KSUB);  // boxes past K are skipped
-          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nsub * (L::kASub + L::kBSub)));
-          for (int j = 0; j < nsub; ++j) {
-            const int kx = (ks * KSUB + j) * kBK;
-            tma_load_2d(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, tm * kBM, &full[s]);
-            tma_load_2d(smem + L::kBOff + s * L::kBBytes + j * L::kBSub, &tmB, kx, tn * BN, &full[s]);
+          const uint32_t bytes = static_cast<uint32_t>(nsub * (L::kASub + L::kBSub));
+          if constexpr (PAIR) {
+            // the leader's full barrier counts both CTAs' bytes
+            const uint32_t full_leader = mapa_shared(smem_u32(&full[s]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * bytes);
+            for (int j = 0; j < nsub; ++j) {
+              const int kx = (ks * KSUB + j) * kBK;
+              tma_load_2d_pair(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, arow, full_leader);
+              tma_load_2d_pair(smem + L::kBOff + s * L::kBBytes + j * L::kBSub, &tmB, kx, brow, full_leader);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[s], bytes);
+            for (int j = 0; j < nsub; ++j) {
+              const int kx = (ks * KSUB + j) * kBK;
+              tma_load_2d(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, arow, &full[s]);
+              tma_load_2d(smem + L::kBOff + s * L::kBBytes + j * L::kBSub, &tmB, kx, brow, &full[s]);
+            }
           }
         }
       }
-      if (!ok) {
+      if (!ok && rank == 0) {
         // Unwinding: let the loads already issued land before the CTA exits.
         const uint32_t inflight = it < STAGES ? it : STAGES;
         for (uint32_t j = 0; j < inflight; ++j) {
@@ -170,11 +203,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       uint32_t it = 0;
       bool ok = true;
       for (int i = 0; i < nitems && ok; ++i) {
-        const WorkItem w = get_item(sched, cta, i);
+        const WorkItem w = get_item(sched, unit, i);
         const uint32_t b = static_cast<uint32_t>(i) & 1u;
         const uint32_t use = static_cast<uint32_t>(i) >> 1;
         if (!mbar_wait(&tmem_empty[b], (use & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
@@ -201,18 +234,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               // +32 bytes per 16 bf16 of K inside the 128-byte swizzle row
-              tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
-                          (ks > w.k0 || j > 0 || kk > 0) ? 1u : 0u);
+              const uint32_t acc = (ks > w.k0 || j > 0 || kk > 0) ? 1u : 0u;
+              if constexpr (PAIR)
+                tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32),
+                                 kIdesc, acc);
+              else
+                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
+                            acc);
             }
           }
-          tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+          // the stage is free (in both CTAs) once these MMAs have read it
+          if constexpr (PAIR)
+            tc_commit_pair_multicast(&empty[s], 0x3);
+          else
+            tc_commit(&empty[s]);
         }
         if (!ok) break;
-        tc_commit(&tmem_full[b]);  // accumulator b is complete
+        if constexpr (PAIR)
+          tc_commit_pair_multicast(&tmem_full[b], 0x3);  // accumulator b complete in both CTAs
+        else
+          tc_commit(&tmem_full[b]);
       }
       if (!ok || *abort_flag) {
         // Unwinding: wait for every MMA issued so far before TMEM is freed.
-        tc_commit(teardown);
+        if constexpr (PAIR)
+          tc_commit_pair_multicast(teardown, 0x1);
+        else
+          tc_commit(teardown);
         volatile uint32_t never = 0;
         if (!mbar_wait(teardown, 0, p.timeout_ns, &never)) record_error(p.err, kDevTimeoutTeardown, 0);
       }
@@ -225,12 +273,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int epi_tid = threadIdx.x - 64;  // 0..127
     uint32_t store_count = 0;
     uint8_t* staging = smem + L::kStagingOff + q * L::kStagingBufs * L::kStagingBufBytes;
+    // the accumulator-free barrier lives in the pair's MMA-issuing CTA
+    const uint32_t tmem_empty_addr0 = PAIR ? mapa_shared(smem_u32(&tmem_empty[0]), 0) : smem_u32(&tmem_empty[0]);
 
     // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
     auto emit_chunk = [&](const float* v, int tm, int tn, int j) {
       if constexpr (!SWAP) {
         const int col0 = tn * BN + j * 32;
-        const int row0 = tm * kBM + q * 32;
+        const int row0 = tm * kTileRows + static_cast<int>(rank) * kBM + q * 32;
         const uint32_t buf = store_count & 1u;
         if (lane == 0) bulk_wait_group_read<1>();  // buffer `buf` no longer read by TMA
         __syncwarp();
@@ -279,16 +329,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     };
 
+    auto release_accumulator = [&](uint32_t b) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(tmem_empty_addr0 + b * 8);
+        else
+          mbar_arrive(&tmem_empty[b]);
+      }
+    };
+
     constexpr int kChunks = BN / L::kChunk;
     constexpr int kQuads = L::kChunk / 4;
+    constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * BN;  // one CTA's share of a tile
     for (int i = 0; i < nitems; ++i) {
-      const WorkItem w = get_item(sched, cta, i);
+      const WorkItem w = get_item(sched, unit, i);
       int32_t tm, tn;
       tile_coords(sched, w.tile, tm, tn);
       const uint32_t b = static_cast<uint32_t>(i) & 1u;
       const uint32_t use = static_cast<uint32_t>(i) >> 1;
       // An accumulator is ready after its k-steps have run: allow 20 us per k-step
-      // on top of the base bound (a k-step normally takes about 0.3 us).
+      // on top of the base bound (a k-step normally takes well under 1 us).
       const uint64_t limit = p.timeout_ns + static_cast<uint64_t>(w.k1 - w.k0) * 20000ull;
       if (!mbar_wait(&tmem_full[b], use & 1u, limit, abort_flag)) {
         if (!*abort_flag) record_error(p.err, kDevTimeoutTmemFull, i);
@@ -303,25 +365,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           load_chunk(tacc + j * L::kChunk, v);
           emit_chunk(v, tm, tn, j);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tmem_empty[b]);
+        release_accumulator(b);
       } else {
-        // Stream-K piece: publish this piece's fp32 partial, then count arrivals.
-        float4* slot = reinterpret_cast<float4*>(p.partials + static_cast<int64_t>(w.slot) * kBM * BN);
+        // Stream-K piece: publish this CTA's fp32 partial, then count arrivals.
+        // Slots and counters are per CTA of a pair (each holds its own rows).
+        const int64_t my_slot = PAIR ? 2 * static_cast<int64_t>(w.slot) + rank : w.slot;
+        const int counter = PAIR ? 2 * w.sk_index + static_cast<int>(rank) : w.sk_index;
+        float4* slot = reinterpret_cast<float4*>(p.partials + my_slot * kSlotFloats);
         for (int j = 0; j < kChunks; ++j) {
           load_chunk(tacc + j * L::kChunk, v);
 #pragma unroll
           for (int q4 = 0; q4 < kQuads; ++q4)
             slot[(j * kQuads + q4) * kBM + row] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tmem_empty[b]);
+        release_accumulator(b);
         __threadfence();
         named_bar_sync(1, 128);
         if (epi_tid == 0) {
-          const uint32_t before = atomicAdd(&p.counters[w.sk_index], 1u);
+          const uint32_t before = atomicAdd(&p.counters[counter], 1u);
           *sk_last = (before == static_cast<uint32_t>(w.npieces - 1)) ? 1u : 0u;
         }
         named_bar_sync(1, 128);
@@ -333,10 +394,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Two pieces per batch: 2 x kQuads independent loads in flight.
             for (int pj = 0; pj < w.npieces; pj += 2) {
               const bool pair = pj + 1 < w.npieces;
-              const float4* s0 = reinterpret_cast<const float4*>(
-                  p.partials + static_cast<int64_t>(piece_slot(sched, w.sk_index, pj)) * kBM * BN);
-              const float4* s1 = reinterpret_cast<const float4*>(
-                  p.partials + static_cast<int64_t>(piece_slot(sched, w.sk_index, pair ? pj + 1 : pj)) * kBM * BN);
+              const int64_t sl0 = piece_slot(sched, w.sk_index, pj);
+              const int64_t sl1 = piece_slot(sched, w.sk_index, pair ? pj + 1 : pj);
+              const float4* s0 = reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl0 + rank : sl0) * kSlotFloats);
+              const float4* s1 = reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl1 + rank : sl1) * kSlotFloats);
               float4 x0[kQuads], x1[kQuads];
 #pragma unroll
               for (int q4 = 0; q4 < kQuads; ++q4) x0[q4] = __ldcg(&s0[(j * kQuads + q4) * kBM + row]);
@@ -359,7 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             emit_chunk(acc, tm, tn, j);
           }
-          if (epi_tid == 0) atomicExch(&p.counters[w.sk_index], 0u);
+          if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
         }
       }
     }
@@ -370,49 +431,74 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, L::kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, L::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, L::kTmemCols);
   }
 }
 
-template <int BN, int STAGES, bool SWAP, int KSUB>
+template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
                            cudaStream_t stream) {
-  using L = TcLayout<BN, STAGES, SWAP, KSUB>;
-  auto kern = tc_gemm_kernel<BN, STAGES, SWAP, KSUB>;
+  using L = TcLayout<BN, STAGES, SWAP, KSUB, PAIR>;
+  auto kern = tc_gemm_kernel<BN, STAGES, SWAP, KSUB, PAIR>;
   static bool configured = false;  // the attribute is per function, process-wide
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<p.sched.grid, kTcThreads, L::kAlloc, stream>>>(a, b, c, p);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * p.sched.grid, 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
+  } else {
+    kern<<<p.sched.grid, kTcThreads, L::kAlloc, stream>>>(a, b, c, p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
 int tc_smem_bytes(int bn, bool swapped) {
-  if (!swapped) return TcLayout<kGemmBN, kGemmStages, false, 1>::kAlloc;
+  if (!swapped) return TcLayout<kGemmBN, kGemmStages, false, 1, false>::kAlloc;
   switch (bn) {
-    case 16: return TcLayout<16, skinny_stages(16), true, kSkinnyKsub>::kAlloc;
-    case 32: return TcLayout<32, skinny_stages(32), true, kSkinnyKsub>::kAlloc;
-    default: return TcLayout<64, skinny_stages(64), true, kSkinnyKsub>::kAlloc;
+    case 16: return TcLayout<16, skinny_stages(16), true, kSkinnyKsub, false>::kAlloc;
+    case 32: return TcLayout<32, skinny_stages(32), true, kSkinnyKsub, false>::kAlloc;
+    default: return TcLayout<64, skinny_stages(64), true, kSkinnyKsub, false>::kAlloc;
   }
 }
 
 cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const TcParams& p, cudaStream_t stream) {
-  return launch_variant<kGemmBN, kGemmStages, false, 1>(tmA, tmB, tmC, p, stream);
+  return launch_variant<kGemmBN, kGemmStages, false, 1, false>(tmA, tmB, tmC, p, stream);
+}
+
+cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                const TcParams& p, cudaStream_t stream) {
+  return launch_variant<kGemmBN, kPairStages, false, 1, true>(tmA, tmB, tmC, p, stream);
 }
 
 cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
                              cudaStream_t stream) {
   switch (bn) {
-    case 16: return launch_variant<16, skinny_stages(16), true, kSkinnyKsub>(tmW, tmX, tmX, p, stream);
-    case 32: return launch_variant<32, skinny_stages(32), true, kSkinnyKsub>(tmW, tmX, tmX, p, stream);
-    case 64: return launch_variant<64, skinny_stages(64), true, kSkinnyKsub>(tmW, tmX, tmX, p, stream);
+    case 16: return launch_variant<16, skinny_stages(16), true, kSkinnyKsub, false>(tmW, tmX, tmX, p, stream);
+    case 32: return launch_variant<32, skinny_stages(32), true, kSkinnyKsub, false>(tmW, tmX, tmX, p, stream);
+    case 64: return launch_variant<64, skinny_stages(64), true, kSkinnyKsub, false>(tmW, tmX, tmX, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -16,6 +16,7 @@ constexpr int kBM = 128;  // MMA M (tile rows; weight rows on the swapped path)
 constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
 constexpr int kGemmBN = 256;
 constexpr int kGemmStages = 4;
+constexpr int kPairStages = 6;  // paired tiles: 32 KB per stage per CTA
 // Skinny (swapped) path: each stage holds kSkinnyKsub consecutive 64-wide k boxes
 // of 128 weight rows, so a weight row is read kSkinnyKsub * 128 contiguous bytes
 // at a time; the ring takes as many stages as fit in 224 KB of shared memory.
@@ -40,6 +41,10 @@ struct TcParams {
 // Non-swapped GEMM: A-operand = A (rows M), B-operand = B (rows N), BN = 256.
 cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const TcParams& p, cudaStream_t stream);
+
+// Paired GEMM over clusters of two CTAs: 256 x 256 tiles, p.sched counts pairs.
+cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                const TcParams& p, cudaStream_t stream);
 
 // Swapped skinny GEMM: A-operand = weights B (rows N), B-operand = activations A
 // (rows M <= bn), bn in {16, 32, 64}.

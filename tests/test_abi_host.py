@@ -80,6 +80,8 @@ def test_empty_problems_are_noops(lib):
 def test_gemv_rejects_large_m_and_bad_path(lib):
     assert lib.gemv_bf16(16, 16, 16, 65, 8, 8, 8, 8, 8, None) == sg.SG_ERR_INVALID_ARG
     assert lib.gemv_bf16_path(16, 16, 16, 4, 8, 8, 8, 8, 8, 7, None) == sg.SG_ERR_INVALID_ARG
+    assert lib.gemm_bf16_path(16, 16, 16, 4, 8, 8, 8, 8, 8, 5, None) == sg.SG_ERR_INVALID_ARG
+    assert lib.gemm_bf16_path(16, 16, 16, 65, 8, 8, 8, 8, 8, sg.PATH_CUDA_CORE, None) == sg.SG_ERR_INVALID_ARG
 
 
 def _golden_rows(name):
@@ -150,17 +152,28 @@ def _check_plan_coverage(info):
                                    (4096, 11008, 4096), (4096, 4096, 11008), (8192, 8192, 8192),
                                    (65, 257, 4104), (1000, 3000, 200), (129, 8, 64)])
 @pytest.mark.parametrize("sms", [148, 152, 170])
-def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms):
-    info = sg.plan(M, N, K, sms, 0)
-    assert info["path"] == sg.PATH_GEMM
-    assert info["tile_m"] == 128 and info["tile_n"] == 256 and info["tile_k"] == 64
-    assert info["tiles_m"] == -(-M // 128) and info["tiles_n"] == -(-N // 256)
-    assert info["grid"] <= sms
+@pytest.mark.parametrize("path", [sg.PATH_GEMM, sg.PATH_GEMM_PAIR])
+def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms, path):
+    info = sg.plan(M, N, K, sms, path)
+    pair = path == sg.PATH_GEMM_PAIR
+    assert info["path"] == path and info["cluster_size"] == (2 if pair else 1)
+    tm = 256 if pair else 128
+    units = sms // 2 if pair else sms
+    assert info["tile_m"] == tm and info["tile_n"] == 256 and info["tile_k"] == 64
+    assert info["tiles_m"] == -(-M // tm) and info["tiles_n"] == -(-N // 256)
+    assert info["grid"] <= units
     T = info["tiles_m"] * info["tiles_n"]
     assert info["dp_tiles"] + info["sk_tiles"] == T
-    if T >= sms and T % sms:
-        assert sms < info["sk_tiles"] < 2 * sms  # Stream-K over one wave plus the remainder
+    if T >= units and T % units:
+        assert units < info["sk_tiles"] < 2 * units  # Stream-K over one wave plus the remainder
     _check_plan_coverage(info)
+
+
+def test_auto_gemm_kernel_choice(lib):
+    assert sg.plan(128, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM
+    assert sg.plan(255, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM
+    assert sg.plan(256, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM_PAIR
+    assert sg.plan(4096, 4096, 4096, 152, 0)["grid"] == 76
 
 
 @pytest.mark.parametrize("M", [1, 2, 9, 16, 17, 33, 64])

@@ -19,7 +19,10 @@ pytestmark = pytest.mark.gpu
 import skinny_gemv_gb300 as sg  # noqa: E402
 
 
-def _run(A_bits, B_bits, M, N, K, ldc=None, fill=None):
+GEMM_PATHS = [sg.PATH_GEMM, sg.PATH_GEMM_PAIR]
+
+
+def _run(A_bits, B_bits, M, N, K, ldc=None, fill=None, path=sg.PATH_AUTO):
     A = to_device(A_bits, K)
     B = to_device(B_bits, K)
     ldc = -(-N // 8) * 8 if ldc is None else ldc  # 16-byte row pitch
@@ -27,24 +30,26 @@ def _run(A_bits, B_bits, M, N, K, ldc=None, fill=None):
     if fill is not None:
         Cfull.view(torch.int16).fill_(fill)
     C = Cfull[:, :N]
-    sg.gemm_bf16(A, B, C)
+    sg.gemm_bf16(A, B, C, path=path)
     torch.cuda.synchronize()
     return to_bits(Cfull)[:, :N]
 
 
+@pytest.mark.parametrize("path", GEMM_PATHS)
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 256), (200, 300, 192), (130, 257, 128),
-                                   (1024, 768, 256), (300, 1000, 64)])
-def test_exact_integers_pm1(M, N, K):
+                                   (1024, 768, 256), (300, 1000, 64), (512, 256, 1024)])
+def test_exact_integers_pm1(M, N, K, path):
     A = syn.small_int_matrix(M, K, -1, 1, 1000 + M)
     B = syn.small_int_matrix(N, K, -1, 1, 2000 + N)
-    assert_exact(_run(A, B, M, N, K), oracle.gemm(A, B), f"pm1 {M}x{N}x{K}")
+    assert_exact(_run(A, B, M, N, K, path=path), oracle.gemm(A, B), f"pm1 {M}x{N}x{K} path {path}")
 
 
+@pytest.mark.parametrize("path", GEMM_PATHS)
 @pytest.mark.parametrize("M,N,K", [(192, 320, 16), (129, 129, 8)])
-def test_exact_integers_pm4(M, N, K):
+def test_exact_integers_pm4(M, N, K, path):
     A = syn.small_int_matrix(M, K, -4, 4, 3000 + M)
     B = syn.small_int_matrix(N, K, -4, 4, 4000 + N)
-    assert_exact(_run(A, B, M, N, K), oracle.gemm(A, B), f"pm4 {M}x{N}x{K}")
+    assert_exact(_run(A, B, M, N, K, path=path), oracle.gemm(A, B), f"pm4 {M}x{N}x{K} path {path}")
 
 
 def test_identity_and_permutation():
@@ -67,14 +72,15 @@ def test_one_hot_rows_select_weight_columns():
     assert_exact(_run(syn.f64_to_bf16_bits(H), B, M, N, K), bf16_f64(B)[:, hot].T, "one-hot")
 
 
+@pytest.mark.parametrize("path", GEMM_PATHS)
 @pytest.mark.parametrize("M,N,K", [
     (65, 1, 8), (65, 8, 16), (127, 9, 24), (129, 255, 72), (200, 257, 4104), (513, 1000, 200),
-    (1000, 520, 1000), (64 + 128 * 3, 256 * 2 + 8, 64 * 5 + 8),
+    (1000, 520, 1000), (64 + 128 * 3, 256 * 2 + 8, 64 * 5 + 8), (2500, 1300, 704),
 ])
-def test_ragged_shapes(M, N, K):
+def test_ragged_shapes(M, N, K, path):
     A = syn.matrix(M, K, "uniform", 5000 + M)
     B = syn.matrix(N, K, "uniform", 6000 + N)
-    assert_close(_run(A, B, M, N, K), oracle.gemm(A, B), K, f"ragged {M}x{N}x{K}")
+    assert_close(_run(A, B, M, N, K, path=path), oracle.gemm(A, B), K, f"ragged {M}x{N}x{K} path {path}")
 
 
 def test_padded_strides_and_guard_band():
@@ -96,21 +102,23 @@ def test_padded_strides_and_guard_band():
     assert np.all(out[M:, :] == sentinel), "rows after C were written"
 
 
+@pytest.mark.parametrize("path", GEMM_PATHS)
 @pytest.mark.parametrize("name", ["sq512", "sq2048"])
-def test_workload_full_oracle(name):
+def test_workload_full_oracle(name, path):
     w = syn.WORKLOADS[name]
     A, B = w.a(), w.b()
-    assert_close(_run(A, B, w.M, w.N, w.K), oracle.gemm(A, B), w.K, name)
+    assert_close(_run(A, B, w.M, w.N, w.K, path=path), oracle.gemm(A, B), w.K, f"{name} path {path}")
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (1000, 3000, 1000), (384, 512, 8192)])
-def test_deterministic_across_runs(M, N, K):
+@pytest.mark.parametrize("path", GEMM_PATHS)
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (1000, 3000, 1000), (384, 512, 8192), (4096, 4096, 1024)])
+def test_deterministic_across_runs(M, N, K, path):
     A = to_device(syn.matrix(M, K, "uniform", 90))
     B = to_device(syn.matrix(N, K, "uniform", 91))
-    C1 = sg.gemm_bf16(A, B)
+    C1 = sg.gemm_bf16(A, B, path=path)
     C2 = torch.empty_like(C1)
     for _ in range(3):
-        sg.gemm_bf16(A, B, C2)
+        sg.gemm_bf16(A, B, C2, path=path)
         torch.cuda.synchronize()
         assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
 
