@@ -139,10 +139,15 @@ SG_HD double wave_efficiency(int64_t ctas, int64_t slots) {
   return static_cast<double>(ctas) / static_cast<double>(slots) / static_cast<double>(waves);
 }
 
+// Smallest Stream-K share (k-steps per CTA) for which the remainder tiles alone
+// are split; below it the last full wave joins the Stream-K region.
+constexpr int64_t kMinSkStepsPerCta = 16;
+
 // Builds the schedule.
 //
-// tiles >= CTAs: whole-tile waves, with the last full wave plus the remainder cut
-//   by Stream-K when the tile count is not a multiple of the CTA count.
+// tiles >= CTAs: whole-tile waves; when the tile count is not a multiple of the
+//   CTA count, the remainder tiles (plus the last full wave if the remainder is
+//   thin) are cut by Stream-K.
 // tiles < CTAs, memory-bound (fill_grid): every tile is split along K so that
 //   all `num_ctas` CTAs stream an equal share (at least min_units_per_cta k-steps
 //   each); the weight stream needs every SM's load bandwidth.
@@ -165,8 +170,14 @@ inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps,
     if (rem == 0 || k_steps < 2) {
       s.dp_tiles = static_cast<int32_t>(T);
       s.sk_tiles = 0;
+    } else if (rem * k_steps >= kMinSkStepsPerCta * G) {
+      // Stream-K over the remainder only: every CTA still gets a piece of at
+      // least kMinSkStepsPerCta k-steps, and fewer tiles exchange partial sums.
+      s.sk_tiles = static_cast<int32_t>(rem);
+      s.dp_tiles = static_cast<int32_t>(T - rem);
     } else {
-      // Stream-K over the last full wave plus the remainder: 1 < waves < 2.
+      // A thin remainder: Stream-K over the last full wave plus the remainder
+      // (1 < waves < 2), so no piece is tiny.
       s.sk_tiles = static_cast<int32_t>(rem + G);
       s.dp_tiles = static_cast<int32_t>(T - s.sk_tiles);
     }
