@@ -183,6 +183,18 @@ SG_API int sg_check_device_errors(sg_stream_t stream, uint32_t detail[4]);
  */
 SG_API void sg_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * sg_debug_inject_missing_tx -- failure injection for tests of the bounded
+ * waits.  The next tcgen05 GEMM launch on any device (gemm_bf16 with M > 64)
+ * arms the first pipeline stage of every CTA with `bytes` more than its copies
+ * deliver, so the MMA issuer's wait can never complete: the kernel gives up
+ * after the wait bound (sg_set_wait_timeout_ns), records the timeout, unwinds
+ * and exits, and sg_check_device_errors then returns SG_ERR_TIMEOUT.  The
+ * output of that launch is undefined.  bytes = 0 cancels a pending injection.
+ * The injection is consumed by one launch.
+ */
+SG_API void sg_debug_inject_missing_tx(uint32_t bytes);
+
 /* --------------------------------------------------------------------------
  * Planning (host only; no CUDA call is made, usable without a GPU)
  * -------------------------------------------------------------------------- */

@@ -102,6 +102,8 @@ def load(build_if_missing: bool = False):
     lib.sg_check_device_errors.restype = ctypes.c_int
     lib.sg_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.sg_set_wait_timeout_ns.restype = None
+    lib.sg_debug_inject_missing_tx.argtypes = [ctypes.c_uint32]
+    lib.sg_debug_inject_missing_tx.restype = None
     lib.sg_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.sg_plan.restype = ctypes.c_int
     lib.sg_plan_item.argtypes = [ctypes.POINTER(PlanInfo), i32, i32, ctypes.POINTER(ctypes.c_int32)]

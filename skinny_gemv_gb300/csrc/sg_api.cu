@@ -22,6 +22,7 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<uint32_t> g_inject_missing_tx{0};  // consumed by the next tcgen05 GEMM launch
 
 int cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -202,6 +203,8 @@ Schedule sched_from_plan(const sg_plan_info& o) {
   s.sk_tiles = o.sk_tiles;
   s.sk_units = o.sk_units;
   s.group_m = o.group_m;
+  s.sk_q = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units / s.grid) : 0;
+  s.sk_r = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units % s.grid) : 0;
   return s;
 }
 
@@ -322,6 +325,7 @@ int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, 
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
+  p.inject_extra_tx = g_inject_missing_tx.exchange(0);
   cudaError_t e = pair ? launch_tc_gemm_pair(ta, tb, tc, p, stream) : launch_tc_gemm(ta, tb, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
@@ -454,6 +458,8 @@ const char* sg_status_string(int status) {
 int sg_last_cuda_error(void) { return g_last_cuda_error; }
 
 void sg_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns < 1000000ull ? 1000000ull : ns); }
+
+void sg_debug_inject_missing_tx(uint32_t bytes) { g_inject_missing_tx.store(bytes); }
 
 int sg_check_device_errors(sg_stream_t stream, uint32_t detail[4]) {
   DeviceState* d = nullptr;

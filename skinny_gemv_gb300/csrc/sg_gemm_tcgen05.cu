@@ -52,7 +52,11 @@ struct TcLayout {
   static constexpr int kABytes = KSUB * kASub;
   static constexpr int kBBytes = KSUB * kBSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  // epilogue warps: one per TMEM lane quarter (eight, two per quarter, measured
+  // no faster and would cap registers at 168)
   static constexpr int kEpiWarps = 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kColsPerEpiWarp = BN / (kEpiWarps / 4);
   static constexpr int kStagingBufBytes = 32 * 64;  // 32 rows x 32 bf16
   static constexpr int kStagingBufs = 2;            // per epilogue warp
   static constexpr int kAOff = 0;
@@ -89,7 +93,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using L = TcLayout<BN, STAGES, SWAP, KSUB, PAIR>;
@@ -149,6 +153,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The set-up above touched no global memory, so it may overlap the previous
+  // kernel's tail; every global access below comes after the dependency wait.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -171,18 +179,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           const int nsub = min(KSUB, kboxes - ks * KSUB);  // boxes past K are skipped
-          const uint32_t bytes = static_cast<uint32_t>(nsub * (L::kASub + L::kBSub));
+          uint32_t bytes = static_cast<uint32_t>(nsub * (L::kASub + L::kBSub));
+          const uint32_t extra = (it == 0) ? p.inject_extra_tx : 0u;  // failure injection only
           if constexpr (PAIR) {
             // the leader's full barrier counts both CTAs' bytes
             const uint32_t full_leader = mapa_shared(smem_u32(&full[s]), 0);
-            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * bytes);
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * bytes + extra);
             for (int j = 0; j < nsub; ++j) {
               const int kx = (ks * KSUB + j) * kBK;
               tma_load_2d_pair(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, arow, full_leader);
               tma_load_2d_pair(smem + L::kBOff + s * L::kBBytes + j * L::kBSub, &tmB, kx, brow, full_leader);
             }
           } else {
-            mbar_arrive_expect_tx(&full[s], bytes);
+            mbar_arrive_expect_tx(&full[s], bytes + extra);
             for (int j = 0; j < nsub; ++j) {
               const int kx = (ks * KSUB + j) * kBK;
               tma_load_2d(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, arow, &full[s]);
@@ -269,10 +278,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    const int ew = warp - 2;                      // epilogue warp index
+    const int chunk_lo = (ew / 4) * (L::kColsPerEpiWarp / L::kChunk);  // this warp's columns
+    const int chunk_hi = chunk_lo + L::kColsPerEpiWarp / L::kChunk;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const int epi_tid = threadIdx.x - 64;  // 0..127
+    const int epi_tid = threadIdx.x - 64;  // 0 .. 32 * kEpiWarps - 1
     uint32_t store_count = 0;
-    uint8_t* staging = smem + L::kStagingOff + q * L::kStagingBufs * L::kStagingBufBytes;
+    uint8_t* staging = smem + L::kStagingOff + ew * L::kStagingBufs * L::kStagingBufBytes;
     // the accumulator-free barrier lives in the pair's MMA-issuing CTA
     const uint32_t tmem_empty_addr0 = PAIR ? mapa_shared(smem_u32(&tmem_empty[0]), 0) : smem_u32(&tmem_empty[0]);
 
@@ -340,7 +352,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     };
 
-    constexpr int kChunks = BN / L::kChunk;
     constexpr int kQuads = L::kChunk / 4;
     constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * BN;  // one CTA's share of a tile
     for (int i = 0; i < nitems; ++i) {
@@ -361,7 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tacc = tmem_base + lane_off + b * BN;
       float v[L::kChunk];
       if (w.npieces == 1) {
-        for (int j = 0; j < kChunks; ++j) {
+        for (int j = chunk_lo; j < chunk_hi; ++j) {
           load_chunk(tacc + j * L::kChunk, v);
           emit_chunk(v, tm, tn, j);
         }
@@ -372,7 +383,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int64_t my_slot = PAIR ? 2 * static_cast<int64_t>(w.slot) + rank : w.slot;
         const int counter = PAIR ? 2 * w.sk_index + static_cast<int>(rank) : w.sk_index;
         float4* slot = reinterpret_cast<float4*>(p.partials + my_slot * kSlotFloats);
-        for (int j = 0; j < kChunks; ++j) {
+        for (int j = chunk_lo; j < chunk_hi; ++j) {
           load_chunk(tacc + j * L::kChunk, v);
 #pragma unroll
           for (int q4 = 0; q4 < kQuads; ++q4)
@@ -380,41 +391,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         release_accumulator(b);
         __threadfence();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 32 * L::kEpiWarps);
         if (epi_tid == 0) {
           const uint32_t before = atomicAdd(&p.counters[counter], 1u);
           *sk_last = (before == static_cast<uint32_t>(w.npieces - 1)) ? 1u : 0u;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 32 * L::kEpiWarps);
         if (*sk_last) {
           // Last arrival: sum all pieces in k order, then store.
           __threadfence();
-          for (int j = 0; j < kChunks; ++j) {
+          // Loads in flight per batch: kBatch pieces x kBQuads float4 of one chunk.
+          constexpr int kBatch = kQuads <= 4 ? 4 : 2;  // pieces per batch (16 loads in flight)
+          constexpr int kBQuads = kQuads;                // float4 per piece per batch: the whole chunk
+          for (int j = chunk_lo; j < chunk_hi; ++j) {
             float acc[L::kChunk];
-            // Two pieces per batch: 2 x kQuads independent loads in flight.
-            for (int pj = 0; pj < w.npieces; pj += 2) {
-              const bool pair = pj + 1 < w.npieces;
-              const int64_t sl0 = piece_slot(sched, w.sk_index, pj);
-              const int64_t sl1 = piece_slot(sched, w.sk_index, pair ? pj + 1 : pj);
-              const float4* s0 = reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl0 + rank : sl0) * kSlotFloats);
-              const float4* s1 = reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl1 + rank : sl1) * kSlotFloats);
-              float4 x0[kQuads], x1[kQuads];
 #pragma unroll
-              for (int q4 = 0; q4 < kQuads; ++q4) x0[q4] = __ldcg(&s0[(j * kQuads + q4) * kBM + row]);
-              if (pair) {
+            for (int h = 0; h < kQuads / kBQuads; ++h) {
+              for (int pj = 0; pj < w.npieces; pj += kBatch) {
+                float4 x[kBatch][kBQuads];
 #pragma unroll
-                for (int q4 = 0; q4 < kQuads; ++q4) x1[q4] = __ldcg(&s1[(j * kQuads + q4) * kBM + row]);
-              }
+                for (int bi = 0; bi < kBatch; ++bi) {
+                  if (pj + bi < w.npieces) {
+                    const int64_t sl = piece_slot(sched, w.sk_index, pj + bi);
+                    const float4* src =
+                        reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl + rank : sl) * kSlotFloats);
 #pragma unroll
-              for (int q4 = 0; q4 < kQuads; ++q4) {
-                float* a4 = &acc[4 * q4];
-                if (pj == 0) {
-                  a4[0] = x0[q4].x; a4[1] = x0[q4].y; a4[2] = x0[q4].z; a4[3] = x0[q4].w;
-                } else {
-                  a4[0] += x0[q4].x; a4[1] += x0[q4].y; a4[2] += x0[q4].z; a4[3] += x0[q4].w;
+                    for (int q4 = 0; q4 < kBQuads; ++q4)
+                      x[bi][q4] = __ldcg(&src[(j * kQuads + h * kBQuads + q4) * kBM + row]);
+                  }
                 }
-                if (pair) {  // k order: piece pj, then pj + 1
-                  a4[0] += x1[q4].x; a4[1] += x1[q4].y; a4[2] += x1[q4].z; a4[3] += x1[q4].w;
+#pragma unroll
+                for (int bi = 0; bi < kBatch; ++bi) {  // k order: pieces pj, pj + 1, ...
+                  if (pj + bi < w.npieces) {
+#pragma unroll
+                    for (int q4 = 0; q4 < kBQuads; ++q4) {
+                      float* a4 = &acc[4 * (h * kBQuads + q4)];
+                      if (pj + bi == 0) {
+                        a4[0] = x[bi][q4].x; a4[1] = x[bi][q4].y; a4[2] = x[bi][q4].z; a4[3] = x[bi][q4].w;
+                      } else {
+                        a4[0] += x[bi][q4].x; a4[1] += x[bi][q4].y; a4[2] += x[bi][q4].z; a4[3] += x[bi][q4].w;
+                      }
+                    }
+                  }
                 }
               }
             }
@@ -452,24 +470,21 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if constexpr (PAIR) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * p.sched.grid, 1, 1);
-    cfg.blockDim = dim3(kTcThreads, 1, 1);
-    cfg.dynamicSmemBytes = L::kAlloc;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
-  } else {
-    kern<<<p.sched.grid, kTcThreads, L::kAlloc, stream>>>(a, b, c, p);
-    return cudaGetLastError();
-  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((PAIR ? 2 : 1) * p.sched.grid, 1, 1);
+  cfg.blockDim = dim3(L::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
 }
 
 }  // namespace

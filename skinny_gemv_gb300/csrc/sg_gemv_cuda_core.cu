@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 
 #include "sg_internal.h"
+#include "sg_ptx.cuh"
 
 namespace sg {
 namespace {
@@ -64,6 +65,8 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   const int v_lo = kb / 8 + (warp * nvec) / kCcWarps;
   const int v_hi = kb / 8 + ((warp + 1) * nvec) / kCcWarps;
   const int tail_k = kb + nvec * 8;  // [tail_k, ke): fewer than 8 elements, warp 0
+  grid_launch_dependents();
+  grid_dependency_wait();  // no global access before the previous kernel has completed
 
   for (int r0 = row_lo; r0 < row_hi; r0 += R) {
     float acc[R][MT];
@@ -180,9 +183,17 @@ cudaError_t launch_one(const CcParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(p.grid_rows, p.split_k);
-  kern<<<grid, kCcWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid_rows, p.split_k, 1);
+  cfg.blockDim = dim3(kCcWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace

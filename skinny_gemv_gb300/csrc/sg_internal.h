@@ -24,7 +24,7 @@ constexpr int kSkinnyKsub = 4;
 constexpr int skinny_stages(int bn) {
   return (224 * 1024) / (kSkinnyKsub * (kBM + bn) * kBK * 2) < 2 ? 2 : (224 * 1024) / (kSkinnyKsub * (kBM + bn) * kBK * 2);
 }
-constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// tcgen05 kernels: warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps.
 
 // Everything a tcgen05 launch needs besides its tensor maps.
 struct TcParams {
@@ -36,6 +36,7 @@ struct TcParams {
   uint32_t* counters;    // one arrival counter per Stream-K tile
   DeviceError* err;
   uint64_t timeout_ns;
+  uint32_t inject_extra_tx;  // failure injection: extra bytes expected on the first stage
 };
 
 // Non-swapped GEMM: A-operand = A (rows M), B-operand = B (rows N), BN = 256.

@@ -50,6 +50,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Blocks until every grid this one depends on (the previous kernel on the
+// stream, when both were launched with programmatic stream serialisation) has
+// completed and its memory operations are visible.  Without such a dependency it
+// returns at once.  Every thread calls it before its first global-memory access.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel on the stream begin launching (its blocks still wait in
+// grid_dependency_wait until this grid has completed).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -43,8 +43,10 @@ struct Schedule {
   int32_t grid;      // persistent CTAs launched
   int32_t dp_tiles;  // whole tiles handed out round-robin
   int32_t sk_tiles;  // tiles split by Stream-K
-  int64_t sk_units;  // sk_tiles * k_steps
+  int64_t sk_units;  // sk_tiles * k_steps (< 2^31)
   int32_t group_m;   // raster group height in tiles (L2 locality)
+  int32_t sk_q;      // Stream-K units per CTA: sk_units / grid ...
+  int32_t sk_r;      // ... and the first sk_r CTAs take one more (sk_units % grid)
   int32_t pad;
 };
 
@@ -57,18 +59,24 @@ struct WorkItem {
   int32_t sk_index;  // tile index inside the Stream-K region (arrival counter)
 };
 
-SG_HD int64_t sk_range_begin(const Schedule& s, int64_t c) { return (c * s.sk_units) / s.grid; }
+// Stream-K ranges: CTA c takes units [begin(c), begin(c + 1)), the first sk_r
+// CTAs sk_q + 1 units each and the rest sk_q.  32-bit arithmetic throughout: the
+// scheduler runs in every role of every CTA before its first copy is issued.
+SG_HD int32_t sk_range_begin(const Schedule& s, int32_t c) {
+  return c * s.sk_q + (c < s.sk_r ? c : s.sk_r);
+}
 
-// The CTA whose range holds Stream-K unit u: the largest c with begin(c) <= u.
-SG_HD int64_t sk_owner(const Schedule& s, int64_t u) {
-  return ((u + 1) * s.grid + s.sk_units - 1) / s.sk_units - 1;
+// The CTA whose range holds Stream-K unit u.
+SG_HD int32_t sk_owner(const Schedule& s, int32_t u) {
+  const int32_t big = s.sk_r * (s.sk_q + 1);  // units held by the sk_r larger ranges
+  return u < big ? u / (s.sk_q + 1) : s.sk_r + (u - big) / s.sk_q;
 }
 
 // Slot of CTA c's piece of SK tile t: 0 if the piece is the first item of c's
 // range (the range starts inside tile t), else 1.
-SG_HD int32_t sk_slot(const Schedule& s, int64_t c, int64_t t) {
-  const int64_t first_tile = sk_range_begin(s, c) / s.k_steps;
-  return static_cast<int32_t>(2 * c + (first_tile == t ? 0 : 1));
+SG_HD int32_t sk_slot(const Schedule& s, int32_t c, int32_t t) {
+  const int32_t first_tile = sk_range_begin(s, c) / s.k_steps;
+  return 2 * c + (first_tile == t ? 0 : 1);
 }
 
 SG_HD int32_t dp_count(const Schedule& s, int32_t c) {
@@ -78,8 +86,8 @@ SG_HD int32_t dp_count(const Schedule& s, int32_t c) {
 // Number of Stream-K pieces of CTA c.
 SG_HD int32_t sk_count(const Schedule& s, int32_t c) {
   if (s.sk_tiles <= 0) return 0;
-  const int64_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
-  return u1 > u0 ? static_cast<int32_t>((u1 - 1) / s.k_steps - u0 / s.k_steps + 1) : 0;
+  const int32_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
+  return u1 > u0 ? (u1 - 1) / s.k_steps - u0 / s.k_steps + 1 : 0;
 }
 
 // Number of work items of CTA c.
@@ -100,23 +108,23 @@ SG_HD WorkItem get_item(const Schedule& s, int32_t c, int32_t i) {
     w.sk_index = -1;
     return w;
   }
-  const int64_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
-  const int64_t t = u0 / s.k_steps + i;
-  const int64_t tb = t * s.k_steps, te = tb + s.k_steps;
-  w.tile = static_cast<int32_t>(t);
-  w.k0 = static_cast<int32_t>((u0 > tb ? u0 : tb) - tb);
-  w.k1 = static_cast<int32_t>((u1 < te ? u1 : te) - tb);
-  const int64_t first = sk_owner(s, tb), last = sk_owner(s, te - 1);
-  w.piece = static_cast<int32_t>(c - first);
-  w.npieces = static_cast<int32_t>(last - first + 1);
+  const int32_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
+  const int32_t t = u0 / s.k_steps + i;
+  const int32_t tb = t * s.k_steps, te = tb + s.k_steps;
+  w.tile = t;
+  w.k0 = (u0 > tb ? u0 : tb) - tb;
+  w.k1 = (u1 < te ? u1 : te) - tb;
+  const int32_t first = sk_owner(s, tb), last = sk_owner(s, te - 1);
+  w.piece = c - first;
+  w.npieces = last - first + 1;
   w.slot = w.npieces > 1 ? sk_slot(s, c, t) : -1;
-  w.sk_index = static_cast<int32_t>(t);
+  w.sk_index = t;
   return w;
 }
 
 // Slot of piece j of Stream-K tile t (t counted inside the Stream-K region).
-SG_HD int32_t piece_slot(const Schedule& s, int64_t t, int32_t j) {
-  const int64_t c = sk_owner(s, t * s.k_steps) + j;
+SG_HD int32_t piece_slot(const Schedule& s, int32_t t, int32_t j) {
+  const int32_t c = sk_owner(s, t * s.k_steps) + j;
   return sk_slot(s, c, t);
 }
 
@@ -143,6 +151,11 @@ SG_HD double wave_efficiency(int64_t ctas, int64_t slots) {
 // are split; below it the last full wave joins the Stream-K region.
 constexpr int64_t kMinSkStepsPerCta = 16;
 
+// What one partial-sum exchange costs, in k-steps of main-loop time (a piece's
+// fp32 partial of 128 KB per CTA written, fenced, counted and read back).
+// Stream-K is used only when the wave-quantisation time it saves is larger.
+constexpr int64_t kSkFixupCostSteps = 24;
+
 // Builds the schedule.
 //
 // tiles >= CTAs: whole-tile waves; when the tile count is not a multiple of the
@@ -167,7 +180,9 @@ inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps,
   if (T >= G) {
     const int64_t rem = T % G;
     s.grid = static_cast<int32_t>(G);
-    if (rem == 0 || k_steps < 2) {
+    // whole-tile waves lose (G - rem) / G of a wave to quantisation
+    const bool sk_pays = fill_grid || (G - rem) * k_steps > kSkFixupCostSteps * G;
+    if (rem == 0 || k_steps < 2 || !sk_pays) {
       s.dp_tiles = static_cast<int32_t>(T);
       s.sk_tiles = 0;
     } else if (rem * k_steps >= kMinSkStepsPerCta * G) {
@@ -188,7 +203,9 @@ inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps,
       g = units / per;
       if (g > G) g = G;
     } else {
-      const int64_t split = G / T;  // >= 1
+      // s-way splits save k_steps * (1 - 1/s) per tile, which must beat a fixup
+      int64_t split = G / T;  // >= 1
+      if (split >= 2 && k_steps - k_steps / split <= kSkFixupCostSteps) split = 1;
       g = split >= 2 ? T * split : T;
       if (g > units / per) g = units / per;
     }
@@ -203,6 +220,13 @@ inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps,
     }
   }
   s.sk_units = static_cast<int64_t>(s.sk_tiles) * k_steps;
+  if (s.sk_units >= (int64_t{1} << 31) - int64_t{2} * s.grid) {  // keep the 32-bit unit math exact
+    s.dp_tiles += s.sk_tiles;
+    s.sk_tiles = 0;
+    s.sk_units = 0;
+  }
+  s.sk_q = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units / s.grid) : 0;
+  s.sk_r = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units % s.grid) : 0;
   return s;
 }
 

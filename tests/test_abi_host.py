@@ -39,7 +39,8 @@ def test_exports_every_declared_symbol(lib):
         # every entry point has a full ctypes prototype: without one, ctypes would
         # pass 64-bit pointers and sizes as 32-bit ints
         assert getattr(lib, n).argtypes is not None, f"{n} has no argtypes"
-        assert getattr(lib, n).restype is not None or n == "sg_set_wait_timeout_ns", n
+        assert getattr(lib, n).restype is not None or n in ("sg_set_wait_timeout_ns",
+                                                            "sg_debug_inject_missing_tx"), n
 
 
 def test_status_strings(lib):
@@ -165,12 +166,13 @@ def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms, path):
     T = info["tiles_m"] * info["tiles_n"]
     assert info["dp_tiles"] + info["sk_tiles"] == T
     if T >= units and T % units:
-        rem = T % units
-        # Stream-K over the remainder, plus the last full wave when the remainder is thin
-        if rem * info["k_steps"] >= 16 * units:
-            assert info["sk_tiles"] == rem
+        rem, KS = T % units, info["k_steps"]
+        if (units - rem) * KS <= 24 * units:
+            assert info["sk_tiles"] == 0  # quantisation costs less than a fixup
+        elif rem * KS >= 16 * units:
+            assert info["sk_tiles"] == rem  # Stream-K over the remainder
         else:
-            assert info["sk_tiles"] == rem + units
+            assert info["sk_tiles"] == rem + units  # thin remainder: plus the last wave
     _check_plan_coverage(info)
 
 
