@@ -236,12 +236,12 @@ int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
   o->path = SG_PATH_TENSOR_CORE;
-  o->tile_m = kBM;
+  o->tile_m = kSwapRows;
   o->tile_n = skinny_bn(M);
   o->tile_k = kBK * kSkinnyKsub;
   o->stages = skinny_stages(o->tile_n);
   o->cluster_size = 1;
-  const int32_t tm = static_cast<int32_t>(ceil_div(N, kBM));
+  const int32_t tm = static_cast<int32_t>(ceil_div(N, kSwapRows));
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK * kSkinnyKsub));
   const Schedule s = make_schedule(tm, 1, ks, sms, 2, 1, true);
   fill_sched(o, s);
@@ -335,7 +335,7 @@ int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C
   sg_plan_info plan;
   plan_tc_skinny(M, N, K, d.sm_count, &plan);
   CUtensorMap tw, tx;
-  int st = make_map(&tw, B, N, K, ldb, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  int st = make_map(&tw, B, N, K, ldb, kSwapRows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);

@@ -46,8 +46,11 @@ namespace {
 // PAIR: B's rows are split between the two CTAs of a pair (BN / 2 each).
 template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
 struct TcLayout {
+  // rows of the MMA's A operand per CTA: 128, or 64 weight rows on the swapped
+  // path (an M = 64 accumulator sits in lanes 0-15 of each TMEM lane quarter)
+  static constexpr int kARows = SWAP ? kSwapRows : kBM;
   static constexpr int kBRowsPerCta = PAIR ? BN / 2 : BN;
-  static constexpr int kASub = kBM * kBK * 2;  // 16 KB: one 128 x 64 box
+  static constexpr int kASub = kARows * kBK * 2;  // one kARows x 64 box
   static constexpr int kBSub = kBRowsPerCta * kBK * 2;
   static constexpr int kABytes = KSUB * kASub;
   static constexpr int kBBytes = KSUB * kBSub;
@@ -64,8 +67,9 @@ struct TcLayout {
   static constexpr int kStagingOff = kBOff + STAGES * kBBytes;
   static constexpr int kStagingBytes = SWAP ? 0 : kEpiWarps * kStagingBufs * kStagingBufBytes;
   static constexpr int kBarOff = kStagingOff + kStagingBytes;
-  // full[S], empty[S], tmem_full[2], tmem_empty[2], teardown
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  // full[S], empty[S], tmem_full[2], tmem_empty[2], teardown, fixup
+  static constexpr int kNumBars = 2 * STAGES + 6;
+  static constexpr int kRingBytes = STAGES * (kABytes + kBBytes);
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, sk flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -97,7 +101,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using L = TcLayout<BN, STAGES, SWAP, KSUB, PAIR>;
-  constexpr int kTileRows = PAIR ? 2 * kBM : kBM;  // output rows per tile (the MMA's M)
+  constexpr int kTileRows = PAIR ? 2 * kBM : L::kARows;  // output rows per tile (the MMA's M)
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, BN);
   const int kboxes = (p.K + kBK - 1) / kBK;  // 64-wide k boxes that hold data
 
@@ -109,6 +113,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
   uint64_t* tmem_full = bars + 2 * STAGES;
   uint64_t* tmem_empty = bars + 2 * STAGES + 2;
   uint64_t* teardown = bars + 2 * STAGES + 4;
+  uint64_t* fixup_bar = bars + 2 * STAGES + 5;  // bulk loads of Stream-K partials
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
   volatile uint32_t* sk_last = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 8);
@@ -130,6 +135,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
       mbar_init(&tmem_empty[b], L::kTmemEmptyCount);
     }
     mbar_init(teardown, 1);
+    mbar_init(fixup_bar, 1);
     *abort_flag = 0;
     *sk_last = 0;
     fence_mbar_init();
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
         const WorkItem w = get_item(sched, unit, i);
         int32_t tm, tn;
         tile_coords(sched, w.tile, tm, tn);
-        const int arow = tm * kTileRows + static_cast<int>(rank) * kBM;
+        const int arow = tm * kTileRows + static_cast<int>(rank) * L::kARows;
         const int brow = tn * BN + static_cast<int>(rank) * L::kBRowsPerCta;
         for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
           const uint32_t s = it % STAGES;
@@ -312,9 +318,10 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
         }
         ++store_count;
       } else {
-        // D[n][m]: this thread's row is weight row n, columns are activation rows m.
-        const int n = tm * kBM + row;
-        if (n < p.N) {
+        // D[n][m]: this thread's row is weight row n (M = 64 accumulator: lanes
+        // 0-15 of each lane quarter), columns are activation rows m.
+        const int n = tm * L::kARows + q * 16 + lane;
+        if (lane < 16 && n < p.N) {
           __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C);
 #pragma unroll
           for (int e = 0; e < L::kChunk; ++e) {
@@ -390,6 +397,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
             slot[(j * kQuads + q4) * kBM + row] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
         }
         release_accumulator(b);
+        fence_proxy_async_global();  // the finisher may read these bytes with bulk copies
         __threadfence();
         named_bar_sync(1, 32 * L::kEpiWarps);
         if (epi_tid == 0) {
@@ -397,7 +405,49 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
           *sk_last = (before == static_cast<uint32_t>(w.npieces - 1)) ? 1u : 0u;
         }
         named_bar_sync(1, 32 * L::kEpiWarps);
-        if (*sk_last) {
+        // The finisher's last item: the copy ring is idle (every stage of this CTA
+        // has been consumed), so all pieces' partials are fetched into it with
+        // bulk copies under one barrier instead of dependent rounds of loads.
+        const bool ring_fixup = *sk_last && i == nitems - 1 &&
+                                static_cast<int64_t>(w.npieces) * kSlotFloats * 4 <= L::kRingBytes;
+        if (ring_fixup) {
+          __threadfence();
+          float* ring = reinterpret_cast<float*>(smem);
+          if (epi_tid == 0) {
+            fence_proxy_async_global();
+            const uint32_t slot_bytes = static_cast<uint32_t>(kSlotFloats * 4);
+            mbar_arrive_expect_tx(fixup_bar, slot_bytes * static_cast<uint32_t>(w.npieces));
+            for (int pj = 0; pj < w.npieces; ++pj) {
+              const int64_t sl = piece_slot(sched, w.sk_index, pj);
+              bulk_load(ring + pj * kSlotFloats, p.partials + (PAIR ? 2 * sl + rank : sl) * kSlotFloats, slot_bytes,
+                        fixup_bar);
+            }
+          }
+          if (!mbar_wait(fixup_bar, 0, p.timeout_ns, abort_flag)) {
+            if (!*abort_flag) record_error(p.err, kDevTimeoutFull, 1000 + i);
+            *abort_flag = 1;
+          } else {
+            const float4* rs = reinterpret_cast<const float4*>(ring);
+            for (int j = chunk_lo; j < chunk_hi; ++j) {
+              float acc[L::kChunk];
+              for (int pj = 0; pj < w.npieces; ++pj) {  // k order
+                const float4* src = rs + pj * (kSlotFloats / 4);
+#pragma unroll
+                for (int q4 = 0; q4 < kQuads; ++q4) {
+                  const float4 x = src[(j * kQuads + q4) * kBM + row];
+                  float* a4 = &acc[4 * q4];
+                  if (pj == 0) {
+                    a4[0] = x.x; a4[1] = x.y; a4[2] = x.z; a4[3] = x.w;
+                  } else {
+                    a4[0] += x.x; a4[1] += x.y; a4[2] += x.z; a4[3] += x.w;
+                  }
+                }
+              }
+              emit_chunk(acc, tm, tn, j);
+            }
+          }
+          if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
+        } else if (*sk_last) {
           // Last arrival: sum all pieces in k order, then store.
           __threadfence();
           // Loads in flight per batch: kBatch pieces x kBQuads float4 of one chunk.

@@ -94,19 +94,24 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
       for (int u = 0; u < U; ++u) {
         const int vv = v + 32 * u;
         if (vv < v_hi) {
+          // activations of this k vector for every row (rows past M read as 0)
+          float a[MT][8];
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            if (m < p.M) {
-              float a[8];
-              bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(m) * p.lda + 8 * vv)), a);
+            const uint4 av = m < p.M
+                                 ? __ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(m) * p.lda + 8 * vv))
+                                 : make_uint4(0, 0, 0, 0);
+            bf16x8_to_f32(av, a[m]);
+          }
+          // each weight vector is widened once and used for all MT rows
 #pragma unroll
-              for (int r = 0; r < R; ++r) {
-                float w[8];
-                bf16x8_to_f32(wv[u][r], w);
+          for (int r = 0; r < R; ++r) {
+            float w[8];
+            bf16x8_to_f32(wv[u][r], w);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[r][m] = fmaf(w[e], a[e], acc[r][m]);
-              }
-            }
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[r][m] = fmaf(w[e], a[m][e], acc[r][m]);
           }
         }
       }

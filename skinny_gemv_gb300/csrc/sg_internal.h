@@ -21,8 +21,11 @@ constexpr int kPairStages = 6;  // paired tiles: 32 KB per stage per CTA
 // of 128 weight rows, so a weight row is read kSkinnyKsub * 128 contiguous bytes
 // at a time; the ring takes as many stages as fit in 224 KB of shared memory.
 constexpr int kSkinnyKsub = 4;
+constexpr int kSwapRows = 64;  // weight rows per tile on the swapped path (MMA M = 64)
 constexpr int skinny_stages(int bn) {
-  return (224 * 1024) / (kSkinnyKsub * (kBM + bn) * kBK * 2) < 2 ? 2 : (224 * 1024) / (kSkinnyKsub * (kBM + bn) * kBK * 2);
+  return (224 * 1024) / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2) < 2
+             ? 2
+             : (224 * 1024) / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2);
 }
 // tcgen05 kernels: warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps.
 

@@ -47,8 +47,14 @@ struct Schedule {
   int32_t group_m;   // raster group height in tiles (L2 locality)
   int32_t sk_q;      // Stream-K units per CTA: sk_units / grid ...
   int32_t sk_r;      // ... and the first sk_r CTAs take one more (sk_units % grid)
-  int32_t pad;
+  int32_t split;     // > 0: split mode (below); 0: waves + Stream-K
 };
+
+// Split mode (split = S > 0): every tile is cut into exactly S pieces of k-steps
+// [KS*p/S, KS*(p+1)/S), and CTA c runs piece c % S of tile c / S as its only
+// item.  Used where all CTAs are resident at once (memory-bound skinny GEMMs,
+// two CTAs per SM): the memory system then shares bandwidth among them, so no
+// CTA idles, and each tile's pieces end together.
 
 struct WorkItem {
   int32_t tile;      // linear tile index in raster order
@@ -91,12 +97,26 @@ SG_HD int32_t sk_count(const Schedule& s, int32_t c) {
 }
 
 // Number of work items of CTA c.
-SG_HD int32_t item_count(const Schedule& s, int32_t c) { return sk_count(s, c) + dp_count(s, c); }
+SG_HD int32_t item_count(const Schedule& s, int32_t c) {
+  if (s.split > 0) return c < s.tiles_m * s.tiles_n * s.split ? 1 : 0;
+  return sk_count(s, c) + dp_count(s, c);
+}
 
 // The i-th work item of CTA c (0 <= i < item_count(s, c)): its Stream-K pieces
 // first, then its whole tiles.
 SG_HD WorkItem get_item(const Schedule& s, int32_t c, int32_t i) {
   WorkItem w;
+  if (s.split > 0) {
+    const int32_t t = c / s.split, pc = c - t * s.split;
+    w.tile = t;
+    w.k0 = (s.k_steps * pc) / s.split;
+    w.k1 = (s.k_steps * (pc + 1)) / s.split;
+    w.piece = pc;
+    w.npieces = s.split;
+    w.slot = s.split > 1 ? c : -1;
+    w.sk_index = t;
+    return w;
+  }
   const int32_t nsk = sk_count(s, c);
   if (i >= nsk) {
     w.tile = s.sk_tiles + c + (i - nsk) * s.grid;
@@ -124,8 +144,24 @@ SG_HD WorkItem get_item(const Schedule& s, int32_t c, int32_t i) {
 
 // Slot of piece j of Stream-K tile t (t counted inside the Stream-K region).
 SG_HD int32_t piece_slot(const Schedule& s, int32_t t, int32_t j) {
+  if (s.split > 0) return t * s.split + j;
   const int32_t c = sk_owner(s, t * s.k_steps) + j;
   return sk_slot(s, c, t);
+}
+
+// Split-mode schedule: tiles_m x tiles_n tiles, each cut into `split` pieces.
+inline Schedule make_split_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps, int32_t split) {
+  Schedule s{};
+  s.tiles_m = tiles_m;
+  s.tiles_n = tiles_n;
+  s.k_steps = k_steps;
+  s.group_m = 1;
+  s.split = split < 1 ? 1 : (split > k_steps ? k_steps : split);
+  s.grid = tiles_m * tiles_n * s.split;
+  s.dp_tiles = 0;
+  s.sk_tiles = tiles_m * tiles_n;
+  s.sk_units = static_cast<int64_t>(s.sk_tiles) * k_steps;
+  return s;
 }
 
 // Grouped raster order: groups of group_m tile-rows, column-major inside a group,
@@ -185,7 +221,9 @@ inline Schedule make_schedule(int32_t tiles_m, int32_t tiles_n, int32_t k_steps,
     if (rem == 0 || k_steps < 2 || !sk_pays) {
       s.dp_tiles = static_cast<int32_t>(T);
       s.sk_tiles = 0;
-    } else if (rem * k_steps >= kMinSkStepsPerCta * G) {
+    } else if (fill_grid || rem * k_steps >= kMinSkStepsPerCta * G) {
+      // (memory-bound: small pieces cost no tensor efficiency, and each CTA then
+      // ends on a whole tile, so no partial exchange sits at the end)
       // Stream-K over the remainder only: every CTA still gets a piece of at
       // least kMinSkStepsPerCta k-steps, and fewer tiles exchange partial sums.
       s.sk_tiles = static_cast<int32_t>(rem);

@@ -189,8 +189,11 @@ def test_skinny_tensor_core_plan(lib, M, N, K):
     info = sg.plan(M, N, K, 152, sg.PATH_TENSOR_CORE)
     assert info["path"] == sg.PATH_TENSOR_CORE
     assert info["tile_n"] == (16 if M <= 16 else 32 if M <= 32 else 64)
-    assert info["tiles_n"] == 1 and info["tiles_m"] == -(-N // 128)
+    assert info["tile_m"] == 64 and info["tiles_n"] == 1 and info["tiles_m"] == -(-N // 64)
     items = _check_plan_coverage(info)
+    T = info["tiles_m"]
+    if T >= 152 and T % 152:
+        assert info["sk_tiles"] == T % 152  # only the remainder is split
     # the weights are read once: each weight tile's k-steps are covered exactly once
     assert sum(k1 - k0 for row in items for (_, k0, k1, *_) in row) == info["tiles_m"] * info["k_steps"]
 
