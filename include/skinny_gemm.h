@@ -210,11 +210,13 @@ typedef struct {
     int64_t sk_units;   /* sk_tiles * k_steps */
     int32_t group_m;    /* raster group height */
     int32_t stages;     /* shared-memory ring depth */
-    int32_t split_k;    /* CUDA-core path: K slices per row group */
+    int32_t split_k;    /* CUDA-core path: K slices per row group; tensor-core skinny
+                           path: k pieces per weight tile, one CTA each, every CTA
+                           resident at once (0: persistent schedule); else 0 */
     int32_t rows_per_cta; /* CUDA-core path: weight rows per CTA */
     double wave_efficiency; /* of one tile per CTA, (ctas/slots)/ceil(ctas/slots) */
     int32_t cluster_size; /* CTAs per schedule unit: 2 for SG_PATH_GEMM_PAIR, else 1 */
-    int32_t reserved;
+    int32_t ctas_per_sm;  /* CTAs the kernel keeps resident on one SM */
 } sg_plan_info;
 
 /*

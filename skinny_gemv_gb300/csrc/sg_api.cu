@@ -203,6 +203,7 @@ Schedule sched_from_plan(const sg_plan_info& o) {
   s.sk_tiles = o.sk_tiles;
   s.sk_units = o.sk_units;
   s.group_m = o.group_m;
+  s.split = o.path == SG_PATH_TENSOR_CORE ? o.split_k : 0;
   s.sk_q = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units / s.grid) : 0;
   s.sk_r = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units % s.grid) : 0;
   return s;
@@ -225,7 +226,8 @@ void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_i
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
   const Schedule s = make_schedule(tm, tn, ks, units, 4, std::min<int32_t>(tm, pair ? 4 : 8), false);
   fill_sched(o, s);
-  o->split_k = 1;
+  o->split_k = 0;
+  o->ctas_per_sm = 1;
   o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, units);
 }
 
@@ -233,6 +235,10 @@ bool auto_pair(int64_t M) { return M >= 2 * kBM; }
 
 int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
+// Swapped skinny plan: 64-row weight tiles, two CTAs per SM.  When every tile
+// fits in the resident slots, each tile is cut into split_k equal k pieces, one
+// CTA per piece, and all CTAs run at once (split mode); past that, a persistent
+// grid of two CTAs per SM walks the tiles with a Stream-K remainder.
 void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
   o->path = SG_PATH_TENSOR_CORE;
@@ -241,12 +247,21 @@ void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   o->tile_k = kBK * kSkinnyKsub;
   o->stages = skinny_stages(o->tile_n);
   o->cluster_size = 1;
+  o->ctas_per_sm = kSkinnyCtasPerSm;
   const int32_t tm = static_cast<int32_t>(ceil_div(N, kSwapRows));
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK * kSkinnyKsub));
-  const Schedule s = make_schedule(tm, 1, ks, sms, 2, 1, true);
-  fill_sched(o, s);
-  o->split_k = 1;
-  o->wave_efficiency = wave_efficiency(tm, sms);
+  const int32_t slots = kSkinnyCtasPerSm * sms;
+  if (tm <= slots) {
+    const int32_t split = std::max(1, std::min(slots / tm, ks / kSkinnyMinPieceSteps));
+    const Schedule s = make_split_schedule(tm, 1, ks, split);
+    fill_sched(o, s);
+    o->split_k = s.split;
+  } else {
+    const Schedule s = make_schedule(tm, 1, ks, slots, 2, 1, true);
+    fill_sched(o, s);
+    o->split_k = 0;
+  }
+  o->wave_efficiency = wave_efficiency(o->grid, slots);
 }
 
 // CUDA-core plan: two CTAs per SM, each owning a contiguous block of weight rows
@@ -256,6 +271,7 @@ void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
   o->path = SG_PATH_CUDA_CORE;
   o->cluster_size = 1;
+  o->ctas_per_sm = 2;
   const int64_t target = 2 * static_cast<int64_t>(sms);
   int64_t rows_grid = std::min<int64_t>(N, target);
   rows_grid = std::max<int64_t>(rows_grid, ceil_div(N, kCcMaxRowsPerCta));
@@ -334,13 +350,14 @@ int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C
                   int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
   sg_plan_info plan;
   plan_tc_skinny(M, N, K, d.sm_count, &plan);
-  CUtensorMap tw, tx;
+  CUtensorMap tw, tx, tc;
   int st = make_map(&tw, B, N, K, ldb, kSwapRows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, plan.tile_n, kSwapRows, CU_TENSOR_MAP_SWIZZLE_NONE, dev);
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
-  cudaError_t e = launch_tc_skinny(plan.tile_n, tw, tx, p, stream);
+  cudaError_t e = launch_tc_skinny(plan.tile_n, tw, tx, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 

@@ -54,7 +54,6 @@ struct TcLayout {
   static constexpr int kBSub = kBRowsPerCta * kBK * 2;
   static constexpr int kABytes = KSUB * kASub;
   static constexpr int kBBytes = KSUB * kBSub;
-  static constexpr int kStageBytes = kABytes + kBBytes;
   // epilogue warps: one per TMEM lane quarter (eight, two per quarter, measured
   // no faster and would cap registers at 168)
   static constexpr int kEpiWarps = 4;
@@ -65,7 +64,8 @@ struct TcLayout {
   static constexpr int kAOff = 0;
   static constexpr int kBOff = STAGES * kABytes;
   static constexpr int kStagingOff = kBOff + STAGES * kBBytes;
-  static constexpr int kStagingBytes = SWAP ? 0 : kEpiWarps * kStagingBufs * kStagingBufBytes;
+  // swapped path: one C tile (BN activation rows x kARows weight rows, bf16)
+  static constexpr int kStagingBytes = SWAP ? BN * kARows * 2 : kEpiWarps * kStagingBufs * kStagingBufBytes;
   static constexpr int kBarOff = kStagingOff + kStagingBytes;
   // full[S], empty[S], tmem_full[2], tmem_empty[2], teardown, fixup
   static constexpr int kNumBars = 2 * STAGES + 6;
@@ -75,6 +75,10 @@ struct TcLayout {
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
   static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
   static constexpr int kChunk = SWAP ? 16 : 32;  // accumulator columns per tcgen05.ld
+  // accumulator rows a Stream-K partial holds (an M = 64 accumulator has 64)
+  static constexpr int kSlotRows = kARows;
+  // CTAs per SM the launch bounds ask for: two when both fit in shared memory
+  static constexpr int kMinBlocks = (kAlloc + 1024) * 2 <= 228 * 1024 ? 2 : 1;
   // epilogue arrivals that free an accumulator: 4 warps, of both CTAs when paired
   static constexpr uint32_t kTmemEmptyCount = PAIR ? 2 * kEpiWarps : kEpiWarps;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -97,7 +101,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
-__global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThreads, 1)
+__global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThreads,
+                                  TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kMinBlocks)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using L = TcLayout<BN, STAGES, SWAP, KSUB, PAIR>;
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (!SWAP) tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -160,9 +165,10 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // The set-up above touched no global memory, so it may overlap the previous
-  // kernel's tail; every global access below comes after the dependency wait.
+  // kernel's tail.  Each role waits for the previous kernel before its first
+  // global access (and before any bounded wait starts its clock); the producer
+  // first works out its first copy, so only the copy itself waits.
   grid_launch_dependents();
-  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -187,6 +193,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
           const int nsub = min(KSUB, kboxes - ks * KSUB);  // boxes past K are skipped
           uint32_t bytes = static_cast<uint32_t>(nsub * (L::kASub + L::kBSub));
           const uint32_t extra = (it == 0) ? p.inject_extra_tx : 0u;  // failure injection only
+          if (it == 0) grid_dependency_wait();
           if constexpr (PAIR) {
             // the leader's full barrier counts both CTAs' bytes
             const uint32_t full_leader = mapa_shared(smem_u32(&full[s]), 0);
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    grid_dependency_wait();
     if (lane == 0 && rank == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -282,6 +290,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    grid_dependency_wait();
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int ew = warp - 2;                      // epilogue warp index
@@ -293,6 +302,11 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
     uint8_t* staging = smem + L::kStagingOff + ew * L::kStagingBufs * L::kStagingBufBytes;
     // the accumulator-free barrier lives in the pair's MMA-issuing CTA
     const uint32_t tmem_empty_addr0 = PAIR ? mapa_shared(smem_u32(&tmem_empty[0]), 0) : smem_u32(&tmem_empty[0]);
+    // The threads that hold accumulator rows and the row each holds: an M = 64
+    // accumulator has its rows in lanes 0-15 of each lane quarter.
+    const bool holds_row = !SWAP || L::kARows == kBM || lane < 16;
+    const int slot_row = (SWAP && L::kARows != kBM) ? q * 16 + lane : row;
+    constexpr int kEpiThreads = 32 * L::kEpiWarps;
 
     // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
     auto emit_chunk = [&](const float* v, int tm, int tn, int j) {
@@ -318,16 +332,32 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
         }
         ++store_count;
       } else {
-        // D[n][m]: this thread's row is weight row n (M = 64 accumulator: lanes
-        // 0-15 of each lane quarter), columns are activation rows m.
-        const int n = tm * L::kARows + q * 16 + lane;
-        if (lane < 16 && n < p.N) {
-          __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C);
+        // D[n][m]: this thread's row is weight row n, its columns activation rows
+        // m; the staging tile is C's layout (row m, 64 consecutive n), so a warp's
+        // 16 rows land in 32 contiguous bytes per m.
+        if (holds_row) {
+          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(smem + L::kStagingOff);
 #pragma unroll
-          for (int e = 0; e < L::kChunk; ++e) {
-            const int m = tn * BN + j * L::kChunk + e;
-            if (m < p.M) c[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(v[e]);
-          }
+          for (int e = 0; e < L::kChunk; ++e)
+            st[(j * L::kChunk + e) * L::kARows + slot_row] = __float2bfloat16_rn(v[e]);
+        }
+      }
+    };
+    // Swapped path: a tile's outputs are gathered in shared memory and written by
+    // one TMA store (rows past M and columns past N are clipped by the copy).
+    auto begin_tile = [&]() {
+      if constexpr (SWAP) {
+        if (epi_tid == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
+        named_bar_sync(2, kEpiThreads);
+      }
+    };
+    auto end_tile = [&](int tm, int tn) {
+      if constexpr (SWAP) {
+        fence_proxy_async_smem();
+        named_bar_sync(2, kEpiThreads);
+        if (epi_tid == 0) {
+          tma_store_2d(&tmC, smem + L::kStagingOff, tm * L::kARows, tn * BN);
+          bulk_commit_group();
         }
       }
     };
@@ -360,7 +390,8 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
     };
 
     constexpr int kQuads = L::kChunk / 4;
-    constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * BN;  // one CTA's share of a tile
+    constexpr int kSR = L::kSlotRows;
+    constexpr int64_t kSlotFloats = static_cast<int64_t>(kSR) * BN;  // one CTA's share of a tile
     for (int i = 0; i < nitems; ++i) {
       const WorkItem w = get_item(sched, unit, i);
       int32_t tm, tn;
@@ -370,8 +401,9 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
       // An accumulator is ready after its k-steps have run: allow 20 us per k-step
       // on top of the base bound (a k-step normally takes well under 1 us).
       const uint64_t limit = p.timeout_ns + static_cast<uint64_t>(w.k1 - w.k0) * 20000ull;
-      if (!mbar_wait(&tmem_full[b], use & 1u, limit, abort_flag)) {
-        if (!*abort_flag) record_error(p.err, kDevTimeoutTmemFull, i);
+      const bool ready = mbar_wait(&tmem_full[b], use & 1u, limit, abort_flag);
+      if (!ready && !*abort_flag) record_error(p.err, kDevTimeoutTmemFull, i);
+      if (bar_sync_or(1, kEpiThreads, !ready)) {  // all epilogue threads give up together
         *abort_flag = 1;
         break;
       }
@@ -379,11 +411,13 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
       const uint32_t tacc = tmem_base + lane_off + b * BN;
       float v[L::kChunk];
       if (w.npieces == 1) {
+        begin_tile();
         for (int j = chunk_lo; j < chunk_hi; ++j) {
           load_chunk(tacc + j * L::kChunk, v);
           emit_chunk(v, tm, tn, j);
         }
         release_accumulator(b);
+        end_tile(tm, tn);
       } else {
         // Stream-K piece: publish this CTA's fp32 partial, then count arrivals.
         // Slots and counters are per CTA of a pair (each holds its own rows).
@@ -392,9 +426,12 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
         float4* slot = reinterpret_cast<float4*>(p.partials + my_slot * kSlotFloats);
         for (int j = chunk_lo; j < chunk_hi; ++j) {
           load_chunk(tacc + j * L::kChunk, v);
+          if (holds_row) {
 #pragma unroll
-          for (int q4 = 0; q4 < kQuads; ++q4)
-            slot[(j * kQuads + q4) * kBM + row] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            for (int q4 = 0; q4 < kQuads; ++q4)
+              slot[(j * kQuads + q4) * kSR + slot_row] =
+                  make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          }
         }
         release_accumulator(b);
         fence_proxy_async_global();  // the finisher may read these bytes with bulk copies
@@ -423,18 +460,22 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
                         fixup_bar);
             }
           }
-          if (!mbar_wait(fixup_bar, 0, p.timeout_ns, abort_flag)) {
-            if (!*abort_flag) record_error(p.err, kDevTimeoutFull, 1000 + i);
+          const bool landed = mbar_wait(fixup_bar, 0, p.timeout_ns, abort_flag);
+          if (!landed && !*abort_flag) record_error(p.err, kDevTimeoutFull, 1000 + i);
+          if (bar_sync_or(1, kEpiThreads, !landed)) {
             *abort_flag = 1;
           } else {
+            begin_tile();
             const float4* rs = reinterpret_cast<const float4*>(ring);
             for (int j = chunk_lo; j < chunk_hi; ++j) {
               float acc[L::kChunk];
-              for (int pj = 0; pj < w.npieces; ++pj) {  // k order
+#pragma unroll
+              for (int e = 0; e < L::kChunk; ++e) acc[e] = 0.f;
+              for (int pj = 0; pj < w.npieces && holds_row; ++pj) {  // k order
                 const float4* src = rs + pj * (kSlotFloats / 4);
 #pragma unroll
                 for (int q4 = 0; q4 < kQuads; ++q4) {
-                  const float4 x = src[(j * kQuads + q4) * kBM + row];
+                  const float4 x = src[(j * kQuads + q4) * kSR + slot_row];
                   float* a4 = &acc[4 * q4];
                   if (pj == 0) {
                     a4[0] = x.x; a4[1] = x.y; a4[2] = x.z; a4[3] = x.w;
@@ -445,6 +486,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
               }
               emit_chunk(acc, tm, tn, j);
             }
+            end_tile(tm, tn);
           }
           if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
         } else if (*sk_last) {
@@ -453,11 +495,14 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
           // Loads in flight per batch: kBatch pieces x kBQuads float4 of one chunk.
           constexpr int kBatch = kQuads <= 4 ? 4 : 2;  // pieces per batch (16 loads in flight)
           constexpr int kBQuads = kQuads;                // float4 per piece per batch: the whole chunk
+          begin_tile();
           for (int j = chunk_lo; j < chunk_hi; ++j) {
             float acc[L::kChunk];
 #pragma unroll
+            for (int e = 0; e < L::kChunk; ++e) acc[e] = 0.f;
+#pragma unroll
             for (int h = 0; h < kQuads / kBQuads; ++h) {
-              for (int pj = 0; pj < w.npieces; pj += kBatch) {
+              for (int pj = 0; pj < w.npieces && holds_row; pj += kBatch) {
                 float4 x[kBatch][kBQuads];
 #pragma unroll
                 for (int bi = 0; bi < kBatch; ++bi) {
@@ -467,7 +512,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
                         reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl + rank : sl) * kSlotFloats);
 #pragma unroll
                     for (int q4 = 0; q4 < kBQuads; ++q4)
-                      x[bi][q4] = __ldcg(&src[(j * kQuads + h * kBQuads + q4) * kBM + row]);
+                      x[bi][q4] = __ldcg(&src[(j * kQuads + h * kBQuads + q4) * kSR + slot_row]);
                   }
                 }
 #pragma unroll
@@ -488,13 +533,12 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
             }
             emit_chunk(acc, tm, tn, j);
           }
+          end_tile(tm, tn);
           if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
         }
       }
     }
-    if constexpr (!SWAP) {
-      if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
-    }
+    if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -558,12 +602,12 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   return launch_variant<kGemmBN, kPairStages, false, 1, true>(tmA, tmB, tmC, p, stream);
 }
 
-cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
-                             cudaStream_t stream) {
+cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmC,
+                             const TcParams& p, cudaStream_t stream) {
   switch (bn) {
-    case 16: return launch_variant<16, skinny_stages(16), true, kSkinnyKsub, false>(tmW, tmX, tmX, p, stream);
-    case 32: return launch_variant<32, skinny_stages(32), true, kSkinnyKsub, false>(tmW, tmX, tmX, p, stream);
-    case 64: return launch_variant<64, skinny_stages(64), true, kSkinnyKsub, false>(tmW, tmX, tmX, p, stream);
+    case 16: return launch_variant<16, skinny_stages(16), true, kSkinnyKsub, false>(tmW, tmX, tmC, p, stream);
+    case 32: return launch_variant<32, skinny_stages(32), true, kSkinnyKsub, false>(tmW, tmX, tmC, p, stream);
+    case 64: return launch_variant<64, skinny_stages(64), true, kSkinnyKsub, false>(tmW, tmX, tmC, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,16 +17,22 @@ constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
 constexpr int kGemmBN = 256;
 constexpr int kGemmStages = 4;
 constexpr int kPairStages = 6;  // paired tiles: 32 KB per stage per CTA
-// Skinny (swapped) path: each stage holds kSkinnyKsub consecutive 64-wide k boxes
-// of 128 weight rows, so a weight row is read kSkinnyKsub * 128 contiguous bytes
-// at a time; the ring takes as many stages as fit in 224 KB of shared memory.
-constexpr int kSkinnyKsub = 4;
+// Skinny (swapped) path: two CTAs per SM, each with a copy ring of at most
+// kSkinnyRingBytes.  Each stage holds kSkinnyKsub consecutive 64-wide k boxes of
+// kSwapRows weight rows (a weight row is read kSkinnyKsub * 128 contiguous bytes
+// at a time) plus the matching activation boxes.
+constexpr int kSkinnyKsub = 2;
 constexpr int kSwapRows = 64;  // weight rows per tile on the swapped path (MMA M = 64)
+constexpr int kSkinnyCtasPerSm = 2;
+constexpr int kSkinnyRingBytes = 104 * 1024;
 constexpr int skinny_stages(int bn) {
-  return (224 * 1024) / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2) < 2
+  return kSkinnyRingBytes / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2) < 2
              ? 2
-             : (224 * 1024) / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2);
+             : kSkinnyRingBytes / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2);
 }
+// Fewest k-steps a split piece of the skinny path gets (each piece's partial sum
+// is written, counted and read back once).
+constexpr int kSkinnyMinPieceSteps = 4;
 // tcgen05 kernels: warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps.
 
 // Everything a tcgen05 launch needs besides its tensor maps.
@@ -51,9 +57,9 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, 
                                 const TcParams& p, cudaStream_t stream);
 
 // Swapped skinny GEMM: A-operand = weights B (rows N), B-operand = activations A
-// (rows M <= bn), bn in {16, 32, 64}.
-cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
-                             cudaStream_t stream);
+// (rows M <= bn), bn in {16, 32, 64}; tmC stores C in boxes of bn rows x 64 columns.
+cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmC,
+                             const TcParams& p, cudaStream_t stream);
 
 // Shared-memory bytes a launch of each variant needs (for the plan and checks).
 int tc_smem_bytes(int bn, bool swapped);

@@ -67,6 +67,22 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
+// Named barrier `id` over `threads` threads that also ORs a predicate across
+// them: every participant gets the same answer, so a decision taken after it
+// (such as giving up after a bounded wait) is uniform.
+__device__ __forceinline__ bool bar_sync_or(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }

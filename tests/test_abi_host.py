@@ -117,6 +117,7 @@ def _check_plan_coverage(info):
     KS = info["k_steps"]
     cover = np.zeros((T, KS), dtype=np.int32)
     pieces = {}
+    split_mode = info["path"] == sg.PATH_TENSOR_CORE and info["split_k"] > 0
     for cta, row in enumerate(items):
         assert len(row) >= 1, f"CTA {cta} has no work"
         n_sk = sum(1 for it in row if it[0] < info["sk_tiles"])
@@ -127,10 +128,13 @@ def _check_plan_coverage(info):
             assert 0 <= tm < info["tiles_m"] and 0 <= tn < info["tiles_n"]
             cover[tile, k0:k1] += 1
             if npieces > 1:
-                assert slot in (2 * cta, 2 * cta + 1)
-                # slot 0 of a CTA is its first Stream-K item, slot 1 its last
-                assert (slot == 2 * cta) == (idx == 0)
-                assert idx in (0, n_sk - 1)
+                if split_mode:  # one piece per CTA, its own slot
+                    assert slot == cta and len(row) == 1
+                else:
+                    assert slot in (2 * cta, 2 * cta + 1)
+                    # slot 0 of a CTA is its first Stream-K item, slot 1 its last
+                    assert (slot == 2 * cta) == (idx == 0)
+                    assert idx in (0, n_sk - 1)
                 pieces.setdefault(tile, []).append((k0, k1, piece, npieces, cta, slot))
             else:
                 assert (k0, k1) == (0, KS) and slot == -1
@@ -184,16 +188,25 @@ def test_auto_gemm_kernel_choice(lib):
 
 
 @pytest.mark.parametrize("M", [1, 2, 9, 16, 17, 33, 64])
-@pytest.mark.parametrize("N,K", [(11008, 4096), (4096, 11008), (300, 700), (128, 64)])
+@pytest.mark.parametrize("N,K", [(11008, 4096), (4096, 11008), (300, 700), (128, 64), (32000, 4096)])
 def test_skinny_tensor_core_plan(lib, M, N, K):
     info = sg.plan(M, N, K, 152, sg.PATH_TENSOR_CORE)
     assert info["path"] == sg.PATH_TENSOR_CORE
     assert info["tile_n"] == (16 if M <= 16 else 32 if M <= 32 else 64)
     assert info["tile_m"] == 64 and info["tiles_n"] == 1 and info["tiles_m"] == -(-N // 64)
+    assert info["ctas_per_sm"] == 2 and info["tile_k"] == 128
     items = _check_plan_coverage(info)
-    T = info["tiles_m"]
-    if T >= 152 and T % 152:
-        assert info["sk_tiles"] == T % 152  # only the remainder is split
+    T, KS = info["tiles_m"], info["k_steps"]
+    if T <= 304:
+        # split mode: S equal k pieces per tile, one resident CTA each
+        S = max(1, min(304 // T, KS // 4))
+        assert info["split_k"] == S and info["grid"] == T * S <= 304
+        sizes = [k1 - k0 for row in items for (_, k0, k1, *_) in row]
+        assert max(sizes) - min(sizes) <= 1
+    else:
+        assert info["split_k"] == 0 and info["grid"] == 304
+        if T % 304:
+            assert info["sk_tiles"] == T % 304  # only the remainder is split
     # the weights are read once: each weight tile's k-steps are covered exactly once
     assert sum(k1 - k0 for row in items for (_, k0, k1, *_) in row) == info["tiles_m"] * info["k_steps"]
 
