@@ -239,20 +239,26 @@ int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 // fits in the resident slots, each tile is cut into split_k equal k pieces, one
 // CTA per piece, and all CTAs run at once (split mode); past that, a persistent
 // grid of two CTAs per SM walks the tiles with a Stream-K remainder.
+// Weight rows per tile.  128-row tiles would halve the activation bytes each
+// weight byte brings along, but measured slower at every M <= 64 on the 7B-model
+// decode shapes (fewer, longer-latency stages and larger partial sums).
+int skinny_rows(int64_t) { return 64; }
+
 void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
+  const int rows = skinny_rows(M);
   o->path = SG_PATH_TENSOR_CORE;
-  o->tile_m = kSwapRows;
+  o->tile_m = rows;
   o->tile_n = skinny_bn(M);
-  o->tile_k = kBK * kSkinnyKsub;
-  o->stages = skinny_stages(o->tile_n);
+  o->tile_k = kBK * skinny_ksub(rows);
+  o->stages = skinny_stages(o->tile_n, rows);
   o->cluster_size = 1;
   o->ctas_per_sm = kSkinnyCtasPerSm;
-  const int32_t tm = static_cast<int32_t>(ceil_div(N, kSwapRows));
-  const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK * kSkinnyKsub));
+  const int32_t tm = static_cast<int32_t>(ceil_div(N, rows));
+  const int32_t ks = static_cast<int32_t>(ceil_div(K, o->tile_k));
   const int32_t slots = kSkinnyCtasPerSm * sms;
   if (tm <= slots) {
-    const int32_t split = std::max(1, std::min(slots / tm, ks / kSkinnyMinPieceSteps));
+    const int32_t split = std::max(1, std::min(slots / tm, ks / (kSkinnyMinPieceK / o->tile_k)));
     const Schedule s = make_split_schedule(tm, 1, ks, split);
     fill_sched(o, s);
     o->split_k = s.split;
@@ -351,13 +357,13 @@ int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C
   sg_plan_info plan;
   plan_tc_skinny(M, N, K, d.sm_count, &plan);
   CUtensorMap tw, tx, tc;
-  int st = make_map(&tw, B, N, K, ldb, kSwapRows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  int st = make_map(&tw, B, N, K, ldb, plan.tile_m, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
-  if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, plan.tile_n, kSwapRows, CU_TENSOR_MAP_SWIZZLE_NONE, dev);
+  if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, plan.tile_n, plan.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE, dev);
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
-  cudaError_t e = launch_tc_skinny(plan.tile_n, tw, tx, tc, p, stream);
+  cudaError_t e = launch_tc_skinny(plan.tile_n, plan.tile_m, tw, tx, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 

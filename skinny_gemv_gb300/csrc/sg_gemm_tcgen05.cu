@@ -44,11 +44,13 @@ namespace {
 
 // KSUB: consecutive 64-wide k boxes per pipeline stage (one schedule k-step).
 // PAIR: B's rows are split between the two CTAs of a pair (BN / 2 each).
-template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
+// SWAP_ROWS: 0 for the GEMM, else the swapped variant's weight rows per tile.
+template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR>
 struct TcLayout {
-  // rows of the MMA's A operand per CTA: 128, or 64 weight rows on the swapped
-  // path (an M = 64 accumulator sits in lanes 0-15 of each TMEM lane quarter)
-  static constexpr int kARows = SWAP ? kSwapRows : kBM;
+  static constexpr bool SWAP = SWAP_ROWS > 0;
+  // rows of the MMA's A operand per CTA: 128, or 64 / 128 weight rows on the
+  // swapped path (an M = 64 accumulator sits in lanes 0-15 of each TMEM lane quarter)
+  static constexpr int kARows = SWAP ? SWAP_ROWS : kBM;
   static constexpr int kBRowsPerCta = PAIR ? BN / 2 : BN;
   static constexpr int kASub = kARows * kBK * 2;  // one kARows x 64 box
   static constexpr int kBSub = kBRowsPerCta * kBK * 2;
@@ -100,12 +102,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
-__global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThreads,
-                                  TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kMinBlocks)
+template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR>
+__global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::kThreads,
+                                  TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::kMinBlocks)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using L = TcLayout<BN, STAGES, SWAP, KSUB, PAIR>;
+  using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
+  constexpr bool SWAP = L::SWAP;
   constexpr int kTileRows = PAIR ? 2 * kBM : L::kARows;  // output rows per tile (the MMA's M)
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, BN);
   const int kboxes = (p.K + kBK - 1) / kBK;  // 64-wide k boxes that hold data
@@ -553,11 +556,11 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP, KSUB, PAIR>::kThrea
   }
 }
 
-template <int BN, int STAGES, bool SWAP, int KSUB, bool PAIR>
+template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
                            cudaStream_t stream) {
-  using L = TcLayout<BN, STAGES, SWAP, KSUB, PAIR>;
-  auto kern = tc_gemm_kernel<BN, STAGES, SWAP, KSUB, PAIR>;
+  using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
+  auto kern = tc_gemm_kernel<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
   static bool configured = false;  // the attribute is per function, process-wide
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
@@ -583,33 +586,35 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
 
 }  // namespace
 
-int tc_smem_bytes(int bn, bool swapped) {
-  if (!swapped) return TcLayout<kGemmBN, kGemmStages, false, 1, false>::kAlloc;
-  switch (bn) {
-    case 16: return TcLayout<16, skinny_stages(16), true, kSkinnyKsub, false>::kAlloc;
-    case 32: return TcLayout<32, skinny_stages(32), true, kSkinnyKsub, false>::kAlloc;
-    default: return TcLayout<64, skinny_stages(64), true, kSkinnyKsub, false>::kAlloc;
-  }
-}
-
 cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const TcParams& p, cudaStream_t stream) {
-  return launch_variant<kGemmBN, kGemmStages, false, 1, false>(tmA, tmB, tmC, p, stream);
+  return launch_variant<kGemmBN, kGemmStages, 0, 1, false>(tmA, tmB, tmC, p, stream);
 }
 
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                 const TcParams& p, cudaStream_t stream) {
-  return launch_variant<kGemmBN, kPairStages, false, 1, true>(tmA, tmB, tmC, p, stream);
+  return launch_variant<kGemmBN, kPairStages, 0, 1, true>(tmA, tmB, tmC, p, stream);
 }
 
-cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmC,
-                             const TcParams& p, cudaStream_t stream) {
-  switch (bn) {
-    case 16: return launch_variant<16, skinny_stages(16), true, kSkinnyKsub, false>(tmW, tmX, tmC, p, stream);
-    case 32: return launch_variant<32, skinny_stages(32), true, kSkinnyKsub, false>(tmW, tmX, tmC, p, stream);
-    case 64: return launch_variant<64, skinny_stages(64), true, kSkinnyKsub, false>(tmW, tmX, tmC, p, stream);
-    default: return cudaErrorInvalidValue;
+template <int BN, int ROWS>
+cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmC, const TcParams& p,
+                          cudaStream_t stream) {
+  static_assert(TcLayout<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>::kMinBlocks == kSkinnyCtasPerSm,
+                "the skinny plan counts on two resident CTAs per SM");
+  return launch_variant<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>(tmW, tmX, tmC, p, stream);
+}
+
+cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
+  if (rows == 64) {
+    switch (bn) {
+      case 16: return launch_skinny<16, 64>(tmW, tmX, tmC, p, stream);
+      case 32: return launch_skinny<32, 64>(tmW, tmX, tmC, p, stream);
+      case 64: return launch_skinny<64, 64>(tmW, tmX, tmC, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace sg

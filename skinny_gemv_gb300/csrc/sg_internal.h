@@ -17,22 +17,23 @@ constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
 constexpr int kGemmBN = 256;
 constexpr int kGemmStages = 4;
 constexpr int kPairStages = 6;  // paired tiles: 32 KB per stage per CTA
-// Skinny (swapped) path: two CTAs per SM, each with a copy ring of at most
-// kSkinnyRingBytes.  Each stage holds kSkinnyKsub consecutive 64-wide k boxes of
-// kSwapRows weight rows (a weight row is read kSkinnyKsub * 128 contiguous bytes
-// at a time) plus the matching activation boxes.
-constexpr int kSkinnyKsub = 2;
-constexpr int kSwapRows = 64;  // weight rows per tile on the swapped path (MMA M = 64)
+// Skinny (swapped) path: two CTAs per SM, each with at most kSkinnySmemBytes of
+// copy ring plus output staging (two such CTAs and their barriers fit in an SM's
+// 228 KB).  A weight tile is `rows` = 64 or 128 weight rows (MMA M); each stage
+// holds skinny_ksub(rows) consecutive 64-wide k boxes of it (a 64-row tile reads
+// 256 contiguous bytes of each weight row per stage) plus the matching
+// activation boxes; the staging holds one bf16 output tile (bn x rows).
 constexpr int kSkinnyCtasPerSm = 2;
-constexpr int kSkinnyRingBytes = 104 * 1024;
-constexpr int skinny_stages(int bn) {
-  return kSkinnyRingBytes / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2) < 2
+constexpr int kSkinnySmemBytes = 111 * 1024;
+constexpr int skinny_ksub(int rows) { return rows == 64 ? 2 : 1; }
+constexpr int skinny_stages(int bn, int rows) {
+  return (kSkinnySmemBytes - bn * rows * 2) / (skinny_ksub(rows) * (rows + bn) * kBK * 2) < 2
              ? 2
-             : kSkinnyRingBytes / (kSkinnyKsub * (kSwapRows + bn) * kBK * 2);
+             : (kSkinnySmemBytes - bn * rows * 2) / (skinny_ksub(rows) * (rows + bn) * kBK * 2);
 }
-// Fewest k-steps a split piece of the skinny path gets (each piece's partial sum
-// is written, counted and read back once).
-constexpr int kSkinnyMinPieceSteps = 4;
+// Smallest K range a split piece of the skinny path gets (each piece's partial
+// sum is written, counted and read back once).
+constexpr int kSkinnyMinPieceK = 512;
 // tcgen05 kernels: warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps.
 
 // Everything a tcgen05 launch needs besides its tensor maps.
@@ -56,13 +57,12 @@ cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                 const TcParams& p, cudaStream_t stream);
 
-// Swapped skinny GEMM: A-operand = weights B (rows N), B-operand = activations A
-// (rows M <= bn), bn in {16, 32, 64}; tmC stores C in boxes of bn rows x 64 columns.
-cudaError_t launch_tc_skinny(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmC,
-                             const TcParams& p, cudaStream_t stream);
+// Swapped skinny GEMM: A-operand = weights B (rows N, tiles of `rows` in {64, 128}),
+// B-operand = activations A (rows M <= bn), bn in {16, 32, 64}; tmC stores C in
+// boxes of bn rows x `rows` columns.
+cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream);
 
-// Shared-memory bytes a launch of each variant needs (for the plan and checks).
-int tc_smem_bytes(int bn, bool swapped);
 
 // CUDA-core skinny kernel.
 struct CcParams {

@@ -193,13 +193,15 @@ def test_skinny_tensor_core_plan(lib, M, N, K):
     info = sg.plan(M, N, K, 152, sg.PATH_TENSOR_CORE)
     assert info["path"] == sg.PATH_TENSOR_CORE
     assert info["tile_n"] == (16 if M <= 16 else 32 if M <= 32 else 64)
-    assert info["tile_m"] == 64 and info["tiles_n"] == 1 and info["tiles_m"] == -(-N // 64)
-    assert info["ctas_per_sm"] == 2 and info["tile_k"] == 128
+    rows = 64
+    assert info["tile_m"] == rows and info["tiles_n"] == 1 and info["tiles_m"] == -(-N // rows)
+    assert info["ctas_per_sm"] == 2 and info["tile_k"] == (128 if rows == 64 else 64)
+    assert info["k_steps"] == -(-K // info["tile_k"])
     items = _check_plan_coverage(info)
     T, KS = info["tiles_m"], info["k_steps"]
     if T <= 304:
-        # split mode: S equal k pieces per tile, one resident CTA each
-        S = max(1, min(304 // T, KS // 4))
+        # split mode: S equal k pieces per tile (each at least 512 of K), one resident CTA each
+        S = max(1, min(304 // T, KS // (512 // info["tile_k"])))
         assert info["split_k"] == S and info["grid"] == T * S <= 304
         sizes = [k1 - k0 for row in items for (_, k0, k1, *_) in row]
         assert max(sizes) - min(sizes) <= 1

@@ -98,3 +98,30 @@ def test_deterministic_split_k(path):
         C2 = sg.gemv_bf16(A, B, path=path)
         torch.cuda.synchronize()
         assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N", [(16, 20000), (64, 40000)])
+def test_tensor_core_persistent_schedule(M, N):
+    # More weight tiles than resident CTAs (two per SM): the tensor-core kernel
+    # walks its tiles persistently with a Stream-K remainder instead of cutting
+    # each tile into k pieces.
+    K = 320
+    info = sg.plan(M, N, K, torch.cuda.get_device_properties(0).multi_processor_count, sg.PATH_TENSOR_CORE)
+    assert info["split_k"] == 0
+    A = syn.matrix(M, K, "normal:1", 51)
+    B = syn.matrix(N, K, "normal:0.02", 52)
+    assert_close(_gemv(A, B, M, N, K, sg.PATH_TENSOR_CORE), oracle.gemm(A, B), K, f"persistent M={M} N={N}")
+
+
+@pytest.mark.parametrize("M", [16, 64])
+def test_tensor_core_split_pieces(M):
+    # Few weight tiles and a long K: each tile is cut into several k pieces whose
+    # fp32 partials the last arriving piece sums in k order (bit-identical reruns).
+    N, K = 640, 8192
+    info = sg.plan(M, N, K, torch.cuda.get_device_properties(0).multi_processor_count, sg.PATH_TENSOR_CORE)
+    assert info["split_k"] > 1
+    A = syn.matrix(M, K, "normal:1", 61)
+    B = syn.matrix(N, K, "normal:0.02", 62)
+    got = _gemv(A, B, M, N, K, sg.PATH_TENSOR_CORE)
+    assert_close(got, oracle.gemm(A, B), K, f"split M={M}")
+    assert np.array_equal(got, _gemv(A, B, M, N, K, sg.PATH_TENSOR_CORE))
