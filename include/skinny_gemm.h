@@ -93,7 +93,7 @@ SG_API int gemm_bf16(const void *A, const void *B, void *C,
  *
  * Each weight byte of B is read from memory once for all M rows of A
  * ("The kernels that were there", "The GEMV": the M = 2 kernel loads each weight
- * once and feeds both rows).  For M <= 8 the kernel is the CUDA-core stream:
+ * once and feeds both rows).  For M <= 2 the kernel is the CUDA-core stream:
  * 16-byte weight loads coalesced along K, fp32 FMAs, warp-shuffle reductions and
  * a K split only when there are too few row groups to keep enough bytes in flight
  * (spark-kernels, "the decode kernel").  For larger M the fp32 FMA rate of the

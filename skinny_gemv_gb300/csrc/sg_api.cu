@@ -305,7 +305,11 @@ void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   o->wave_efficiency = wave_efficiency(o->grid, 2 * static_cast<int64_t>(sms));
 }
 
-int choose_skinny_path(int64_t M) { return M <= 8 ? SG_PATH_CUDA_CORE : SG_PATH_TENSOR_CORE; }
+// The CUDA-core kernel spends M/2 paired fp32 FMAs per weight element; measured
+// on the 7B-model decode shapes it keeps up with the weight stream at M <= 2,
+// beyond which the tcgen05 kernel (same single pass over the weights) is faster.
+constexpr int64_t kCudaCoreMaxRows = 2;
+int choose_skinny_path(int64_t M) { return M <= kCudaCoreMaxRows ? SG_PATH_CUDA_CORE : SG_PATH_TENSOR_CORE; }
 
 // ----------------------------------------------------------------- validation
 int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,

@@ -1,4 +1,5 @@
-// CUDA-core skinny GEMM (decode GEMV) for M <= 8 activation rows.
+// CUDA-core skinny GEMM (decode GEMV) for M <= 8 activation rows per launch (the
+// automatic choice sends it M <= 2; beyond that the tcgen05 kernel is faster).
 //
 // C[m, n] = sum_k A[m, k] B[n, k].  The grid is grid_rows x split_k CTAs.  CTA
 // (b, s) owns the contiguous weight rows [b*N/grid_rows, (b+1)*N/grid_rows), so
@@ -7,7 +8,8 @@
 // 16-byte (8 x bf16) non-caching loads, adjacent lanes on adjacent 16-byte vectors
 // (512 contiguous bytes per row per warp instruction).  Every loaded weight vector
 // is multiplied against all M activation rows before the next is loaded, so each
-// weight byte crosses the memory bus once ("The kernels that were there", "The
+// weight byte crosses the memory bus once; pairs of weight rows share paired fp32
+// FMAs (fma.rn.f32x2, two independent single-rounding FMAs) ("The kernels that were there", "The
 // GEMV": parallel over output columns, warps stride K with adjacent threads on
 // adjacent weights, 128-bit loads, fp32 accumulation, bf16 store; the M = 2
 // kernel feeds both rows from one load).  Lane partials are combined with warp
@@ -68,12 +70,15 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   grid_launch_dependents();
   grid_dependency_wait();  // no global access before the previous kernel has completed
 
+  static_assert(R % 2 == 0, "weight rows are processed in pairs");
   for (int r0 = row_lo; r0 < row_hi; r0 += R) {
-    float acc[R][MT];
+    // acc[r / 2][m] holds the fp32 sums of weight rows r (x) and r + 1 (y) for
+    // activation row m; one paired FMA updates both.
+    float2 acc[R / 2][MT];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R / 2; ++r)
 #pragma unroll
-      for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+      for (int m = 0; m < MT; ++m) acc[r][m] = make_float2(0.f, 0.f);
     const uint16_t* brow[R];
     bool row_ok[R];
 #pragma unroll
@@ -103,15 +108,19 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
                                  : make_uint4(0, 0, 0, 0);
             bf16x8_to_f32(av, a[m]);
           }
-          // each weight vector is widened once and used for all MT rows
+          // each weight vector is widened once and used for all MT rows; two
+          // weight rows share each paired FMA (the same fp32 operations, in the
+          // same order, as two scalar FMAs)
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            float w[8];
-            bf16x8_to_f32(wv[u][r], w);
+          for (int r = 0; r < R / 2; ++r) {
+            float w0[8], w1[8];
+            bf16x8_to_f32(wv[u][2 * r], w0);
+            bf16x8_to_f32(wv[u][2 * r + 1], w1);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc[r][m] = fmaf(w[e], a[m][e], acc[r][m]);
+              for (int e = 0; e < 8; ++e)
+                acc[r][m] = __ffma2_rn(make_float2(w0[e], w1[e]), make_float2(a[m][e], a[m][e]), acc[r][m]);
           }
         }
       }
@@ -119,18 +128,22 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     if (warp == 0 && tail_k + lane < ke) {  // K tail: one element per lane
       const int k = tail_k + lane;
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float w = row_ok[r] ? bf16_to_f32(brow[r][k]) : 0.f;
+      for (int r = 0; r < R / 2; ++r) {
+        const float w0 = row_ok[2 * r] ? bf16_to_f32(brow[2 * r][k]) : 0.f;
+        const float w1 = row_ok[2 * r + 1] ? bf16_to_f32(brow[2 * r + 1][k]) : 0.f;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
-          if (m < p.M) acc[r][m] = fmaf(w, bf16_to_f32(p.A[static_cast<int64_t>(m) * p.lda + k]), acc[r][m]);
+          if (m < p.M) {
+            const float x = bf16_to_f32(p.A[static_cast<int64_t>(m) * p.lda + k]);
+            acc[r][m] = __ffma2_rn(make_float2(w0, w1), make_float2(x, x), acc[r][m]);
+          }
       }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        float v = acc[r][m];
+        float v = (r & 1) ? acc[r / 2][m].y : acc[r / 2][m].x;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
         if (lane == 0 && row_ok[r]) red[((r0 + r - row_lo) * MT + m) * kCcWarps + warp] = v;

@@ -214,8 +214,9 @@ def test_skinny_tensor_core_plan(lib, M, N, K):
 
 
 def test_auto_path_choice(lib):
+    assert sg.plan(1, 4096, 4096, 152, 0)["path"] == sg.PATH_CUDA_CORE
     assert sg.plan(2, 4096, 4096, 152, 0)["path"] == sg.PATH_CUDA_CORE
-    assert sg.plan(8, 4096, 4096, 152, 0)["path"] == sg.PATH_CUDA_CORE
+    assert sg.plan(3, 4096, 4096, 152, 0)["path"] == sg.PATH_TENSOR_CORE
     assert sg.plan(9, 4096, 4096, 152, 0)["path"] == sg.PATH_TENSOR_CORE
     assert sg.plan(64, 4096, 4096, 152, 0)["path"] == sg.PATH_TENSOR_CORE
     assert sg.plan(65, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM

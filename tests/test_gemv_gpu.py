@@ -83,7 +83,7 @@ def test_decode_workloads(w):
     ref = oracle.gemm(A, B)
     assert_close(_gemv(A, B, w.M, w.N, w.K, sg.PATH_AUTO), ref, w.K, w.name + " gemv")
     assert_close(_gemv(A, B, w.M, w.N, w.K, None, entry="gemm"), ref, w.K, w.name + " gemm")
-    other = sg.PATH_TENSOR_CORE if w.M <= 8 else sg.PATH_CUDA_CORE
+    other = sg.PATH_TENSOR_CORE if w.M <= 2 else sg.PATH_CUDA_CORE
     assert_close(_gemv(A, B, w.M, w.N, w.K, other), ref, w.K, w.name + f" path {other}")
 
 
