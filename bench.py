@@ -240,6 +240,9 @@ def time_launches(torch, stream, fns, steps: int, warmup: int, graph_chunk: int 
         fns[i % len(fns)]()
     stream.synchronize()
     graphs = build_graphs(torch, stream, fns, steps, graph_chunk, offset=warmup)
+    # The first replay of a new graph also uploads it to the device; replay each
+    # once untimed so the timed replay measures the launches alone.
+    replay_ms(torch, stream, graphs)
     return replay_ms(torch, stream, graphs)
 
 
@@ -462,13 +465,18 @@ def measure_e2e(torch, sg, w, A0, B0, stream, args, dist, world):
             "steps": steps, "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N}
 
 
-def measure_rows(torch, sg, syn, stream, l2, peaks, args):
+ENTRIES = {"auto": None, "cuda_core": 1, "tensor_core": 2}
+
+
+def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=None):
     """Other workloads of the pages, timed the same way (inputs rotated past L2).
     Inputs are drawn on the device from seeded generators with the workloads'
-    distributions; the parity tests check these shapes on the host generator's inputs."""
+    distributions; the parity tests check these shapes on the host generator's inputs.
+    `names` limits the workloads and `entries` the skinny entries (auto, cuda_core,
+    tensor_core) that are timed."""
     out = []
     gen = torch.Generator(device=stream.device)
-    steps = 20 if args.quick else 50
+    steps = 20 if args.quick else 100
 
     def draw(rows, cols, dist, seed):
         gen.manual_seed(seed)
@@ -479,7 +487,8 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args):
             t = torch.randn((rows, cols), generator=gen, device=stream.device, dtype=torch.float32) * sigma
         return t.to(torch.bfloat16)
 
-    names = ["sq2048", "mlp_up", "mlp_down", "sq8192"] + [n for n in syn.WORKLOADS if n.startswith("dec")]
+    if names is None:
+        names = ["sq2048", "mlp_up", "mlp_down", "sq8192"] + [n for n in syn.WORKLOADS if n.startswith("dec")]
     for name in names:
         w = syn.WORKLOADS[name]
         with torch.cuda.stream(stream):
@@ -495,6 +504,9 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args):
         if w.M <= 64:
             paths = [("gemm_bf16", None), ("gemv_bf16/cuda_core", sg.PATH_CUDA_CORE),
                      ("gemv_bf16/tensor_core", sg.PATH_TENSOR_CORE)]
+        if entries is not None:
+            keep = {ENTRIES[e] for e in entries}
+            paths = [(label, path) for label, path in paths if path in keep]
         for label, path in paths:
             if path is None:
                 fns = [(lambda a=a, b=b: sg.gemm_bf16(a, b, C, stream=stream)) for a, b in zip(As, Bs)]
@@ -551,6 +563,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--rows-only", metavar="WORKLOADS",
+                    help="time only these comma-separated workloads (e.g. dec16_up) as rows and print them; "
+                         "no headline (for profiling one kernel)")
+    ap.add_argument("--entry", choices=sorted(ENTRIES), action="append",
+                    help="with --rows-only: the entries to time (default: all)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -559,7 +576,33 @@ def main(argv=None):
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.rows_only:
+        return run_rows_only(args, local)
     return run_ours(args, world, rank, local)
+
+
+def run_rows_only(args, local):
+    import synthetic as syn
+
+    names = [n.strip() for n in args.rows_only.split(",") if n.strip()]
+    unknown = [n for n in names if n not in syn.WORKLOADS]
+    if unknown or not names:
+        raise SystemExit(f"unknown workloads: {unknown or args.rows_only!r}")
+    import torch
+
+    import skinny_gemv_gb300 as sg
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    sg.load()
+    stream = torch.cuda.Stream(device)
+    rows = measure_rows(torch, sg, syn, stream, sg.device_query()["l2_bytes"], measured_peaks(), args,
+                        names=names, entries=args.entry)
+    st, detail = sg.check_device_errors(stream)
+    if st != sg.SG_OK:
+        raise RuntimeError(f"device error {st} {detail}")
+    print(json.dumps({"rows": rows}), flush=True)
+    return 0
 
 
 if __name__ == "__main__":

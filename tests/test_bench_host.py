@@ -71,3 +71,11 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOPS" and line["higher_is_better"] is True
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_rows_only_rejects_unknown_workloads():
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--rows-only", "no_such_workload"])
+    with pytest.raises(SystemExit):
+        bench.main(["--rows-only", "dec16_up", "--entry", "no_such_entry"])
