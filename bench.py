@@ -488,7 +488,9 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         return t.to(torch.bfloat16)
 
     if names is None:
-        names = ["sq2048", "mlp_up", "mlp_down", "sq8192"] + [n for n in syn.WORKLOADS if n.startswith("dec")]
+        # decode rows first: right after seconds of power-capped GEMMs the
+        # memory-bound rows measured up to 2 us slower per launch
+        names = [n for n in syn.WORKLOADS if n.startswith("dec")] + ["sq2048", "mlp_up", "mlp_down", "sq8192"]
     for name in names:
         w = syn.WORKLOADS[name]
         with torch.cuda.stream(stream):
