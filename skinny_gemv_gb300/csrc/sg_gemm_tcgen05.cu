@@ -365,20 +365,20 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
       }
     };
 
-    auto load_chunk = [&](uint32_t taddr, float* v) {
-      if constexpr (L::kChunk == 32) {
-        uint32_t r[32];
+    // Asynchronous TMEM load of one chunk (kChunk columns of this thread's row);
+    // its registers are valid after tmem_ld_wait(r).
+    auto issue_chunk = [&](uint32_t taddr, uint32_t (&r)[L::kChunk]) {
+      if constexpr (L::kChunk == 32)
         tmem_ld_32x32b_x32(taddr, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-      } else {
-        uint32_t r[16];
+      else
         tmem_ld_32x32b_x16(taddr, r);
-        tmem_ld_wait();
+    };
+    auto load_chunk = [&](uint32_t taddr, float* v) {
+      uint32_t r[L::kChunk];
+      issue_chunk(taddr, r);
+      tmem_ld_wait(r);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-      }
+      for (int e = 0; e < L::kChunk; ++e) v[e] = __uint_as_float(r[e]);
     };
 
     auto release_accumulator = [&](uint32_t b) {
@@ -414,10 +414,22 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
       const uint32_t tacc = tmem_base + lane_off + b * BN;
       float v[L::kChunk];
       if (w.npieces == 1) {
+        // Whole tile: the TMEM load of chunk j + 1 is in flight while chunk j is
+        // converted and stored.
+        constexpr int kChunks = L::kColsPerEpiWarp / L::kChunk;
         begin_tile();
-        for (int j = chunk_lo; j < chunk_hi; ++j) {
-          load_chunk(tacc + j * L::kChunk, v);
-          emit_chunk(v, tm, tn, j);
+        uint32_t ra[L::kChunk], rb[L::kChunk];
+        issue_chunk(tacc + chunk_lo * L::kChunk, ra);
+        tmem_ld_wait(ra);
+#pragma unroll
+        for (int jj = 0; jj < kChunks; ++jj) {
+          uint32_t(&cur)[L::kChunk] = (jj & 1) ? rb : ra;
+          uint32_t(&nxt)[L::kChunk] = (jj & 1) ? ra : rb;
+          if (jj + 1 < kChunks) issue_chunk(tacc + (chunk_lo + jj + 1) * L::kChunk, nxt);
+#pragma unroll
+          for (int e = 0; e < L::kChunk; ++e) v[e] = __uint_as_float(cur[e]);
+          emit_chunk(v, tm, tn, chunk_lo + jj);
+          if (jj + 1 < kChunks) tmem_ld_wait(nxt);
         }
         release_accumulator(b);
         end_tile(tm, tn);
