@@ -178,6 +178,19 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# A back-to-back run longer than this settles under the 1.4 kW power cap (the
+# SM clock drops from 2070 MHz to ~1870 MHz within ~40 ms of dense GEMMs), so its
+# tensor roof is the sustained cuBLAS figure; shorter runs use the burst figure.
+SUSTAINED_AFTER_MS = 50.0
+
+
+def tensor_peak(peaks: dict, timed_ms: float):
+    """The measured bf16 tensor roof that matches a timed region of timed_ms."""
+    if timed_ms > SUSTAINED_AFTER_MS and peaks.get("bf16_tflops_sustained"):
+        return peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
+    return peaks["bf16_tflops"], "bf16_tflops"
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "skinny_gemv_gb300", "csrc")
@@ -372,7 +385,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return 0
     plan = sg.plan(M, N, K, info["sm_count"], 0)
-    peak = peaks["bf16_tflops"]
+    peak, peak_key = tensor_peak(peaks, total_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -394,7 +407,10 @@ def run_ours(args, world, rank, local):
             "traffic": recorded_traffic("tc_gemm_kernel", HEADLINE),
             "kernel": ("tc_gemm_kernel<256,6,pair>" if plan["path"] == sg.PATH_GEMM_PAIR
                        else "tc_gemm_kernel<256,4,single>"), "kernel_ms": kernel_ms,
-            "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peaks['source']}, burst: cuBLAS 8192^3)",
+            "peak_source": (f"MEASURED_PEAKS.json {peak_key} ({peaks['source']}; cuBLAS 8192^3, "
+                            f"{'back to back for 4 s under the power cap' if peak_key.endswith('sustained') else 'burst'}"
+                            f"): the timed region ran {total_ms:.0f} ms of back-to-back launches"),
+            "frac_of_burst": achieved / peaks["bf16_tflops"],
             "algorithmic": f"2*M*N*K = {2 * M * N * K / 1e9:.1f} GFLOP per launch",
         },
         "e2e": e2e,
@@ -520,7 +536,9 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
             row = {"workload": name, "entry": label, "M": w.M, "N": w.N, "K": w.K, "us": med * 1e3}
             if w.M > 64:
                 row["tflops"] = tflops(w.M, w.N, w.K, med / 1e3)
-                row["frac_of_peak"] = row["tflops"] / peaks["bf16_tflops"]
+                rpeak, rkey = tensor_peak(peaks, total)
+                row["frac_of_peak"] = row["tflops"] / rpeak
+                row["peak"] = rkey
             else:
                 gbs = decode_bytes(w.M, w.N, w.K) / (med / 1e3) / 1e9
                 row["gbs"] = gbs

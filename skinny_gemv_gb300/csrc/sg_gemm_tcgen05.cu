@@ -59,7 +59,13 @@ struct TcLayout {
   // epilogue warps: one per TMEM lane quarter (eight, two per quarter, measured
   // no faster and would cap registers at 168)
   static constexpr int kEpiWarps = 4;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  // GEMM variants: two more warps sum the fp32 partials of Stream-K tiles, so a
+  // tile finished in the middle of a CTA's schedule does not hold up the
+  // epilogue of the tiles after it (the skinny variant's split pieces end the
+  // CTA's schedule and are summed from the idle copy ring instead).
+  static constexpr int kFixupWarps = SWAP ? 0 : 2;
+  static constexpr int kMaxJobs = 4;  // Stream-K pieces per CTA the fixup warps take
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kFixupWarps;
   static constexpr int kColsPerEpiWarp = BN / (kEpiWarps / 4);
   static constexpr int kStagingBufBytes = 32 * 64;  // 32 rows x 32 bf16
   static constexpr int kStagingBufs = 2;            // per epilogue warp
@@ -68,12 +74,15 @@ struct TcLayout {
   static constexpr int kStagingOff = kBOff + STAGES * kBBytes;
   // swapped path: one C tile (BN activation rows x kARows weight rows, bf16)
   static constexpr int kStagingBytes = SWAP ? BN * kARows * 2 : kEpiWarps * kStagingBufs * kStagingBufBytes;
-  static constexpr int kBarOff = kStagingOff + kStagingBytes;
-  // full[S], empty[S], tmem_full[2], tmem_empty[2], teardown, fixup
-  static constexpr int kNumBars = 2 * STAGES + 6;
+  static constexpr int kFixStagingOff = kStagingOff + kStagingBytes;
+  static constexpr int kFixStagingBytes = kFixupWarps * kStagingBufs * kStagingBufBytes;
+  static constexpr int kBarOff = kFixStagingOff + kFixStagingBytes;
+  // full[S], empty[S], tmem_full[2], tmem_empty[2], teardown, fixup, job[kMaxJobs]
+  static constexpr int kNumBars = 2 * STAGES + 6 + kMaxJobs;
   static constexpr int kRingBytes = STAGES * (kABytes + kBBytes);
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, sk flag
-  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kJobOff = kMiscOff + 16;            // kMaxJobs x {tm, tn, last, -}
+  static constexpr int kBytes = kJobOff + kMaxJobs * 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
   static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
   static constexpr int kChunk = SWAP ? 16 : 32;  // accumulator columns per tcgen05.ld
@@ -84,6 +93,9 @@ struct TcLayout {
   // epilogue arrivals that free an accumulator: 4 warps, of both CTAs when paired
   static constexpr uint32_t kTmemEmptyCount = PAIR ? 2 * kEpiWarps : kEpiWarps;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+  static_assert(kFixupWarps == 0 || (kChunk == 32 && kStagingBufs == 2 && kStagingBufBytes == 32 * 64 &&
+                                     kFixupWarps * 64 == kBM),
+                "fixup warps: 64 rows each, 32-column chunks, two 2 KB store buffers");
   static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
   static_assert(!(PAIR && SWAP), "the paired variant is the non-swapped GEMM");
 };
@@ -100,6 +112,31 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
+}
+
+// One warp writes 32 rows x 32 fp32 columns (lane = row) to C as bf16 (round to
+// nearest even): 64-byte-swizzled staging in one of two 2 KB buffers, then a TMA
+// store clipped at M and N.
+__device__ __forceinline__ void store_rows_32x32(const CUtensorMap* tmC, const float* v, int col0, int row0,
+                                                 uint8_t* staging, uint32_t& count, int lane, int M, int N) {
+  constexpr int kBuf = 32 * 64;
+  const uint32_t buf = count & 1u;
+  if (lane == 0) bulk_wait_group_read<1>();  // buffer `buf` no longer read by TMA
+  __syncwarp();
+  const uint32_t base = smem_u32(staging + buf * kBuf) + lane * 64;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t phys = static_cast<uint32_t>(c) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
+    st_shared_v4(base + phys * 16, pack_bf16x2(v[8 * c + 0], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                 pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (row0 < M && col0 < N) tma_store_2d(tmC, staging + buf * kBuf, col0, row0);
+    bulk_commit_group();
+  }
+  ++count;
 }
 
 template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR>
@@ -122,6 +159,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
   uint64_t* tmem_empty = bars + 2 * STAGES + 2;
   uint64_t* teardown = bars + 2 * STAGES + 4;
   uint64_t* fixup_bar = bars + 2 * STAGES + 5;  // bulk loads of Stream-K partials
+  uint64_t* job_bar = bars + 2 * STAGES + 6;    // Stream-K piece j handed to the fixup warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
   volatile uint32_t* sk_last = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 8);
@@ -144,6 +182,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
     }
     mbar_init(teardown, 1);
     mbar_init(fixup_bar, 1);
+    for (int j = 0; j < L::kMaxJobs; ++j) mbar_init(&job_bar[j], 1);
     *abort_flag = 0;
     *sk_last = 0;
     fence_mbar_init();
@@ -291,7 +330,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
         if (!mbar_wait(teardown, 0, p.timeout_ns, &never)) record_error(p.err, kDevTimeoutTeardown, 0);
       }
     }
-  } else {
+  } else if (warp < 2 + L::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     grid_dependency_wait();
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -314,26 +353,8 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
     // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
     auto emit_chunk = [&](const float* v, int tm, int tn, int j) {
       if constexpr (!SWAP) {
-        const int col0 = tn * BN + j * 32;
-        const int row0 = tm * kTileRows + static_cast<int>(rank) * kBM + q * 32;
-        const uint32_t buf = store_count & 1u;
-        if (lane == 0) bulk_wait_group_read<1>();  // buffer `buf` no longer read by TMA
-        __syncwarp();
-        const uint32_t base = smem_u32(staging + buf * L::kStagingBufBytes) + lane * 64;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t phys = static_cast<uint32_t>(c) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
-          st_shared_v4(base + phys * 16, pack_bf16x2(v[8 * c + 0], v[8 * c + 1]),
-                       pack_bf16x2(v[8 * c + 2], v[8 * c + 3]), pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
-                       pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (row0 < p.M && col0 < p.N) tma_store_2d(&tmC, staging + buf * L::kStagingBufBytes, col0, row0);
-          bulk_commit_group();
-        }
-        ++store_count;
+        store_rows_32x32(&tmC, v, tn * BN + j * 32, tm * kTileRows + static_cast<int>(rank) * kBM + q * 32, staging,
+                         store_count, lane, p.M, p.N);
       } else {
         // D[n][m]: this thread's row is weight row n, its columns activation rows
         // m; the staging tile is C's layout (row m, 64 consecutive n), so a warp's
@@ -457,6 +478,18 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
           *sk_last = (before == static_cast<uint32_t>(w.npieces - 1)) ? 1u : 0u;
         }
         named_bar_sync(1, 32 * L::kEpiWarps);
+        if (L::kFixupWarps > 0 && i < L::kMaxJobs) {
+          // Hand the piece to the fixup warps (the sum, if this piece arrived last,
+          // runs there while this epilogue goes on to the next tile).
+          if (epi_tid == 0) {
+            int32_t* job = reinterpret_cast<int32_t*>(smem + L::kJobOff) + 4 * i;
+            job[0] = tm;
+            job[1] = tn;
+            job[2] = static_cast<int32_t>(*sk_last);
+            mbar_arrive(&job_bar[i]);
+          }
+          continue;
+        }
         // The finisher's last item: the copy ring is idle (every stage of this CTA
         // has been consumed), so all pieces' partials are fetched into it with
         // bulk copies under one barrier instead of dependent rounds of loads.
@@ -552,6 +585,75 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
           if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
         }
       }
+    }
+    if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
+  } else {
+    // ------------------------------------------------------------ Stream-K fixup
+    // Takes the CTA's Stream-K pieces in order.  For a piece whose tile this CTA
+    // finished last, sums every piece's fp32 partial in k order (each thread one
+    // row, 64 rows per warp) and stores bf16.
+    grid_dependency_wait();
+    const int fw = warp - 2 - L::kEpiWarps;
+    uint8_t* fstaging = smem + L::kFixStagingOff + fw * L::kStagingBufs * L::kStagingBufBytes;
+    uint32_t fstore_count = 0;
+    constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * BN;
+    constexpr int kQuads = 8;  // float4 per 32-column chunk
+    const int njobs = min(sk_count(sched, unit), L::kMaxJobs);
+    for (int jidx = 0; jidx < njobs; ++jidx) {
+      const WorkItem w = get_item(sched, unit, jidx);
+      if (w.npieces <= 1) continue;  // a whole tile: the epilogue stored it
+      // the job is posted once this piece's accumulator is ready, after at most
+      // jidx + 1 items of this CTA: allow 20 us per k-step of those
+      const uint64_t limit = p.timeout_ns + static_cast<uint64_t>((jidx + 1) * sched.k_steps) * 20000ull;
+      const bool posted = mbar_wait(&job_bar[jidx], 0, limit, abort_flag);
+      if (!posted && !*abort_flag) record_error(p.err, kDevTimeoutTmemFull, 2000 + jidx);
+      if (bar_sync_or(3, 32 * L::kFixupWarps, !posted)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int32_t* job = reinterpret_cast<const int32_t*>(smem + L::kJobOff) + 4 * jidx;
+      const int tm = job[0], tn = job[1];
+      if (!job[2]) continue;
+      __threadfence();  // the other pieces' partials were published before their arrivals
+#pragma unroll 1
+      for (int j = 0; j < BN / 32; ++j) {
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          const int frow = fw * 64 + g * 32 + lane;
+          float acc[32];
+          for (int pj = 0; pj < w.npieces; pj += 4) {
+            float4 x[4][kQuads];
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) {
+              if (pj + bi < w.npieces) {
+                const int64_t sl = piece_slot(sched, w.sk_index, pj + bi);
+                const float4* src =
+                    reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl + rank : sl) * kSlotFloats);
+#pragma unroll
+                for (int q4 = 0; q4 < kQuads; ++q4) x[bi][q4] = __ldcg(&src[(j * kQuads + q4) * kBM + frow]);
+              }
+            }
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) {  // k order: pieces pj, pj + 1, ...
+              if (pj + bi < w.npieces) {
+#pragma unroll
+                for (int q4 = 0; q4 < kQuads; ++q4) {
+                  float* a4 = &acc[4 * q4];
+                  if (pj + bi == 0) {
+                    a4[0] = x[bi][q4].x; a4[1] = x[bi][q4].y; a4[2] = x[bi][q4].z; a4[3] = x[bi][q4].w;
+                  } else {
+                    a4[0] += x[bi][q4].x; a4[1] += x[bi][q4].y; a4[2] += x[bi][q4].z; a4[3] += x[bi][q4].w;
+                  }
+                }
+              }
+            }
+          }
+          store_rows_32x32(&tmC, acc, tn * BN + j * 32,
+                           tm * kTileRows + static_cast<int>(rank) * kBM + fw * 64 + g * 32, fstaging,
+                           fstore_count, lane, p.M, p.N);
+        }
+      }
+      if (fw == 0 && lane == 0) atomicExch(&p.counters[PAIR ? 2 * w.sk_index + static_cast<int>(rank) : w.sk_index], 0u);
     }
     if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
   }

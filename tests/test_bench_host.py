@@ -79,3 +79,11 @@ def test_rows_only_rejects_unknown_workloads():
         bench.main(["--rows-only", "no_such_workload"])
     with pytest.raises(SystemExit):
         bench.main(["--rows-only", "dec16_up", "--entry", "no_such_entry"])
+
+
+def test_tensor_peak_follows_the_timed_region():
+    import bench
+    peaks = {"bf16_tflops": 1883.7, "bf16_tflops_sustained": 1707.5, "hbm_gbs": 6769.4}
+    assert bench.tensor_peak(peaks, 10.0) == (1883.7, "bf16_tflops")
+    assert bench.tensor_peak(peaks, 400.0) == (1707.5, "bf16_tflops_sustained")
+    assert bench.tensor_peak({"bf16_tflops": 1.0, "bf16_tflops_sustained": None}, 400.0) == (1.0, "bf16_tflops")
