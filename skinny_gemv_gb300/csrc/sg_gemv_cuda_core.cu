@@ -51,6 +51,33 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
+// One butterfly step per lane bit OFF = 16, 8, ..., 1 over the N values still
+// held: lanes with that bit set keep the upper half, the others the lower half,
+// and each kept value gains its partner's copy.  Once one value is left, the
+// remaining steps add the partner's value.
+template <int N, int OFF>
+struct Butterfly {
+  __device__ __forceinline__ static void run(float* v, int lane, int& idx) {
+    if constexpr (OFF > 0) {
+      if constexpr (N > 1) {
+        constexpr int H = N / 2;
+        const bool upper = (lane & OFF) != 0;
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float send = upper ? v[i] : v[i + H];
+          const float keep = upper ? v[i + H] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, OFF);
+        }
+        if (upper) idx += H;
+        Butterfly<H, OFF / 2>::run(v, lane, idx);
+      } else {
+        v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], OFF);
+        Butterfly<1, OFF / 2>::run(v, lane, idx);
+      }
+    }
+  }
+};
+
 // MT: activation rows held (>= M); R: weight rows per warp pass; U: 16-byte
 // vectors per lane per row in flight.
 template <int MT, int R, int U>
@@ -139,15 +166,24 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
           }
       }
     }
+    // Reduce the R x MT sums across the warp's 32 lanes with a butterfly that
+    // also scatters them: at each step a lane keeps half of its values and sends
+    // the other half to its partner, so NV values take NV - 1 + (5 - log2 NV)
+    // shuffles instead of 5 NV.  Afterwards lane l holds the full sum of value
+    // index(l) (flattened r * MT + m), duplicated in lanes 2^(log2 NV) apart.
+    constexpr int NV = R * MT;
+    static_assert((NV & (NV - 1)) == 0 && NV <= 32, "power-of-two sums per lane");
+    float v[NV];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        float v = (r & 1) ? acc[r / 2][m].y : acc[r / 2][m].x;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-        if (lane == 0 && row_ok[r]) red[((r0 + r - row_lo) * MT + m) * kCcWarps + warp] = v;
-      }
+      for (int m = 0; m < MT; ++m) v[r * MT + m] = (r & 1) ? acc[r / 2][m].y : acc[r / 2][m].x;
+    int idx = 0;
+    Butterfly<NV, 16>::run(v, lane, idx);
+    if ((lane & ((32 / NV) - 1)) == 0) {  // one lane per value index
+      const int r = idx / MT, m = idx % MT;
+      if (r0 + r < row_hi) red[((r0 + r - row_lo) * MT + m) * kCcWarps + warp] = v[0];
+    }
   }
   __syncthreads();
 
