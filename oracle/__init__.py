@@ -10,6 +10,8 @@ Functions
 ---------
 gemm(A, B)                    full fp64 reference, shape (M, N)
 gemm_sampled(A, B, rows, cols) the same sum at the intersections rows x cols
+silu(x)                        x * sigmoid(x) = x / (1 + exp(-x)), fp64
+swiglu(A, Wg, Wu)              silu(A . Wg^T) * (A . Wu^T), fp64 (gated MLP)
 build()                        compile the C oracle (idempotent)
 
 A and B are uint16 arrays of bf16 bit patterns, A[M, lda] and B[N, ldb]; the
@@ -97,3 +99,22 @@ def gemm_sampled(A: np.ndarray, B: np.ndarray, rows, cols, K: int | None = None,
     if used < 0:
         raise ValueError("oracle_gemm_sampled_f64: bad arguments")
     return (out, used) if return_threads else out
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """SiLU (the swish with unit slope) in fp64: x * sigmoid(x), written as
+    x / (1 + exp(-x)).  For x far below zero exp(-x) overflows to inf and the
+    quotient is the correct limit, -0 or 0."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def swiglu(A: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, K: int | None = None,
+           threads: int | None = None) -> np.ndarray:
+    """The gated MLP's first half: silu(A . Wg^T) * (A . Wu^T), each product an
+    fp64 gemm() of the same inputs, the SiLU and the product in fp64 (no
+    rounding to bf16).  Wg and Wu are [N, K] bf16 bit patterns."""
+    g = gemm(A, Wg, K=K, threads=threads)
+    u = gemm(A, Wu, K=K, threads=threads)
+    return silu(g) * u
