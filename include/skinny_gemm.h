@@ -116,6 +116,34 @@ SG_API int gemv_bf16_path(const void *A, const void *B, void *C,
                    int64_t lda, int64_t ldb, int64_t ldc, int path, sg_stream_t stream);
 
 /*
+ * gemm_bf16_swiglu -- the gated MLP's first half in one launch:
+ *
+ *     C[m, n] = silu(G[m, n]) * U[m, n],   G = A . Wg^T,  U = A . Wu^T,
+ *     silu(x) = x / (1 + e^-x),
+ *
+ * the fused gate/up projection with a SwiGLU epilogue (spark-kernels, "the bf16
+ * gemm": the fused MLP kernels; the pages' "fused MLP epilogues" as the next
+ * step).  A is M x K (lda), Wg and Wu are N x K weights with one leading
+ * dimension ldw, C is M x N (ldc); all bf16, row-major, 16-byte aligned, leading
+ * dimensions multiples of 8.  G and U accumulate in fp32; the SiLU and the
+ * product are fp32 (expf); C is rounded to bf16 (nearest even).  G and U are
+ * never written to memory.
+ *
+ * Kernel: the single-CTA tcgen05 GEMM with each B tile made of 128 rows of Wg
+ * over 128 rows of Wu (128 output columns per tile), for every M.  Same errors
+ * as gemm_bf16 (a null or misaligned Wu as for B).  K = 0 gives C = 0.
+ */
+SG_API int gemm_bf16_swiglu(const void *A, const void *Wg, const void *Wu, void *C,
+                     int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldw, int64_t ldc, sg_stream_t stream);
+
+/* gemm_bf16_swiglu with the kernel named: SG_PATH_AUTO or SG_PATH_GEMM (others:
+ * SG_ERR_INVALID_ARG). */
+SG_API int gemm_bf16_swiglu_path(const void *A, const void *Wg, const void *Wu, void *C,
+                          int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldw, int64_t ldc, int path, sg_stream_t stream);
+
+/*
  * gemv_bf16_noalloc -- gemv_bf16 on the CUDA-core kernel (SG_PATH_CUDA_CORE),
  * for callers that cannot allocate device memory.  The pages have no
  * counterpart: this entry point exists for integration, not for the method.
@@ -226,6 +254,11 @@ typedef struct {
  * Returns SG_OK or SG_ERR_INVALID_ARG.
  */
 SG_API int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
+
+/* sg_plan_swiglu -- the launch plan of gemm_bf16_swiglu_path (entry SG_PATH_AUTO
+ * or SG_PATH_GEMM): tile_n counts output columns (each from tile_n gate and
+ * tile_n up weight rows). */
+SG_API int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
 
 /*
  * sg_plan_item -- work item `index` of CTA `cta` under a tcgen05 plan from sg_plan:

@@ -94,6 +94,10 @@ def load(build_if_missing: bool = False):
         f = getattr(lib, name)
         f.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
         f.restype = ctypes.c_int
+    lib.gemm_bf16_swiglu.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, p]
+    lib.gemm_bf16_swiglu.restype = ctypes.c_int
+    lib.gemm_bf16_swiglu_path.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
+    lib.gemm_bf16_swiglu_path.restype = ctypes.c_int
     lib.sg_status_string.argtypes = [ctypes.c_int]
     lib.sg_status_string.restype = ctypes.c_char_p
     lib.sg_last_cuda_error.argtypes = []
@@ -106,6 +110,8 @@ def load(build_if_missing: bool = False):
     lib.sg_debug_inject_missing_tx.restype = None
     lib.sg_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.sg_plan.restype = ctypes.c_int
+    lib.sg_plan_swiglu.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.sg_plan_swiglu.restype = ctypes.c_int
     lib.sg_plan_item.argtypes = [ctypes.POINTER(PlanInfo), i32, i32, ctypes.POINTER(ctypes.c_int32)]
     lib.sg_plan_item.restype = ctypes.c_int
     lib.sg_wave_efficiency.argtypes = [i64, i64]
@@ -203,6 +209,32 @@ def gemm_bf16(A, B, C=None, stream=None, path: int = PATH_AUTO):
     return _call("gemm_bf16", A, B, C, stream, path)
 
 
+def gemm_bf16_swiglu(A, Wg, Wu, C=None, stream=None, path: int = PATH_AUTO):
+    """C[M, N] = silu(A @ Wg^T) * (A @ Wu^T) in one launch (fp32 accumulation and
+    epilogue, bf16 out); Wg and Wu are [N, K] with one leading dimension."""
+    torch = _torch()
+    a_ptr, lda = _operand(A, "A")
+    g_ptr, ldg = _operand(Wg, "Wg")
+    u_ptr, ldu = _operand(Wu, "Wu")
+    M, K = A.shape
+    N = Wg.shape[0]
+    if tuple(Wg.shape) != (N, K) or tuple(Wu.shape) != (N, K):
+        raise ValueError(f"Wg and Wu must both be {(N, K)}: {tuple(Wg.shape)} {tuple(Wu.shape)}")
+    if ldg != ldu:
+        raise ValueError(f"Wg and Wu must share a leading dimension ({ldg} vs {ldu})")
+    if C is None:
+        ld = -(-N // 8) * 8
+        C = torch.empty((M, ld), dtype=torch.bfloat16, device=A.device)[:, :N]
+    c_ptr, ldc = _operand(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    with torch.cuda.device(A.device):
+        st = load().gemm_bf16_swiglu_path(a_ptr, g_ptr, u_ptr, c_ptr, M, N, K, lda, ldg, ldc, path,
+                                          _stream_handle(stream))
+    _check(st, "gemm_bf16_swiglu")
+    return C
+
+
 def gemv_bf16(A, B, C=None, stream=None, path: int = PATH_AUTO):
     """The skinny path (1 <= M <= 64); ``path`` picks the kernel (PATH_*)."""
     return _call("gemv_bf16", A, B, C, stream, path)
@@ -218,6 +250,14 @@ def gemv_bf16_noalloc(A, B, C=None, stream=None):
 def plan(M: int, N: int, K: int, num_sms: int, entry: int = 0) -> dict:
     info = PlanInfo()
     _check(load().sg_plan(M, N, K, num_sms, entry, ctypes.byref(info)), "sg_plan")
+    d = info.as_dict()
+    d["_struct"] = info
+    return d
+
+
+def plan_swiglu(M: int, N: int, K: int, num_sms: int, entry: int = 0) -> dict:
+    info = PlanInfo()
+    _check(load().sg_plan_swiglu(M, N, K, num_sms, entry, ctypes.byref(info)), "sg_plan_swiglu")
     d = info.as_dict()
     d["_struct"] = info
     return d

@@ -233,6 +233,39 @@ void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_i
 
 bool auto_pair(int64_t M) { return M >= 2 * kBM; }
 
+// Most Stream-K pieces any CTA of the schedule runs.
+int32_t max_sk_items(const Schedule& s) {
+  int32_t m = 0;
+  for (int32_t c = 0; c < s.grid; ++c) m = std::max(m, sk_count(s, c));
+  return m;
+}
+
+// Gated GEMM plan (silu(A . G^T) * (A . U^T)): single-CTA tiles of 128 rows x 128
+// output columns (each computed from 128 gate and 128 up weight rows).  Stream-K
+// stays only where no CTA gets more pieces than the fixup warps take.
+void plan_tc_swiglu(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+  std::memset(o, 0, sizeof *o);
+  o->path = SG_PATH_GEMM;
+  o->tile_m = kBM;
+  o->tile_n = kGemmBN / 2;
+  o->tile_k = kBK;
+  o->stages = kGemmStages;
+  o->cluster_size = 1;
+  o->ctas_per_sm = 1;
+  const int32_t tm = static_cast<int32_t>(ceil_div(M, kBM)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN / 2));
+  const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
+  Schedule s = make_schedule(tm, tn, ks, sms, 4, std::min<int32_t>(tm, 8), false);
+  if (s.sk_tiles > 0 && max_sk_items(s) > kFixupMaxJobs) {
+    s.dp_tiles += s.sk_tiles;
+    s.sk_tiles = 0;
+    s.sk_units = 0;
+    s.sk_q = s.sk_r = 0;
+  }
+  fill_sched(o, s);
+  o->split_k = 0;
+  o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, sms);
+}
+
 int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
 // Swapped skinny plan: 64-row weight tiles, two CTAs per SM.  When every tile
@@ -356,6 +389,22 @@ int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, 
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
+int run_tc_swiglu(DeviceState& d, int dev, const void* A, const void* Wg, const void* Wu, void* C, int64_t M,
+                  int64_t N, int64_t K, int64_t lda, int64_t ldw, int64_t ldc, cudaStream_t stream) {
+  sg_plan_info plan;
+  plan_tc_swiglu(M, N, K, d.sm_count, &plan);
+  CUtensorMap ta, tg, tu, tc;
+  int st = make_map(&ta, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tg, Wg, N, K, ldw, kGemmBN / 2, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tu, Wu, N, K, ldw, kGemmBN / 2, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, dev);
+  if (st != SG_OK) return st;
+  TcParams p = base_params(d, M, N, K, ldc, C);
+  p.sched = sched_from_plan(plan);
+  cudaError_t e = launch_tc_gemm_swiglu(ta, tg, tu, tc, p, stream);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
 int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                   int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
   sg_plan_info plan;
@@ -467,6 +516,41 @@ int gemv_bf16_path(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 int gemv_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
               int64_t ldc, sg_stream_t stream) {
   return gemv_bf16_path(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, stream);
+}
+
+int gemm_bf16_swiglu_path(const void* A, const void* Wg, const void* Wu, void* C, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldw, int64_t ldc, int path, sg_stream_t stream) {
+  if (path != SG_PATH_AUTO && path != SG_PATH_GEMM) return SG_ERR_INVALID_ARG;
+  int st = validate(A, Wg, C, M, N, K, lda, ldw, ldc);
+  if (st == SG_OK && M > 0 && N > 0 && K > 0) {
+    if (!Wu) return SG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(Wu) & 15u) return SG_ERR_MISALIGNED;
+  }
+  if (st != SG_OK || M == 0 || N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState* d = nullptr;
+  int dev = 0;
+  st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  if (K == 0) {  // silu(0) * 0 = 0
+    cudaError_t e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, s);
+    return e == cudaSuccess ? SG_OK : cuda_fail(e);
+  }
+  st = ensure_workspace(*d, s);
+  if (st != SG_OK) return st;
+  return run_tc_swiglu(*d, dev, A, Wg, Wu, C, M, N, K, lda, ldw, ldc, s);
+}
+
+int gemm_bf16_swiglu(const void* A, const void* Wg, const void* Wu, void* C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldw, int64_t ldc, sg_stream_t stream) {
+  return gemm_bf16_swiglu_path(A, Wg, Wu, C, M, N, K, lda, ldw, ldc, SG_PATH_AUTO, stream);
+}
+
+int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info* out) {
+  if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
+  if (entry != SG_PATH_AUTO && entry != SG_PATH_GEMM) return SG_ERR_INVALID_ARG;
+  plan_tc_swiglu(M, N, K, num_sms, out);
+  return SG_OK;
 }
 
 const char* sg_status_string(int status) {

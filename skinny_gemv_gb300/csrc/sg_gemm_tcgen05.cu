@@ -64,7 +64,7 @@ struct TcLayout {
   // epilogue of the tiles after it (the skinny variant's split pieces end the
   // CTA's schedule and are summed from the idle copy ring instead).
   static constexpr int kFixupWarps = SWAP ? 0 : 2;
-  static constexpr int kMaxJobs = 4;  // Stream-K pieces per CTA the fixup warps take
+  static constexpr int kMaxJobs = kFixupMaxJobs;  // Stream-K pieces per CTA the fixup warps take
   static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kFixupWarps;
   static constexpr int kColsPerEpiWarp = BN / (kEpiWarps / 4);
   static constexpr int kStagingBufBytes = 32 * 64;  // 32 rows x 32 bf16
@@ -105,6 +105,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// SwiGLU of one output: silu(g) * u = g / (1 + e^-g) * u in fp32; for g far
+// below zero e^-g is inf and the result the correct limit, a signed zero.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -139,13 +143,19 @@ __device__ __forceinline__ void store_rows_32x32(const CUtensorMap* tmC, const f
   ++count;
 }
 
-template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR>
+// GATED: the B tile is BN / 2 rows of the gate weights (tmB) over BN / 2 rows
+// of the up weights (tmB2) for the same output columns; the epilogue writes
+// silu(gate) * up, BN / 2 columns per tile.
+template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR, bool GATED>
 __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::kThreads,
                                   TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::kMinBlocks)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
+                   const TcParams p) {
   using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
   constexpr bool SWAP = L::SWAP;
+  static_assert(!GATED || (!SWAP && !PAIR), "the gated epilogue is built on the single-CTA GEMM");
+  constexpr int kOutCols = GATED ? BN / 2 : BN;  // output columns per tile
   constexpr int kTileRows = PAIR ? 2 * kBM : L::kARows;  // output rows per tile (the MMA's M)
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, BN);
   const int kboxes = (p.K + kBK - 1) / kBK;  // 64-wide k boxes that hold data
@@ -191,6 +201,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
+    if (GATED) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
         int32_t tm, tn;
         tile_coords(sched, w.tile, tm, tn);
         const int arow = tm * kTileRows + static_cast<int>(rank) * L::kARows;
-        const int brow = tn * BN + static_cast<int>(rank) * L::kBRowsPerCta;
+        const int brow = tn * kOutCols + static_cast<int>(rank) * L::kBRowsPerCta;
         for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -249,8 +260,15 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
             mbar_arrive_expect_tx(&full[s], bytes + extra);
             for (int j = 0; j < nsub; ++j) {
               const int kx = (ks * KSUB + j) * kBK;
+              uint8_t* bdst = smem + L::kBOff + s * L::kBBytes + j * L::kBSub;
               tma_load_2d(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, arow, &full[s]);
-              tma_load_2d(smem + L::kBOff + s * L::kBBytes + j * L::kBSub, &tmB, kx, brow, &full[s]);
+              if constexpr (GATED) {
+                // gate rows over up rows of the same output columns
+                tma_load_2d(bdst, &tmB, kx, brow, &full[s]);
+                tma_load_2d(bdst + L::kBSub / 2, &tmB2, kx, brow, &full[s]);
+              } else {
+                tma_load_2d(bdst, &tmB, kx, brow, &full[s]);
+              }
             }
           }
         }
@@ -353,7 +371,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
     // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
     auto emit_chunk = [&](const float* v, int tm, int tn, int j) {
       if constexpr (!SWAP) {
-        store_rows_32x32(&tmC, v, tn * BN + j * 32, tm * kTileRows + static_cast<int>(rank) * kBM + q * 32, staging,
+        store_rows_32x32(&tmC, v, tn * kOutCols + j * 32, tm * kTileRows + static_cast<int>(rank) * kBM + q * 32, staging,
                          store_count, lane, p.M, p.N);
       } else {
         // D[n][m]: this thread's row is weight row n, its columns activation rows
@@ -434,7 +452,24 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + b * BN;
       float v[L::kChunk];
-      if (w.npieces == 1) {
+      if (GATED && w.npieces == 1) {
+        // Whole gated tile: output chunk j combines accumulator columns j * 32
+        // (gate) and kOutCols + j * 32 (up) of this thread's row.
+        begin_tile();
+#pragma unroll 1
+        for (int jo = 0; jo < kOutCols / 32; ++jo) {
+          uint32_t rg[L::kChunk], ru[L::kChunk];
+          issue_chunk(tacc + jo * 32, rg);
+          issue_chunk(tacc + kOutCols + jo * 32, ru);
+          tmem_ld_wait(rg);
+          tmem_ld_wait(ru);
+#pragma unroll
+          for (int e = 0; e < L::kChunk; ++e) v[e] = silu_mul(__uint_as_float(rg[e]), __uint_as_float(ru[e]));
+          emit_chunk(v, tm, tn, jo);
+        }
+        release_accumulator(b);
+        end_tile(tm, tn);
+      } else if (w.npieces == 1) {
         // Whole tile: the TMEM load of chunk j + 1 is in flight while chunk j is
         // converted and stored.
         constexpr int kChunks = L::kColsPerEpiWarp / L::kChunk;
@@ -488,6 +523,11 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
             job[2] = static_cast<int32_t>(*sk_last);
             mbar_arrive(&job_bar[i]);
           }
+          continue;
+        }
+        if constexpr (GATED) {
+          // the gated plan gives no CTA more Stream-K pieces than the fixup warps take
+          if (epi_tid == 0) record_error(p.err, kDevTimeoutFull, 3000 + i);
           continue;
         }
         // The finisher's last item: the copy ring is idle (every stage of this CTA
@@ -615,40 +655,51 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
       const int tm = job[0], tn = job[1];
       if (!job[2]) continue;
       __threadfence();  // the other pieces' partials were published before their arrivals
-#pragma unroll 1
-      for (int j = 0; j < BN / 32; ++j) {
-#pragma unroll 1
-        for (int g = 0; g < 2; ++g) {
-          const int frow = fw * 64 + g * 32 + lane;
-          float acc[32];
-          for (int pj = 0; pj < w.npieces; pj += 4) {
-            float4 x[4][kQuads];
+      // Sums 32-column chunk j of every piece's partial for row frow, in k order.
+      constexpr int kFB = GATED ? 1 : 4;  // pieces whose loads are in flight together
+      auto sum_chunk = [&](int j, int frow, float* acc) {
+        for (int pj = 0; pj < w.npieces; pj += kFB) {
+          float4 x[kFB][kQuads];
 #pragma unroll
-            for (int bi = 0; bi < 4; ++bi) {
-              if (pj + bi < w.npieces) {
-                const int64_t sl = piece_slot(sched, w.sk_index, pj + bi);
-                const float4* src =
-                    reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl + rank : sl) * kSlotFloats);
+          for (int bi = 0; bi < kFB; ++bi) {
+            if (pj + bi < w.npieces) {
+              const int64_t sl = piece_slot(sched, w.sk_index, pj + bi);
+              const float4* src =
+                  reinterpret_cast<const float4*>(p.partials + (PAIR ? 2 * sl + rank : sl) * kSlotFloats);
 #pragma unroll
-                for (int q4 = 0; q4 < kQuads; ++q4) x[bi][q4] = __ldcg(&src[(j * kQuads + q4) * kBM + frow]);
-              }
+              for (int q4 = 0; q4 < kQuads; ++q4) x[bi][q4] = __ldcg(&src[(j * kQuads + q4) * kBM + frow]);
             }
+          }
 #pragma unroll
-            for (int bi = 0; bi < 4; ++bi) {  // k order: pieces pj, pj + 1, ...
-              if (pj + bi < w.npieces) {
+          for (int bi = 0; bi < kFB; ++bi) {  // k order: pieces pj, pj + 1, ...
+            if (pj + bi < w.npieces) {
 #pragma unroll
-                for (int q4 = 0; q4 < kQuads; ++q4) {
-                  float* a4 = &acc[4 * q4];
-                  if (pj + bi == 0) {
-                    a4[0] = x[bi][q4].x; a4[1] = x[bi][q4].y; a4[2] = x[bi][q4].z; a4[3] = x[bi][q4].w;
-                  } else {
-                    a4[0] += x[bi][q4].x; a4[1] += x[bi][q4].y; a4[2] += x[bi][q4].z; a4[3] += x[bi][q4].w;
-                  }
+              for (int q4 = 0; q4 < kQuads; ++q4) {
+                float* a4 = &acc[4 * q4];
+                if (pj + bi == 0) {
+                  a4[0] = x[bi][q4].x; a4[1] = x[bi][q4].y; a4[2] = x[bi][q4].z; a4[3] = x[bi][q4].w;
+                } else {
+                  a4[0] += x[bi][q4].x; a4[1] += x[bi][q4].y; a4[2] += x[bi][q4].z; a4[3] += x[bi][q4].w;
                 }
               }
             }
           }
-          store_rows_32x32(&tmC, acc, tn * BN + j * 32,
+        }
+      };
+#pragma unroll 1
+      for (int j = 0; j < kOutCols / 32; ++j) {
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          const int frow = fw * 64 + g * 32 + lane;
+          float acc[32];
+          sum_chunk(j, frow, acc);
+          if constexpr (GATED) {
+            float up[32];
+            sum_chunk(j + kOutCols / 32, frow, up);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = silu_mul(acc[e], up[e]);
+          }
+          store_rows_32x32(&tmC, acc, tn * kOutCols + j * 32,
                            tm * kTileRows + static_cast<int>(rank) * kBM + fw * 64 + g * 32, fstaging,
                            fstore_count, lane, p.M, p.N);
         }
@@ -670,11 +721,11 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
   }
 }
 
-template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR>
+template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR, bool GATED = false>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const CUtensorMap* b2 = nullptr) {
   using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
-  auto kern = tc_gemm_kernel<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
+  auto kern = tc_gemm_kernel<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   static bool configured = false;  // the attribute is per function, process-wide
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
@@ -695,7 +746,7 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, b2 ? *b2 : b, p);
 }
 
 }  // namespace
@@ -703,6 +754,11 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
 cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const TcParams& p, cudaStream_t stream) {
   return launch_variant<kGemmBN, kGemmStages, 0, 1, false>(tmA, tmB, tmC, p, stream);
+}
+
+cudaError_t launch_tc_gemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmG, const CUtensorMap& tmU,
+                                  const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
+  return launch_variant<kGemmBN, kGemmStages, 0, 1, false, true>(tmA, tmG, tmC, p, stream, &tmU);
 }
 
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,

@@ -17,6 +17,9 @@ constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
 constexpr int kGemmBN = 256;
 constexpr int kGemmStages = 4;
 constexpr int kPairStages = 6;  // paired tiles: 32 KB per stage per CTA
+// Stream-K pieces per CTA that the GEMM's fixup warps take (more fall back to
+// the epilogue warps; the gated GEMM's plans never give more).
+constexpr int kFixupMaxJobs = 4;
 // Skinny (swapped) path: two CTAs per SM, each with at most kSkinnySmemBytes of
 // copy ring plus output staging (two such CTAs and their barriers fit in an SM's
 // 228 KB).  A weight tile is `rows` = 64 or 128 weight rows (MMA M); each stage
@@ -52,6 +55,11 @@ struct TcParams {
 // Non-swapped GEMM: A-operand = A (rows M), B-operand = B (rows N), BN = 256.
 cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const TcParams& p, cudaStream_t stream);
+
+// Gated GEMM: C = silu(A . G^T) * (A . U^T); each 128 x 256 B tile is 128 rows of
+// G over 128 rows of U (boxes 64 x 128 each), 128 output columns per tile.
+cudaError_t launch_tc_gemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmG, const CUtensorMap& tmU,
+                                  const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream);
 
 // Paired GEMM over clusters of two CTAs: 256 x 256 tiles, p.sched counts pairs.
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,

@@ -244,3 +244,14 @@ def test_plan_rejects_bad_arguments(lib):
     assert lib.sg_plan(-1, 8, 8, 152, 0, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
     assert lib.sg_plan(8, 8, 8, 0, 0, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
     assert lib.sg_plan(65, 8, 8, 152, sg.PATH_CUDA_CORE, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 11008, 4096), (2048, 4096, 4096), (128, 128, 64), (1000, 3000, 200),
+                                   (16, 11008, 4096), (130, 257, 128)])
+def test_swiglu_plan_covers_every_unit_once(lib, M, N, K):
+    info = sg.plan_swiglu(M, N, K, 152)
+    assert info["path"] == sg.PATH_GEMM and info["tile_m"] == 128 and info["tile_n"] == 128
+    assert info["tiles_m"] == -(-M // 128) and info["tiles_n"] == -(-N // 128)
+    items = _check_plan_coverage(info)
+    # no CTA gets more Stream-K pieces than the fixup warps take
+    assert max(sum(1 for it in row if it[4] > 1) for row in items) <= 4

@@ -1,0 +1,109 @@
+"""Parity of the fused gate/up projection with its SwiGLU epilogue,
+gemm_bf16_swiglu: C = silu(A . Wg^T) * (A . Wu^T), against the fp64 oracle
+(oracle.swiglu), within the benchmark spec's tolerance (tests/_parity.py).  The fp32
+accumulators, the fp32 SiLU and product and the bf16 rounding of the output
+keep the GPU's error near the output rounding; the tolerance is the GEMM's.
+
+Covers tiles with ragged M, N and K, leading dimensions wider than the rows,
+Stream-K tiles (whose partial sums the fixup warps combine before the gate),
+the 7B-model gate/up shape on sampled rows and columns, determinism, K = 0 and
+argument errors."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as syn
+from _parity import assert_close, to_bits, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import skinny_gemv_gb300 as sg  # noqa: E402
+
+
+def _run(A_bits, G_bits, U_bits, M, N, K, path=sg.PATH_AUTO):
+    A = to_device(A_bits, K)
+    Wg = to_device(G_bits, K)
+    Wu = to_device(U_bits, K)
+    ld = -(-N // 8) * 8
+    Cfull = torch.empty((M, ld), dtype=torch.bfloat16, device="cuda")
+    sg.gemm_bf16_swiglu(A, Wg, Wu, Cfull[:, :N], path=path)
+    torch.cuda.synchronize()
+    return to_bits(Cfull)[:, :N]
+
+
+def _inputs(M, N, K, seed, ld=None):
+    A = syn.matrix(M, K, "normal:1", seed, ld=ld)
+    G = syn.matrix(N, K, "normal:0.05", seed + 1, ld=ld)
+    U = syn.matrix(N, K, "normal:0.05", seed + 2, ld=ld)
+    return A, G, U
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (128, 256, 512), (200, 300, 192), (130, 257, 128),
+                                   (65, 1000, 1024), (1000, 96, 4104)])
+def test_full_oracle(M, N, K):
+    A, G, U = _inputs(M, N, K, 700 + M + N)
+    assert_close(_run(A, G, U, M, N, K), oracle.swiglu(A, G, U), K, f"swiglu {M}x{N}x{K}")
+
+
+def test_padded_leading_dimensions():
+    M, N, K = 150, 140, 200
+    A, G, U = _inputs(M, N, K, 801, ld=216)
+    assert_close(_run(A, G, U, M, N, K), oracle.swiglu(A, G, U, K=K), K, "padded")
+
+
+def test_stream_k_tiles_are_gated_after_the_sum():
+    # 2048 x 4096 x 4096: 512 tiles of 128 x 128 over the SMs leave a Stream-K
+    # remainder; each split tile's gate and up sums are combined by the fixup
+    # warps before the SiLU.
+    M, N, K = 2048, 4096, 4096
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    info = sg.plan_swiglu(M, N, K, sms)
+    assert info["sk_tiles"] > 0
+    A, G, U = _inputs(M, N, K, 811)
+    got = _run(A, G, U, M, N, K)
+    rows = syn.sample_indices(M, 256, 3)
+    ref = oracle.silu(oracle.gemm(A[rows], G)) * oracle.gemm(A[rows], U)
+    assert_close(got[rows], ref, K, "stream-k")
+
+
+def test_mlp_gate_up_shape_sampled():
+    # the 7B model's gate/up projection: M = 4096 tokens, K = 4096, N = 11008
+    w = syn.WORKLOADS["mlp_up"]
+    A = w.a()
+    G = w.b()
+    U = syn.matrix(w.N, w.K, w.dist_b, w.seed_b + 77)
+    got = _run(A, G, U, w.M, w.N, w.K)
+    rows = syn.sample_indices(w.M, 128, 5)
+    cols = syn.sample_indices(w.N, 128, 6)
+    g = oracle.gemm_sampled(A, G, rows, cols)
+    u = oracle.gemm_sampled(A, U, rows, cols)
+    assert_close(got[np.ix_(rows, cols)], oracle.silu(g) * u, w.K, "mlp gate/up sampled")
+
+
+def test_deterministic():
+    M, N, K = 1024, 2048, 2048
+    A, G, U = (to_device(x) for x in _inputs(M, N, K, 821))
+    C1 = sg.gemm_bf16_swiglu(A, G, U)
+    for _ in range(2):
+        C2 = sg.gemm_bf16_swiglu(A, G, U)
+        torch.cuda.synchronize()
+        assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+def test_zero_k_and_errors():
+    A = torch.zeros((4, 8), dtype=torch.bfloat16, device="cuda")[:, :0]   # K = 0, rows 16-byte aligned
+    W = torch.zeros((16, 8), dtype=torch.bfloat16, device="cuda")[:, :0]
+    C = torch.full((4, 16), 3.0, dtype=torch.bfloat16, device="cuda")
+    sg.gemm_bf16_swiglu(A, W, W, C)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(C).item() == 0
+    A = torch.randn(64, 64, device="cuda").bfloat16()
+    W = torch.randn(64, 64, device="cuda").bfloat16()
+    lib = sg.load()
+    st = lib.gemm_bf16_swiglu(A.data_ptr(), W.data_ptr(), None, torch.empty_like(A).data_ptr(), 64, 64, 64,
+                              64, 64, 64, None)
+    assert st == sg.SG_ERR_INVALID_ARG
+    st = lib.gemm_bf16_swiglu(A.data_ptr(), W.data_ptr(), W.data_ptr() + 2, torch.empty_like(A).data_ptr(),
+                              64, 64, 64, 64, 64, 64, None)
+    assert st == sg.SG_ERR_MISALIGNED
