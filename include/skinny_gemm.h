@@ -129,16 +129,20 @@ SG_API int gemv_bf16_path(const void *A, const void *B, void *C,
  * product are fp32 (expf); C is rounded to bf16 (nearest even).  G and U are
  * never written to memory.
  *
- * Kernel: the single-CTA tcgen05 GEMM with each B tile made of 128 rows of Wg
- * over 128 rows of Wu (128 output columns per tile), for every M.  Same errors
- * as gemm_bf16 (a null or misaligned Wu as for B).  K = 0 gives C = 0.
+ * Kernels (SG_PATH_AUTO): M <= 2, the CUDA-core stream, each CTA reading the gate
+ * and up rows of its outputs once for all M rows (paired FMAs on gate and up);
+ * 3 <= M <= 64, the swapped tcgen05 kernel with a gate and an up accumulator
+ * side by side in TMEM (64 outputs per tile); M > 64, the single-CTA tcgen05
+ * GEMM with each B tile made of 128 rows of Wg over 128 rows of Wu (128 output
+ * columns per tile).  Same errors as gemm_bf16 (a null or misaligned Wu as for
+ * B).  K = 0 gives C = 0.
  */
 SG_API int gemm_bf16_swiglu(const void *A, const void *Wg, const void *Wu, void *C,
                      int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldw, int64_t ldc, sg_stream_t stream);
 
-/* gemm_bf16_swiglu with the kernel named: SG_PATH_AUTO or SG_PATH_GEMM (others:
- * SG_ERR_INVALID_ARG). */
+/* gemm_bf16_swiglu with the kernel named: SG_PATH_AUTO, SG_PATH_GEMM (any M), or
+ * SG_PATH_CUDA_CORE / SG_PATH_TENSOR_CORE (M <= 64); others SG_ERR_INVALID_ARG. */
 SG_API int gemm_bf16_swiglu_path(const void *A, const void *Wg, const void *Wu, void *C,
                           int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldw, int64_t ldc, int path, sg_stream_t stream);
@@ -255,9 +259,10 @@ typedef struct {
  */
 SG_API int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
 
-/* sg_plan_swiglu -- the launch plan of gemm_bf16_swiglu_path (entry SG_PATH_AUTO
- * or SG_PATH_GEMM): tile_n counts output columns (each from tile_n gate and
- * tile_n up weight rows). */
+/* sg_plan_swiglu -- the launch plan of gemm_bf16_swiglu_path for `entry` (an
+ * sg_path it accepts).  GEMM plans: tile_n counts output columns (each from
+ * tile_n gate and tile_n up weight rows); tensor-core skinny plans: tile_m
+ * counts outputs (each from one gate and one up weight row). */
 SG_API int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
 
 /*

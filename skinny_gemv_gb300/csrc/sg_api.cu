@@ -277,14 +277,14 @@ int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 // decode shapes (fewer, longer-latency stages and larger partial sums).
 int skinny_rows(int64_t) { return 64; }
 
-void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o, bool gated = false) {
   std::memset(o, 0, sizeof *o);
-  const int rows = skinny_rows(M);
+  const int rows = gated ? 64 : skinny_rows(M);  // gated: 64 outputs from 64 gate + 64 up rows
   o->path = SG_PATH_TENSOR_CORE;
   o->tile_m = rows;
   o->tile_n = skinny_bn(M);
-  o->tile_k = kBK * skinny_ksub(rows);
-  o->stages = skinny_stages(o->tile_n, rows);
+  o->tile_k = gated ? kBK : kBK * skinny_ksub(rows);
+  o->stages = gated ? skinny_stages_gated(o->tile_n) : skinny_stages(o->tile_n, rows);
   o->cluster_size = 1;
   o->ctas_per_sm = kSkinnyCtasPerSm;
   const int32_t tm = static_cast<int32_t>(ceil_div(N, rows));
@@ -306,7 +306,7 @@ void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
 // CUDA-core plan: two CTAs per SM, each owning a contiguous block of weight rows
 // (at most kCcMaxRowsPerCta); K is split across CTAs only when there are fewer
 // row blocks than that.
-void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o, bool gated = false) {
   std::memset(o, 0, sizeof *o);
   o->path = SG_PATH_CUDA_CORE;
   o->cluster_size = 1;
@@ -321,7 +321,7 @@ void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   split = ceil_div(K, k_slice);
   if (split < 1) split = 1;
   const int64_t mrows = std::min<int64_t>(M, 8);
-  if (split > 1 && (static_cast<size_t>(split) * mrows * N * 4 > kPartialBytes ||
+  if (split > 1 && (static_cast<size_t>(split) * mrows * N * 4 * (gated ? 2 : 1) > kPartialBytes ||
                     static_cast<size_t>(rows_grid) > kNumCounters)) {
     split = 1;
     k_slice = ceil_div(K, 8) * 8;
@@ -343,6 +343,9 @@ void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
 // beyond which the tcgen05 kernel (same single pass over the weights) is faster.
 constexpr int64_t kCudaCoreMaxRows = 2;
 int choose_skinny_path(int64_t M) { return M <= kCudaCoreMaxRows ? SG_PATH_CUDA_CORE : SG_PATH_TENSOR_CORE; }
+
+// The gated entry's automatic kernel: the skinny kernels up to M = 64, the GEMM after.
+int swiglu_path(int64_t M) { return M <= 64 ? choose_skinny_path(M) : SG_PATH_GEMM; }
 
 // ----------------------------------------------------------------- validation
 int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -405,6 +408,22 @@ int run_tc_swiglu(DeviceState& d, int dev, const void* A, const void* Wg, const 
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
+int run_tc_skinny_swiglu(DeviceState& d, int dev, const void* A, const void* Wg, const void* Wu, void* C, int64_t M,
+                         int64_t N, int64_t K, int64_t lda, int64_t ldw, int64_t ldc, cudaStream_t stream) {
+  sg_plan_info plan;
+  plan_tc_skinny(M, N, K, d.sm_count, &plan, true);
+  CUtensorMap tg, tu, tx, tc;
+  int st = make_map(&tg, Wg, N, K, ldw, plan.tile_m, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tu, Wu, N, K, ldw, plan.tile_m, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, plan.tile_n, plan.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE, dev);
+  if (st != SG_OK) return st;
+  TcParams p = base_params(d, M, N, K, ldc, C);
+  p.sched = sched_from_plan(plan);
+  cudaError_t e = launch_tc_skinny_swiglu(plan.tile_n, tg, tu, tx, tc, p, stream);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
 int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                   int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
   sg_plan_info plan;
@@ -421,15 +440,16 @@ int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C
 }
 
 int run_cc(DeviceState& d, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-           int64_t ldb, int64_t ldc, cudaStream_t stream) {
+           int64_t ldb, int64_t ldc, cudaStream_t stream, const void* B2 = nullptr) {
   // At most 8 activation rows per launch; larger M runs as consecutive row blocks.
   for (int64_t m0 = 0; m0 < M; m0 += 8) {
     const int64_t mb = std::min<int64_t>(8, M - m0);
     sg_plan_info plan;
-    plan_cc(mb, N, K, d.sm_count, &plan);
+    plan_cc(mb, N, K, d.sm_count, &plan, B2 != nullptr);
     CcParams p{};
     p.A = static_cast<const uint16_t*>(A) + m0 * lda;
     p.B = static_cast<const uint16_t*>(B);
+    p.B2 = static_cast<const uint16_t*>(B2);
     p.C = static_cast<uint16_t*>(C) + m0 * ldc;
     p.M = static_cast<int32_t>(mb);
     p.N = static_cast<int32_t>(N);
@@ -520,7 +540,9 @@ int gemv_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
 
 int gemm_bf16_swiglu_path(const void* A, const void* Wg, const void* Wu, void* C, int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldw, int64_t ldc, int path, sg_stream_t stream) {
-  if (path != SG_PATH_AUTO && path != SG_PATH_GEMM) return SG_ERR_INVALID_ARG;
+  if (path != SG_PATH_AUTO && path != SG_PATH_GEMM && path != SG_PATH_CUDA_CORE && path != SG_PATH_TENSOR_CORE)
+    return SG_ERR_INVALID_ARG;
+  if ((path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE) && M > 64) return SG_ERR_INVALID_ARG;
   int st = validate(A, Wg, C, M, N, K, lda, ldw, ldc);
   if (st == SG_OK && M > 0 && N > 0 && K > 0) {
     if (!Wu) return SG_ERR_INVALID_ARG;
@@ -538,6 +560,9 @@ int gemm_bf16_swiglu_path(const void* A, const void* Wg, const void* Wu, void* C
   }
   st = ensure_workspace(*d, s);
   if (st != SG_OK) return st;
+  if (path == SG_PATH_AUTO) path = swiglu_path(M);
+  if (path == SG_PATH_CUDA_CORE) return run_cc(*d, A, Wg, C, M, N, K, lda, ldw, ldc, s, Wu);
+  if (path == SG_PATH_TENSOR_CORE) return run_tc_skinny_swiglu(*d, dev, A, Wg, Wu, C, M, N, K, lda, ldw, ldc, s);
   return run_tc_swiglu(*d, dev, A, Wg, Wu, C, M, N, K, lda, ldw, ldc, s);
 }
 
@@ -548,8 +573,16 @@ int gemm_bf16_swiglu(const void* A, const void* Wg, const void* Wu, void* C, int
 
 int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info* out) {
   if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
-  if (entry != SG_PATH_AUTO && entry != SG_PATH_GEMM) return SG_ERR_INVALID_ARG;
-  plan_tc_swiglu(M, N, K, num_sms, out);
+  if (entry != SG_PATH_AUTO && entry != SG_PATH_GEMM && entry != SG_PATH_CUDA_CORE && entry != SG_PATH_TENSOR_CORE)
+    return SG_ERR_INVALID_ARG;
+  if ((entry == SG_PATH_CUDA_CORE || entry == SG_PATH_TENSOR_CORE) && M > 64) return SG_ERR_INVALID_ARG;
+  const int path = entry == SG_PATH_AUTO ? swiglu_path(M) : entry;
+  if (path == SG_PATH_CUDA_CORE)
+    plan_cc(std::min<int64_t>(std::max<int64_t>(M, 1), 8), N, K, num_sms, out, true);
+  else if (path == SG_PATH_TENSOR_CORE)
+    plan_tc_skinny(M, N, K, num_sms, out, true);
+  else
+    plan_tc_swiglu(M, N, K, num_sms, out);
   return SG_OK;
 }
 

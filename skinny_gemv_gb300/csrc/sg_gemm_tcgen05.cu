@@ -45,16 +45,20 @@ namespace {
 // KSUB: consecutive 64-wide k boxes per pipeline stage (one schedule k-step).
 // PAIR: B's rows are split between the two CTAs of a pair (BN / 2 each).
 // SWAP_ROWS: 0 for the GEMM, else the swapped variant's weight rows per tile.
-template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR>
+// GATED: gate and up weights (see the kernel); the swapped variant keeps two
+// accumulators side by side in TMEM, gate in columns [0, BN), up in [BN, 2 BN).
+template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR, bool GATED = false>
 struct TcLayout {
   static constexpr bool SWAP = SWAP_ROWS > 0;
+  static constexpr int kAMats = (SWAP && GATED) ? 2 : 1;      // A-side boxes per k box
+  static constexpr int kAccCols = (SWAP && GATED) ? 2 * BN : BN;  // TMEM columns per accumulator
   // rows of the MMA's A operand per CTA: 128, or 64 / 128 weight rows on the
   // swapped path (an M = 64 accumulator sits in lanes 0-15 of each TMEM lane quarter)
   static constexpr int kARows = SWAP ? SWAP_ROWS : kBM;
   static constexpr int kBRowsPerCta = PAIR ? BN / 2 : BN;
   static constexpr int kASub = kARows * kBK * 2;  // one kARows x 64 box
   static constexpr int kBSub = kBRowsPerCta * kBK * 2;
-  static constexpr int kABytes = KSUB * kASub;
+  static constexpr int kABytes = KSUB * kAMats * kASub;
   static constexpr int kBBytes = KSUB * kBSub;
   // epilogue warps: one per TMEM lane quarter (eight, two per quarter, measured
   // no faster and would cap registers at 168)
@@ -74,6 +78,8 @@ struct TcLayout {
   static constexpr int kStagingOff = kBOff + STAGES * kBBytes;
   // swapped path: one C tile (BN activation rows x kARows weight rows, bf16)
   static constexpr int kStagingBytes = SWAP ? BN * kARows * 2 : kEpiWarps * kStagingBufs * kStagingBufBytes;
+  // columns of a Stream-K partial (all of an accumulator's columns)
+  static constexpr int kSlotCols = kAccCols;
   static constexpr int kFixStagingOff = kStagingOff + kStagingBytes;
   static constexpr int kFixStagingBytes = kFixupWarps * kStagingBufs * kStagingBufBytes;
   static constexpr int kBarOff = kFixStagingOff + kFixStagingBytes;
@@ -84,7 +90,7 @@ struct TcLayout {
   static constexpr int kJobOff = kMiscOff + 16;            // kMaxJobs x {tm, tn, last, -}
   static constexpr int kBytes = kJobOff + kMaxJobs * 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
-  static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32u : static_cast<uint32_t>(2 * BN);
+  static constexpr uint32_t kTmemCols = (2 * kAccCols < 32) ? 32u : static_cast<uint32_t>(2 * kAccCols);
   static constexpr int kChunk = SWAP ? 16 : 32;  // accumulator columns per tcgen05.ld
   // accumulator rows a Stream-K partial holds (an M = 64 accumulator has 64)
   static constexpr int kSlotRows = kARows;
@@ -143,19 +149,22 @@ __device__ __forceinline__ void store_rows_32x32(const CUtensorMap* tmC, const f
   ++count;
 }
 
-// GATED: the B tile is BN / 2 rows of the gate weights (tmB) over BN / 2 rows
-// of the up weights (tmB2) for the same output columns; the epilogue writes
-// silu(gate) * up, BN / 2 columns per tile.
+// GATED: C = silu(A . G^T) * (A . U^T) with tmW2 mapping the up weights U.  GEMM:
+// the B tile is BN / 2 rows of G (tmB) over BN / 2 rows of U for the same output
+// columns, and the epilogue writes BN / 2 columns per tile.  Swapped: each k box
+// holds a weight box of G (tmA) and one of U, two MMAs fill a gate and an up
+// accumulator, and each thread combines its row's two.
 template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR, bool GATED>
-__global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::kThreads,
-                                  TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::kMinBlocks)
+__global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>::kThreads,
+                                  TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>::kMinBlocks)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW2,
                    const TcParams p) {
-  using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
+  using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   constexpr bool SWAP = L::SWAP;
-  static_assert(!GATED || (!SWAP && !PAIR), "the gated epilogue is built on the single-CTA GEMM");
-  constexpr int kOutCols = GATED ? BN / 2 : BN;  // output columns per tile
+  static_assert(!GATED || !PAIR, "the gated variants are single-CTA kernels");
+  // output columns per tile; in a gated accumulator the up columns start here
+  constexpr int kOutCols = (GATED && !SWAP) ? BN / 2 : BN;
   constexpr int kTileRows = PAIR ? 2 * kBM : L::kARows;  // output rows per tile (the MMA's M)
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, BN);
   const int kboxes = (p.K + kBK - 1) / kBK;  // 64-wide k boxes that hold data
@@ -201,7 +210,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
-    if (GATED) tma_prefetch_desc(&tmB2);
+    if (GATED) tma_prefetch_desc(&tmW2);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
             break;
           }
           const int nsub = min(KSUB, kboxes - ks * KSUB);  // boxes past K are skipped
-          uint32_t bytes = static_cast<uint32_t>(nsub * (L::kASub + L::kBSub));
+          uint32_t bytes = static_cast<uint32_t>(nsub * (L::kAMats * L::kASub + L::kBSub));
           const uint32_t extra = (it == 0) ? p.inject_extra_tx : 0u;  // failure injection only
           if (it == 0) grid_dependency_wait();
           if constexpr (PAIR) {
@@ -261,11 +270,13 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
             for (int j = 0; j < nsub; ++j) {
               const int kx = (ks * KSUB + j) * kBK;
               uint8_t* bdst = smem + L::kBOff + s * L::kBBytes + j * L::kBSub;
-              tma_load_2d(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, arow, &full[s]);
-              if constexpr (GATED) {
+              uint8_t* adst = smem + L::kAOff + s * L::kABytes + j * L::kAMats * L::kASub;
+              tma_load_2d(adst, &tmA, kx, arow, &full[s]);
+              if constexpr (SWAP && GATED) tma_load_2d(adst + L::kASub, &tmW2, kx, arow, &full[s]);
+              if constexpr (GATED && !SWAP) {
                 // gate rows over up rows of the same output columns
                 tma_load_2d(bdst, &tmB, kx, brow, &full[s]);
-                tma_load_2d(bdst + L::kBSub / 2, &tmB2, kx, brow, &full[s]);
+                tma_load_2d(bdst + L::kBSub / 2, &tmW2, kx, brow, &full[s]);
               } else {
                 tma_load_2d(bdst, &tmB, kx, brow, &full[s]);
               }
@@ -299,7 +310,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * BN;
+        const uint32_t d_tmem = tmem_base + b * L::kAccCols;
         for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -312,18 +323,22 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
           tc_fence_after();
           const int nsub = min(KSUB, kboxes - ks * KSUB);
           for (int j = 0; j < nsub; ++j) {
-            const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes + j * L::kASub);
+            const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes + j * L::kAMats * L::kASub);
             const uint32_t b_addr = smem_u32(smem + L::kBOff + s * L::kBBytes + j * L::kBSub);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               // +32 bytes per 16 bf16 of K inside the 128-byte swizzle row
               const uint32_t acc = (ks > w.k0 || j > 0 || kk > 0) ? 1u : 0u;
-              if constexpr (PAIR)
+              if constexpr (PAIR) {
                 tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32),
                                  kIdesc, acc);
-              else
+              } else {
                 tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
                             acc);
+                if constexpr (SWAP && GATED)  // the up weights into the up accumulator
+                  tc_mma_bf16(d_tmem + BN, smem_desc_sw128(a_addr + L::kASub + kk * 32),
+                              smem_desc_sw128(b_addr + kk * 32), kIdesc, acc);
+              }
             }
           }
           // the stage is free (in both CTAs) once these MMAs have read it
@@ -433,7 +448,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
 
     constexpr int kQuads = L::kChunk / 4;
     constexpr int kSR = L::kSlotRows;
-    constexpr int64_t kSlotFloats = static_cast<int64_t>(kSR) * BN;  // one CTA's share of a tile
+    constexpr int64_t kSlotFloats = static_cast<int64_t>(kSR) * L::kSlotCols;  // one CTA's share of a tile
     for (int i = 0; i < nitems; ++i) {
       const WorkItem w = get_item(sched, unit, i);
       int32_t tm, tn;
@@ -450,17 +465,17 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
         break;
       }
       tc_fence_after();
-      const uint32_t tacc = tmem_base + lane_off + b * BN;
+      const uint32_t tacc = tmem_base + lane_off + b * L::kAccCols;
       float v[L::kChunk];
       if (GATED && w.npieces == 1) {
-        // Whole gated tile: output chunk j combines accumulator columns j * 32
-        // (gate) and kOutCols + j * 32 (up) of this thread's row.
+        // Whole gated tile: output chunk j combines accumulator columns j * kChunk
+        // (gate) and kOutCols + j * kChunk (up) of this thread's row.
         begin_tile();
 #pragma unroll 1
-        for (int jo = 0; jo < kOutCols / 32; ++jo) {
+        for (int jo = 0; jo < kOutCols / L::kChunk; ++jo) {
           uint32_t rg[L::kChunk], ru[L::kChunk];
-          issue_chunk(tacc + jo * 32, rg);
-          issue_chunk(tacc + kOutCols + jo * 32, ru);
+          issue_chunk(tacc + jo * L::kChunk, rg);
+          issue_chunk(tacc + kOutCols + jo * L::kChunk, ru);
           tmem_ld_wait(rg);
           tmem_ld_wait(ru);
 #pragma unroll
@@ -495,7 +510,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
         const int64_t my_slot = PAIR ? 2 * static_cast<int64_t>(w.slot) + rank : w.slot;
         const int counter = PAIR ? 2 * w.sk_index + static_cast<int>(rank) : w.sk_index;
         float4* slot = reinterpret_cast<float4*>(p.partials + my_slot * kSlotFloats);
-        for (int j = chunk_lo; j < chunk_hi; ++j) {
+        for (int j = 0; j < L::kAccCols / L::kChunk; ++j) {  // every accumulator column
           load_chunk(tacc + j * L::kChunk, v);
           if (holds_row) {
 #pragma unroll
@@ -525,11 +540,27 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
           }
           continue;
         }
-        if constexpr (GATED) {
+        if constexpr (GATED && !SWAP) {
           // the gated plan gives no CTA more Stream-K pieces than the fixup warps take
           if (epi_tid == 0) record_error(p.err, kDevTimeoutFull, 3000 + i);
           continue;
         }
+        // Writes output chunk jo from the summed accumulator chunks: chunk jo, or
+        // silu(chunk jo) * chunk jo + kOutCols / kChunk when gated.
+        auto emit_summed = [&](auto&& sum_chunk) {
+#pragma unroll 1
+          for (int jo = 0; jo < kOutCols / L::kChunk; ++jo) {
+            float acc[L::kChunk];
+            sum_chunk(jo, acc);
+            if constexpr (GATED) {
+              float up[L::kChunk];
+              sum_chunk(jo + kOutCols / L::kChunk, up);
+#pragma unroll
+              for (int e = 0; e < L::kChunk; ++e) acc[e] = silu_mul(acc[e], up[e]);
+            }
+            emit_chunk(acc, tm, tn, jo);
+          }
+        };
         // The finisher's last item: the copy ring is idle (every stage of this CTA
         // has been consumed), so all pieces' partials are fetched into it with
         // bulk copies under one barrier instead of dependent rounds of loads.
@@ -555,8 +586,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
           } else {
             begin_tile();
             const float4* rs = reinterpret_cast<const float4*>(ring);
-            for (int j = chunk_lo; j < chunk_hi; ++j) {
-              float acc[L::kChunk];
+            emit_summed([&](int j, float* acc) {
 #pragma unroll
               for (int e = 0; e < L::kChunk; ++e) acc[e] = 0.f;
               for (int pj = 0; pj < w.npieces && holds_row; ++pj) {  // k order
@@ -572,8 +602,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
                   }
                 }
               }
-              emit_chunk(acc, tm, tn, j);
-            }
+            });
             end_tile(tm, tn);
           }
           if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
@@ -581,11 +610,10 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
           // Last arrival: sum all pieces in k order, then store.
           __threadfence();
           // Loads in flight per batch: kBatch pieces x kBQuads float4 of one chunk.
-          constexpr int kBatch = kQuads <= 4 ? 4 : 2;  // pieces per batch (16 loads in flight)
+          constexpr int kBatch = (kQuads <= 4 && !GATED) ? 4 : 2;  // pieces per batch (8-16 loads in flight)
           constexpr int kBQuads = kQuads;                // float4 per piece per batch: the whole chunk
           begin_tile();
-          for (int j = chunk_lo; j < chunk_hi; ++j) {
-            float acc[L::kChunk];
+          emit_summed([&](int j, float* acc) {
 #pragma unroll
             for (int e = 0; e < L::kChunk; ++e) acc[e] = 0.f;
 #pragma unroll
@@ -619,8 +647,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
                 }
               }
             }
-            emit_chunk(acc, tm, tn, j);
-          }
+          });
           end_tile(tm, tn);
           if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
         }
@@ -724,7 +751,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>::k
 template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR, bool GATED = false>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
                            cudaStream_t stream, const CUtensorMap* b2 = nullptr) {
-  using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR>;
+  using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   auto kern = tc_gemm_kernel<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   static bool configured = false;  // the attribute is per function, process-wide
   if (!configured) {
@@ -772,6 +799,25 @@ cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
   static_assert(TcLayout<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>::kMinBlocks == kSkinnyCtasPerSm,
                 "the skinny plan counts on two resident CTAs per SM");
   return launch_variant<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>(tmW, tmX, tmC, p, stream);
+}
+
+template <int BN>
+cudaError_t launch_skinny_swiglu(const CUtensorMap& tmG, const CUtensorMap& tmU, const CUtensorMap& tmX,
+                                 const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
+  constexpr int kS = skinny_stages_gated(BN);
+  static_assert(TcLayout<BN, kS, 64, 1, false, true>::kMinBlocks == kSkinnyCtasPerSm,
+                "the skinny plan counts on two resident CTAs per SM");
+  return launch_variant<BN, kS, 64, 1, false, true>(tmG, tmX, tmC, p, stream, &tmU);
+}
+
+cudaError_t launch_tc_skinny_swiglu(int bn, const CUtensorMap& tmG, const CUtensorMap& tmU, const CUtensorMap& tmX,
+                                    const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
+  switch (bn) {
+    case 16: return launch_skinny_swiglu<16>(tmG, tmU, tmX, tmC, p, stream);
+    case 32: return launch_skinny_swiglu<32>(tmG, tmU, tmX, tmC, p, stream);
+    case 64: return launch_skinny_swiglu<64>(tmG, tmU, tmX, tmC, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUtensorMap& tmX,

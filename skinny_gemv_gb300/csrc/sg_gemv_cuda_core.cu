@@ -51,6 +51,9 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
+// silu(g) * u = g / (1 + e^-g) * u in fp32 (a signed zero where e^-g is inf).
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 // One butterfly step per lane bit OFF = 16, 8, ..., 1 over the N values still
 // held: lanes with that bit set keep the upper half, the others the lower half,
 // and each kept value gains its partner's copy.  Once one value is left, the
@@ -79,10 +82,13 @@ struct Butterfly {
 };
 
 // MT: activation rows held (>= M); R: weight rows per warp pass; U: 16-byte
-// vectors per lane per row in flight.
-template <int MT, int R, int U>
+// vectors per lane per row in flight.  GATED: the CTA's rows are outputs n, each
+// from weight row n of B (gate) and of B2 (up); a pass takes R / 2 outputs, their
+// gate and up rows sharing each paired FMA, and the result is silu(gate) * up.
+template <int MT, int R, int U, bool GATED>
 __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParams p) {
-  extern __shared__ float red[];  // [rows of this CTA][MT][kCcWarps]
+  extern __shared__ float red[];  // [rows of this CTA (x 2 gated)][MT][kCcWarps]
+  constexpr int kRowStep = GATED ? R / 2 : R;  // output rows per pass
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int row_lo = static_cast<int>((static_cast<int64_t>(blockIdx.x) * p.N) / p.grid_rows);
@@ -98,7 +104,7 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   grid_dependency_wait();  // no global access before the previous kernel has completed
 
   static_assert(R % 2 == 0, "weight rows are processed in pairs");
-  for (int r0 = row_lo; r0 < row_hi; r0 += R) {
+  for (int r0 = row_lo; r0 < row_hi; r0 += kRowStep) {
     // acc[r / 2][m] holds the fp32 sums of weight rows r (x) and r + 1 (y) for
     // activation row m; one paired FMA updates both.
     float2 acc[R / 2][MT];
@@ -110,8 +116,13 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     bool row_ok[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      row_ok[r] = r0 + r < row_hi;
-      brow[r] = p.B + static_cast<int64_t>(row_ok[r] ? r0 + r : r0) * p.ldb;
+      if constexpr (GATED) {  // gate and up rows of output r0 + r / 2
+        row_ok[r] = r0 + r / 2 < row_hi;
+        brow[r] = ((r & 1) ? p.B2 : p.B) + static_cast<int64_t>(row_ok[r] ? r0 + r / 2 : r0) * p.ldb;
+      } else {
+        row_ok[r] = r0 + r < row_hi;
+        brow[r] = p.B + static_cast<int64_t>(row_ok[r] ? r0 + r : r0) * p.ldb;
+      }
     }
     for (int v = v_lo + lane; v < v_hi; v += 32 * U) {
       uint4 wv[U][R];
@@ -182,25 +193,37 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     Butterfly<NV, 16>::run(v, lane, idx);
     if ((lane & ((32 / NV) - 1)) == 0) {  // one lane per value index
       const int r = idx / MT, m = idx % MT;
-      if (r0 + r < row_hi) red[((r0 + r - row_lo) * MT + m) * kCcWarps + warp] = v[0];
+      if constexpr (GATED) {  // red row 2 * output + (0 gate, 1 up)
+        if (r0 + r / 2 < row_hi) red[(((r0 - row_lo) * 2 + r) * MT + m) * kCcWarps + warp] = v[0];
+      } else {
+        if (r0 + r < row_hi) red[((r0 + r - row_lo) * MT + m) * kCcWarps + warp] = v[0];
+      }
     }
   }
   __syncthreads();
 
-  // Sum the warps' partials in warp order.
+  // Sum the warps' partials in warp order.  Split-K partials are [slice][gu][M][N]
+  // (gu = 0 gate, 1 up; one plane when not gated).
+  constexpr int kPlanes = GATED ? 2 : 1;
   const int rows = row_hi - row_lo;
   __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.C);
-  float* part = p.partials + static_cast<int64_t>(slice) * p.M * p.N;
+  float* part = p.partials + static_cast<int64_t>(slice) * kPlanes * p.M * p.N;
   for (int e = threadIdx.x; e < rows * p.M; e += blockDim.x) {
     const int r = e / p.M, m = e % p.M;
-    const float* src = red + (r * MT + m) * kCcWarps;
-    float s = src[0];
+    float s[kPlanes];
 #pragma unroll
-    for (int w = 1; w < kCcWarps; ++w) s += src[w];
-    if (p.split_k == 1)
-      C[static_cast<int64_t>(m) * p.ldc + row_lo + r] = __float2bfloat16_rn(s);
-    else
-      part[static_cast<int64_t>(m) * p.N + row_lo + r] = s;
+    for (int gu = 0; gu < kPlanes; ++gu) {
+      const float* src = red + ((r * kPlanes + gu) * MT + m) * kCcWarps;
+      s[gu] = src[0];
+#pragma unroll
+      for (int w = 1; w < kCcWarps; ++w) s[gu] += src[w];
+    }
+    if (p.split_k == 1) {
+      C[static_cast<int64_t>(m) * p.ldc + row_lo + r] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0]);
+    } else {
+#pragma unroll
+      for (int gu = 0; gu < kPlanes; ++gu) part[(static_cast<int64_t>(gu) * p.M + m) * p.N + row_lo + r] = s[gu];
+    }
   }
   if (p.split_k == 1) return;
 
@@ -218,21 +241,25 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   for (int e = threadIdx.x; e < rows * p.M; e += blockDim.x) {
     const int r = e / p.M, m = e % p.M;
     const int n = row_lo + r;
-    float s = 0.f;
-    for (int sl = 0; sl < p.split_k; ++sl) {
-      const float x = __ldcg(p.partials + (static_cast<int64_t>(sl) * p.M + m) * p.N + n);
-      s = (sl == 0) ? x : s + x;
+    float s[kPlanes];
+#pragma unroll
+    for (int gu = 0; gu < kPlanes; ++gu) {
+      s[gu] = 0.f;
+      for (int sl = 0; sl < p.split_k; ++sl) {
+        const float x = __ldcg(p.partials + ((static_cast<int64_t>(sl) * kPlanes + gu) * p.M + m) * p.N + n);
+        s[gu] = (sl == 0) ? x : s[gu] + x;
+      }
     }
-    C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(s);
+    C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0]);
   }
   if (threadIdx.x == 0) atomicExch(&p.counters[blockIdx.x], 0u);
 }
 
-template <int MT, int R, int U>
+template <int MT, int R, int U, bool GATED>
 cudaError_t launch_one(const CcParams& p, cudaStream_t stream) {
   const int rows_max = (p.N + p.grid_rows - 1) / p.grid_rows;
-  const size_t smem = static_cast<size_t>(rows_max) * MT * kCcWarps * sizeof(float);
-  auto kern = cc_gemv_kernel<MT, R, U>;
+  const size_t smem = static_cast<size_t>(rows_max) * (GATED ? 2 : 1) * MT * kCcWarps * sizeof(float);
+  auto kern = cc_gemv_kernel<MT, R, U, GATED>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -252,16 +279,23 @@ cudaError_t launch_one(const CcParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int cc_smem_bytes(int64_t M, int64_t N, int grid_rows) {
+int cc_smem_bytes(int64_t M, int64_t N, int grid_rows, bool gated) {
   const int64_t mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
-  return static_cast<int>(((N + grid_rows - 1) / grid_rows) * mt * kCcWarps * sizeof(float));
+  return static_cast<int>(((N + grid_rows - 1) / grid_rows) * (gated ? 2 : 1) * mt * kCcWarps * sizeof(float));
 }
 
 cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream) {
-  if (p.M <= 1) return launch_one<1, 8, 2>(p, stream);
-  if (p.M <= 2) return launch_one<2, 8, 2>(p, stream);
-  if (p.M <= 4) return launch_one<4, 4, 2>(p, stream);
-  if (p.M <= 8) return launch_one<8, 2, 2>(p, stream);
+  if (p.B2 != nullptr) {
+    if (p.M <= 1) return launch_one<1, 8, 2, true>(p, stream);
+    if (p.M <= 2) return launch_one<2, 8, 2, true>(p, stream);
+    if (p.M <= 4) return launch_one<4, 4, 2, true>(p, stream);
+    if (p.M <= 8) return launch_one<8, 2, 2, true>(p, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (p.M <= 1) return launch_one<1, 8, 2, false>(p, stream);
+  if (p.M <= 2) return launch_one<2, 8, 2, false>(p, stream);
+  if (p.M <= 4) return launch_one<4, 4, 2, false>(p, stream);
+  if (p.M <= 8) return launch_one<8, 2, 2, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -34,6 +34,13 @@ constexpr int skinny_stages(int bn, int rows) {
              ? 2
              : (kSkinnySmemBytes - bn * rows * 2) / (skinny_ksub(rows) * (rows + bn) * kBK * 2);
 }
+// Gated skinny kernel: 64 output rows per tile, each k box a 64-row box of the
+// gate weights and one of the up weights (one 64-wide k box per stage).
+constexpr int skinny_stages_gated(int bn) {
+  return (kSkinnySmemBytes - bn * 64 * 2) / ((2 * 64 + bn) * kBK * 2) < 2
+             ? 2
+             : (kSkinnySmemBytes - bn * 64 * 2) / ((2 * 64 + bn) * kBK * 2);
+}
 // Smallest K range a split piece of the skinny path gets (each piece's partial
 // sum is written, counted and read back once).
 constexpr int kSkinnyMinPieceK = 512;
@@ -72,10 +79,16 @@ cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUt
                              const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream);
 
 
+// Gated swapped skinny GEMM: C = silu(X . G^T) * (X . U^T) for M <= bn activation
+// rows X; tmG / tmU map the gate / up weights in 64-row boxes.
+cudaError_t launch_tc_skinny_swiglu(int bn, const CUtensorMap& tmG, const CUtensorMap& tmU, const CUtensorMap& tmX,
+                                    const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream);
+
 // CUDA-core skinny kernel.
 struct CcParams {
   const uint16_t* A;
   const uint16_t* B;
+  const uint16_t* B2;    // non-null: gated, C = silu(A . B^T) * (A . B2^T), B2 with B's ldb
   uint16_t* C;
   int32_t M, N, K;
   int64_t lda, ldb, ldc;
@@ -89,7 +102,7 @@ struct CcParams {
 cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream);
 
 // Dynamic shared memory of the CUDA-core kernel for M rows over grid_rows row blocks.
-int cc_smem_bytes(int64_t M, int64_t N, int grid_rows);
+int cc_smem_bytes(int64_t M, int64_t N, int grid_rows, bool gated = false);
 
 // Records a CUDA error for sg_last_cuda_error() (this host thread).
 void set_last_cuda_error(int e);

@@ -91,6 +91,40 @@ def test_deterministic():
         assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 13])
+@pytest.mark.parametrize("N,K", [(300, 1000), (4096, 11008), (1000, 4104)])
+def test_cuda_core_path(M, N, K):
+    # the decode path for M <= 2 (and, chosen explicitly, any M <= 64): each CTA
+    # streams the gate and up rows of its outputs once for all M activation rows
+    A, G, U = _inputs(M, N, K, 900 + M + N)
+    ref = oracle.swiglu(A, G, U)
+    assert_close(_run(A, G, U, M, N, K, path=sg.PATH_CUDA_CORE), ref, K, f"cuda core M={M}")
+    if M <= 2:
+        assert_close(_run(A, G, U, M, N, K), ref, K, f"auto M={M}")
+
+
+@pytest.mark.parametrize("M", [3, 9, 16, 17, 33, 64])
+@pytest.mark.parametrize("N,K", [(300, 1000), (11008, 4096), (4096, 11008), (640, 8192)])
+def test_tensor_core_path(M, N, K):
+    # the decode path for 3 <= M <= 64: two MMAs per k slice fill a gate and an up
+    # accumulator side by side in TMEM; split pieces are summed before the gate
+    A, G, U = _inputs(M, N, K, 950 + M + N)
+    ref = oracle.swiglu(A, G, U)
+    assert_close(_run(A, G, U, M, N, K, path=sg.PATH_TENSOR_CORE), ref, K, f"tensor core M={M}")
+    assert_close(_run(A, G, U, M, N, K), ref, K, f"auto M={M}")
+
+
+def test_tensor_core_path_persistent_and_deterministic():
+    # more 64-output tiles than resident CTAs: the persistent schedule
+    M, N, K = 16, 24000, 320
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sg.plan_swiglu(M, N, K, sms, sg.PATH_TENSOR_CORE)["split_k"] == 0
+    A, G, U = _inputs(M, N, K, 971)
+    got = _run(A, G, U, M, N, K, path=sg.PATH_TENSOR_CORE)
+    assert_close(got, oracle.swiglu(A, G, U), K, "persistent")
+    assert np.array_equal(got, _run(A, G, U, M, N, K, path=sg.PATH_TENSOR_CORE))
+
+
 def test_zero_k_and_errors():
     A = torch.zeros((4, 8), dtype=torch.bfloat16, device="cuda")[:, :0]   # K = 0, rows 16-byte aligned
     W = torch.zeros((16, 8), dtype=torch.bfloat16, device="cuda")[:, :0]
