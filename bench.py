@@ -507,6 +507,9 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         # decode rows first: right after seconds of power-capped GEMMs the
         # memory-bound rows measured up to 2 us slower per launch
         names = [n for n in syn.WORKLOADS if n.startswith("dec")] + ["sq2048", "mlp_up", "mlp_down", "sq8192"]
+        names += list(syn.GATED_WORKLOADS)
+    gated_names = [n for n in names if n in syn.GATED_WORKLOADS]
+    names = [n for n in names if n not in syn.GATED_WORKLOADS]
     for name in names:
         w = syn.WORKLOADS[name]
         with torch.cuda.stream(stream):
@@ -545,6 +548,34 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
                 row["frac_of_hbm"] = gbs / peaks["hbm_gbs"]
             out.append(row)
         del As, Bs, A, B, C
+        torch.cuda.empty_cache()
+    for name in gated_names:
+        g = syn.GATED_WORKLOADS[name]
+        w = g.base
+        with torch.cuda.stream(stream):
+            A = draw(w.M, w.K, w.dist_a, w.seed_a)
+            Wg = draw(w.N, w.K, w.dist_b, w.seed_b)
+            Wu = draw(w.N, w.K, w.dist_b, w.seed_b + 1000)
+            nrot = rotation_count(2 * (w.M * w.K + 2 * w.N * w.K), l2)
+            As = copies(A, nrot) if w.M > 64 else [A] * nrot
+            Gs, Us = copies(Wg, nrot), copies(Wu, nrot)
+            C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=stream.device)
+        stream.synchronize()
+        fns = [(lambda a=a, wg=wg, wu=wu: sg.gemm_bf16_swiglu(a, wg, wu, C, stream=stream))
+               for a, wg, wu in zip(As, Gs, Us)]
+        total = time_launches(torch, stream, fns, steps, 5)
+        med = total / steps
+        row = {"workload": name, "entry": "gemm_bf16_swiglu", "M": w.M, "N": w.N, "K": w.K, "us": med * 1e3}
+        if w.M > 64:
+            row["tflops"] = g.flops / (med / 1e3) / 1e12
+            rpeak, rkey = tensor_peak(peaks, total)
+            row["frac_of_peak"] = row["tflops"] / rpeak
+            row["peak"] = rkey
+        else:
+            row["gbs"] = g.decode_bytes / (med / 1e3) / 1e9
+            row["frac_of_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+        out.append(row)
+        del As, Gs, Us, A, Wg, Wu, C
         torch.cuda.empty_cache()
     return out
 
@@ -605,7 +636,7 @@ def run_rows_only(args, local):
     import synthetic as syn
 
     names = [n.strip() for n in args.rows_only.split(",") if n.strip()]
-    unknown = [n for n in names if n not in syn.WORKLOADS]
+    unknown = [n for n in names if n not in syn.WORKLOADS and n not in syn.GATED_WORKLOADS]
     if unknown or not names:
         raise SystemExit(f"unknown workloads: {unknown or args.rows_only!r}")
     import torch

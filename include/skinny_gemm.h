@@ -132,17 +132,18 @@ SG_API int gemv_bf16_path(const void *A, const void *B, void *C,
  * Kernels (SG_PATH_AUTO): M <= 2, the CUDA-core stream, each CTA reading the gate
  * and up rows of its outputs once for all M rows (paired FMAs on gate and up);
  * 3 <= M <= 64, the swapped tcgen05 kernel with a gate and an up accumulator
- * side by side in TMEM (64 outputs per tile); M > 64, the single-CTA tcgen05
- * GEMM with each B tile made of 128 rows of Wg over 128 rows of Wu (128 output
- * columns per tile).  Same errors as gemm_bf16 (a null or misaligned Wu as for
- * B).  K = 0 gives C = 0.
+ * side by side in TMEM (64 outputs per tile); M > 64, the tcgen05 GEMM with each
+ * tile's 256 B rows made of 128 rows of Wg and 128 of Wu (128 output columns per
+ * tile), on CTA pairs from M = 256 as in gemm_bf16.  Same errors as gemm_bf16 (a
+ * null or misaligned Wu as for B).  K = 0 gives C = 0.
  */
 SG_API int gemm_bf16_swiglu(const void *A, const void *Wg, const void *Wu, void *C,
                      int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldw, int64_t ldc, sg_stream_t stream);
 
-/* gemm_bf16_swiglu with the kernel named: SG_PATH_AUTO, SG_PATH_GEMM (any M), or
- * SG_PATH_CUDA_CORE / SG_PATH_TENSOR_CORE (M <= 64); others SG_ERR_INVALID_ARG. */
+/* gemm_bf16_swiglu with the kernel named: SG_PATH_AUTO, SG_PATH_GEMM or
+ * SG_PATH_GEMM_PAIR (any M), or SG_PATH_CUDA_CORE / SG_PATH_TENSOR_CORE (M <= 64);
+ * others SG_ERR_INVALID_ARG. */
 SG_API int gemm_bf16_swiglu_path(const void *A, const void *Wg, const void *Wu, void *C,
                           int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldw, int64_t ldc, int path, sg_stream_t stream);

@@ -240,21 +240,23 @@ int32_t max_sk_items(const Schedule& s) {
   return m;
 }
 
-// Gated GEMM plan (silu(A . G^T) * (A . U^T)): single-CTA tiles of 128 rows x 128
-// output columns (each computed from 128 gate and 128 up weight rows).  Stream-K
-// stays only where no CTA gets more pieces than the fixup warps take.
-void plan_tc_swiglu(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+// Gated GEMM plan (silu(A . G^T) * (A . U^T)): tiles of 128 (single CTA) or 256
+// (CTA pair) rows x 128 output columns, each computed from 128 gate and 128 up
+// weight rows.  Stream-K stays only where no CTA gets more pieces than the fixup
+// warps take.
+void plan_tc_swiglu(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
-  o->path = SG_PATH_GEMM;
-  o->tile_m = kBM;
+  o->path = pair ? SG_PATH_GEMM_PAIR : SG_PATH_GEMM;
+  o->tile_m = pair ? 2 * kBM : kBM;
   o->tile_n = kGemmBN / 2;
   o->tile_k = kBK;
-  o->stages = kGemmStages;
-  o->cluster_size = 1;
+  o->stages = pair ? kPairStages : kGemmStages;
+  o->cluster_size = pair ? 2 : 1;
   o->ctas_per_sm = 1;
-  const int32_t tm = static_cast<int32_t>(ceil_div(M, kBM)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN / 2));
+  const int32_t units = pair ? std::max(1, sms / 2) : sms;
+  const int32_t tm = static_cast<int32_t>(ceil_div(M, o->tile_m)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN / 2));
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
-  Schedule s = make_schedule(tm, tn, ks, sms, 4, std::min<int32_t>(tm, 8), false);
+  Schedule s = make_schedule(tm, tn, ks, units, 4, std::min<int32_t>(tm, pair ? 4 : 8), false);
   if (s.sk_tiles > 0 && max_sk_items(s) > kFixupMaxJobs) {
     s.dp_tiles += s.sk_tiles;
     s.sk_tiles = 0;
@@ -263,7 +265,7 @@ void plan_tc_swiglu(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
   }
   fill_sched(o, s);
   o->split_k = 0;
-  o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, sms);
+  o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, units);
 }
 
 int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
@@ -344,8 +346,11 @@ void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o, bool gat
 constexpr int64_t kCudaCoreMaxRows = 2;
 int choose_skinny_path(int64_t M) { return M <= kCudaCoreMaxRows ? SG_PATH_CUDA_CORE : SG_PATH_TENSOR_CORE; }
 
-// The gated entry's automatic kernel: the skinny kernels up to M = 64, the GEMM after.
-int swiglu_path(int64_t M) { return M <= 64 ? choose_skinny_path(M) : SG_PATH_GEMM; }
+// The gated entry's automatic kernel: the skinny kernels up to M = 64, then the
+// GEMM, on CTA pairs from M = 256 (as gemm_bf16).
+int swiglu_path(int64_t M) {
+  return M <= 64 ? choose_skinny_path(M) : (M >= 2 * kBM ? SG_PATH_GEMM_PAIR : SG_PATH_GEMM);
+}
 
 // ----------------------------------------------------------------- validation
 int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -393,18 +398,21 @@ int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, 
 }
 
 int run_tc_swiglu(DeviceState& d, int dev, const void* A, const void* Wg, const void* Wu, void* C, int64_t M,
-                  int64_t N, int64_t K, int64_t lda, int64_t ldw, int64_t ldc, cudaStream_t stream) {
+                  int64_t N, int64_t K, int64_t lda, int64_t ldw, int64_t ldc, bool pair, cudaStream_t stream) {
   sg_plan_info plan;
-  plan_tc_swiglu(M, N, K, d.sm_count, &plan);
+  plan_tc_swiglu(M, N, K, d.sm_count, pair, &plan);
+  // each CTA loads 128 (single) or 64 (pair) rows of each of Wg and Wu per tile
+  const uint32_t w_rows = pair ? kGemmBN / 4 : kGemmBN / 2;
   CUtensorMap ta, tg, tu, tc;
   int st = make_map(&ta, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
-  if (st == SG_OK) st = make_map(&tg, Wg, N, K, ldw, kGemmBN / 2, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
-  if (st == SG_OK) st = make_map(&tu, Wu, N, K, ldw, kGemmBN / 2, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tg, Wg, N, K, ldw, w_rows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tu, Wu, N, K, ldw, w_rows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, dev);
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
-  cudaError_t e = launch_tc_gemm_swiglu(ta, tg, tu, tc, p, stream);
+  cudaError_t e = pair ? launch_tc_gemm_swiglu_pair(ta, tg, tu, tc, p, stream)
+                       : launch_tc_gemm_swiglu(ta, tg, tu, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
@@ -540,8 +548,7 @@ int gemv_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
 
 int gemm_bf16_swiglu_path(const void* A, const void* Wg, const void* Wu, void* C, int64_t M, int64_t N, int64_t K,
                           int64_t lda, int64_t ldw, int64_t ldc, int path, sg_stream_t stream) {
-  if (path != SG_PATH_AUTO && path != SG_PATH_GEMM && path != SG_PATH_CUDA_CORE && path != SG_PATH_TENSOR_CORE)
-    return SG_ERR_INVALID_ARG;
+  if (path < SG_PATH_AUTO || path > SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
   if ((path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE) && M > 64) return SG_ERR_INVALID_ARG;
   int st = validate(A, Wg, C, M, N, K, lda, ldw, ldc);
   if (st == SG_OK && M > 0 && N > 0 && K > 0) {
@@ -563,7 +570,7 @@ int gemm_bf16_swiglu_path(const void* A, const void* Wg, const void* Wu, void* C
   if (path == SG_PATH_AUTO) path = swiglu_path(M);
   if (path == SG_PATH_CUDA_CORE) return run_cc(*d, A, Wg, C, M, N, K, lda, ldw, ldc, s, Wu);
   if (path == SG_PATH_TENSOR_CORE) return run_tc_skinny_swiglu(*d, dev, A, Wg, Wu, C, M, N, K, lda, ldw, ldc, s);
-  return run_tc_swiglu(*d, dev, A, Wg, Wu, C, M, N, K, lda, ldw, ldc, s);
+  return run_tc_swiglu(*d, dev, A, Wg, Wu, C, M, N, K, lda, ldw, ldc, path == SG_PATH_GEMM_PAIR, s);
 }
 
 int gemm_bf16_swiglu(const void* A, const void* Wg, const void* Wu, void* C, int64_t M, int64_t N, int64_t K,
@@ -573,8 +580,7 @@ int gemm_bf16_swiglu(const void* A, const void* Wg, const void* Wu, void* C, int
 
 int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info* out) {
   if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
-  if (entry != SG_PATH_AUTO && entry != SG_PATH_GEMM && entry != SG_PATH_CUDA_CORE && entry != SG_PATH_TENSOR_CORE)
-    return SG_ERR_INVALID_ARG;
+  if (entry < SG_PATH_AUTO || entry > SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
   if ((entry == SG_PATH_CUDA_CORE || entry == SG_PATH_TENSOR_CORE) && M > 64) return SG_ERR_INVALID_ARG;
   const int path = entry == SG_PATH_AUTO ? swiglu_path(M) : entry;
   if (path == SG_PATH_CUDA_CORE)
@@ -582,7 +588,7 @@ int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t ent
   else if (path == SG_PATH_TENSOR_CORE)
     plan_tc_skinny(M, N, K, num_sms, out, true);
   else
-    plan_tc_swiglu(M, N, K, num_sms, out);
+    plan_tc_swiglu(M, N, K, num_sms, path == SG_PATH_GEMM_PAIR, out);
   return SG_OK;
 }
 

@@ -162,9 +162,14 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
                    const TcParams p) {
   using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   constexpr bool SWAP = L::SWAP;
-  static_assert(!GATED || !PAIR, "the gated variants are single-CTA kernels");
-  // output columns per tile; in a gated accumulator the up columns start here
+  // output columns per tile
   constexpr int kOutCols = (GATED && !SWAP) ? BN / 2 : BN;
+  // Gated accumulators alternate blocks of kHalf gate columns and kHalf up
+  // columns: one block each on the swapped path and in a single-CTA tile, and
+  // per CTA of a pair (each CTA's B rows are 64 gate over 64 up rows).
+  constexpr int kHalf = SWAP ? BN : (PAIR ? 64 : 128);
+  // accumulator column of the gate value of output column c (up: + kHalf)
+  auto gate_col = [](int c) { return (c / kHalf) * 2 * kHalf + c % kHalf; };
   constexpr int kTileRows = PAIR ? 2 * kBM : L::kARows;  // output rows per tile (the MMA's M)
   constexpr uint32_t kIdesc = idesc_bf16_f32(kTileRows, BN);
   const int kboxes = (p.K + kBK - 1) / kBK;  // 64-wide k boxes that hold data
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         int32_t tm, tn;
         tile_coords(sched, w.tile, tm, tn);
         const int arow = tm * kTileRows + static_cast<int>(rank) * L::kARows;
-        const int brow = tn * kOutCols + static_cast<int>(rank) * L::kBRowsPerCta;
+        const int brow = tn * kOutCols + static_cast<int>(rank) * (GATED ? L::kBRowsPerCta / 2 : L::kBRowsPerCta);
         for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -262,8 +267,10 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
             if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * bytes + extra);
             for (int j = 0; j < nsub; ++j) {
               const int kx = (ks * KSUB + j) * kBK;
+              uint8_t* bdst = smem + L::kBOff + s * L::kBBytes + j * L::kBSub;
               tma_load_2d_pair(smem + L::kAOff + s * L::kABytes + j * L::kASub, &tmA, kx, arow, full_leader);
-              tma_load_2d_pair(smem + L::kBOff + s * L::kBBytes + j * L::kBSub, &tmB, kx, brow, full_leader);
+              tma_load_2d_pair(bdst, &tmB, kx, brow, full_leader);
+              if constexpr (GATED) tma_load_2d_pair(bdst + L::kBSub / 2, &tmW2, kx, brow, full_leader);
             }
           } else {
             mbar_arrive_expect_tx(&full[s], bytes + extra);
@@ -474,8 +481,9 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
 #pragma unroll 1
         for (int jo = 0; jo < kOutCols / L::kChunk; ++jo) {
           uint32_t rg[L::kChunk], ru[L::kChunk];
-          issue_chunk(tacc + jo * L::kChunk, rg);
-          issue_chunk(tacc + kOutCols + jo * L::kChunk, ru);
+          const int gcol = gate_col(jo * L::kChunk);
+          issue_chunk(tacc + gcol, rg);
+          issue_chunk(tacc + gcol + kHalf, ru);
           tmem_ld_wait(rg);
           tmem_ld_wait(ru);
 #pragma unroll
@@ -551,10 +559,10 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
 #pragma unroll 1
           for (int jo = 0; jo < kOutCols / L::kChunk; ++jo) {
             float acc[L::kChunk];
-            sum_chunk(jo, acc);
+            sum_chunk(GATED ? gate_col(jo * L::kChunk) / L::kChunk : jo, acc);
             if constexpr (GATED) {
               float up[L::kChunk];
-              sum_chunk(jo + kOutCols / L::kChunk, up);
+              sum_chunk((gate_col(jo * L::kChunk) + kHalf) / L::kChunk, up);
 #pragma unroll
               for (int e = 0; e < L::kChunk; ++e) acc[e] = silu_mul(acc[e], up[e]);
             }
@@ -719,10 +727,10 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         for (int g = 0; g < 2; ++g) {
           const int frow = fw * 64 + g * 32 + lane;
           float acc[32];
-          sum_chunk(j, frow, acc);
+          sum_chunk(GATED ? gate_col(j * 32) / 32 : j, frow, acc);
           if constexpr (GATED) {
             float up[32];
-            sum_chunk(j + kOutCols / 32, frow, up);
+            sum_chunk((gate_col(j * 32) + kHalf) / 32, frow, up);
 #pragma unroll
             for (int e = 0; e < 32; ++e) acc[e] = silu_mul(acc[e], up[e]);
           }
@@ -786,6 +794,11 @@ cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_tc_gemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmG, const CUtensorMap& tmU,
                                   const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
   return launch_variant<kGemmBN, kGemmStages, 0, 1, false, true>(tmA, tmG, tmC, p, stream, &tmU);
+}
+
+cudaError_t launch_tc_gemm_swiglu_pair(const CUtensorMap& tmA, const CUtensorMap& tmG, const CUtensorMap& tmU,
+                                       const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
+  return launch_variant<kGemmBN, kPairStages, 0, 1, true, true>(tmA, tmG, tmC, p, stream, &tmU);
 }
 
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,

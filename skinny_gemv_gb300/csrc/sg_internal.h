@@ -68,6 +68,11 @@ cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_tc_gemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmG, const CUtensorMap& tmU,
                                   const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream);
 
+// Gated paired GEMM: 256 x 128-output tiles on clusters of two CTAs; each CTA's
+// B rows are 64 of G over 64 of U (boxes 64 x 64 each).
+cudaError_t launch_tc_gemm_swiglu_pair(const CUtensorMap& tmA, const CUtensorMap& tmG, const CUtensorMap& tmU,
+                                       const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream);
+
 // Paired GEMM over clusters of two CTAs: 256 x 256 tiles, p.sched counts pairs.
 cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                 const TcParams& p, cudaStream_t stream);

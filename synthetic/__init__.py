@@ -184,6 +184,33 @@ WORKLOADS = {w.name: w for w in [
 ]}
 
 
+@dataclasses.dataclass(frozen=True)
+class GatedWorkload:
+    """One synthetic gated projection C = silu(A . Wg^T) * (A . Wu^T): the Llama
+    MLP's gate and up weights [N, K] share a shape and a distribution."""
+    base: Workload   # A and the gate weights Wg (its B)
+
+    @property
+    def name(self) -> str:
+        return "swiglu_" + self.base.name
+
+    def up(self) -> np.ndarray:
+        return matrix(self.base.N, self.base.K, self.base.dist_b, self.base.seed_b + 1000)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.base.flops
+
+    @property
+    def decode_bytes(self) -> int:
+        b = self.base
+        return 2 * (2 * b.N * b.K + b.M * b.K + b.M * b.N)
+
+
+GATED_WORKLOADS = {g.name: g for g in [GatedWorkload(WORKLOADS[n]) for n in
+                                       ("mlp_up", "dec1_up", "dec2_up", "dec16_up", "dec64_up")]}
+
+
 def sample_indices(extent: int, count: int, seed: int) -> np.ndarray:
     """A sorted, seeded choice of ``count`` distinct indices in [0, extent)."""
     if count >= extent:

@@ -248,10 +248,12 @@ def test_plan_rejects_bad_arguments(lib):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 11008, 4096), (2048, 4096, 4096), (128, 128, 64), (1000, 3000, 200),
                                    (16, 11008, 4096), (130, 257, 128)])
-def test_swiglu_plan_covers_every_unit_once(lib, M, N, K):
-    info = sg.plan_swiglu(M, N, K, 152, sg.PATH_GEMM)
-    assert info["path"] == sg.PATH_GEMM and info["tile_m"] == 128 and info["tile_n"] == 128
-    assert info["tiles_m"] == -(-M // 128) and info["tiles_n"] == -(-N // 128)
+@pytest.mark.parametrize("path", [sg.PATH_GEMM, sg.PATH_GEMM_PAIR])
+def test_swiglu_plan_covers_every_unit_once(lib, M, N, K, path):
+    info = sg.plan_swiglu(M, N, K, 152, path)
+    tm = 256 if path == sg.PATH_GEMM_PAIR else 128
+    assert info["path"] == path and info["tile_m"] == tm and info["tile_n"] == 128
+    assert info["tiles_m"] == -(-M // tm) and info["tiles_n"] == -(-N // 128)
     items = _check_plan_coverage(info)
     # no CTA gets more Stream-K pieces than the fixup warps take
     assert max(sum(1 for it in row if it[4] > 1) for row in items) <= 4
@@ -265,6 +267,7 @@ def test_swiglu_path_choice(lib):
     assert info["grid"] == 172 and info["split_k"] == 1
     assert sg.plan_swiglu(64, 4096, 11008, 152)["split_k"] == 4
     assert sg.plan_swiglu(65, 4096, 4096, 152)["path"] == sg.PATH_GEMM
+    assert sg.plan_swiglu(256, 4096, 4096, 152)["path"] == sg.PATH_GEMM_PAIR
     out = sg.PlanInfo()
     assert lib.sg_plan_swiglu(65, 8, 8, 152, sg.PATH_TENSOR_CORE, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
-    assert lib.sg_plan_swiglu(8, 8, 8, 152, sg.PATH_GEMM_PAIR, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
+    assert lib.sg_plan_swiglu(8, 8, 8, 152, 7, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG

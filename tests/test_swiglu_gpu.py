@@ -39,29 +39,35 @@ def _inputs(M, N, K, seed, ld=None):
     return A, G, U
 
 
+GEMM_PATHS = [sg.PATH_GEMM, sg.PATH_GEMM_PAIR]
+
+
+@pytest.mark.parametrize("path", GEMM_PATHS)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (128, 256, 512), (200, 300, 192), (130, 257, 128),
-                                   (65, 1000, 1024), (1000, 96, 4104)])
-def test_full_oracle(M, N, K):
+                                   (65, 1000, 1024), (1000, 96, 4104), (520, 640, 256)])
+def test_full_oracle(M, N, K, path):
     A, G, U = _inputs(M, N, K, 700 + M + N)
-    assert_close(_run(A, G, U, M, N, K), oracle.swiglu(A, G, U), K, f"swiglu {M}x{N}x{K}")
+    assert_close(_run(A, G, U, M, N, K, path=path), oracle.swiglu(A, G, U), K, f"swiglu {M}x{N}x{K} path {path}")
 
 
-def test_padded_leading_dimensions():
-    M, N, K = 150, 140, 200
+@pytest.mark.parametrize("path", GEMM_PATHS)
+def test_padded_leading_dimensions(path):
+    M, N, K = 300, 140, 200
     A, G, U = _inputs(M, N, K, 801, ld=216)
-    assert_close(_run(A, G, U, M, N, K), oracle.swiglu(A, G, U, K=K), K, "padded")
+    assert_close(_run(A, G, U, M, N, K, path=path), oracle.swiglu(A, G, U, K=K), K, "padded")
 
 
-def test_stream_k_tiles_are_gated_after_the_sum():
-    # 2048 x 4096 x 4096: 512 tiles of 128 x 128 over the SMs leave a Stream-K
-    # remainder; each split tile's gate and up sums are combined by the fixup
-    # warps before the SiLU.
+@pytest.mark.parametrize("path", GEMM_PATHS)
+def test_stream_k_tiles_are_gated_after_the_sum(path):
+    # 2048 x 4096 x 4096: 512 tiles of 128 x 128 (256 of 256 x 128 on pairs) over
+    # the SMs leave a Stream-K remainder; each split tile's gate and up sums are
+    # combined by the fixup warps before the SiLU.
     M, N, K = 2048, 4096, 4096
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    info = sg.plan_swiglu(M, N, K, sms)
+    info = sg.plan_swiglu(M, N, K, sms, path)
     assert info["sk_tiles"] > 0
     A, G, U = _inputs(M, N, K, 811)
-    got = _run(A, G, U, M, N, K)
+    got = _run(A, G, U, M, N, K, path=path)
     rows = syn.sample_indices(M, 256, 3)
     ref = oracle.silu(oracle.gemm(A[rows], G)) * oracle.gemm(A[rows], U)
     assert_close(got[rows], ref, K, "stream-k")
@@ -141,3 +147,11 @@ def test_zero_k_and_errors():
     st = lib.gemm_bf16_swiglu(A.data_ptr(), W.data_ptr(), W.data_ptr() + 2, torch.empty_like(A).data_ptr(),
                               64, 64, 64, 64, 64, 64, None)
     assert st == sg.SG_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("g", [g for g in syn.GATED_WORKLOADS.values() if g.base.M <= 64], ids=lambda g: g.name)
+def test_decode_gated_workloads(g):
+    # the bench's gated decode rows: M = 1, 2, 16, 64 against 11008 x 4096 gate and up weights
+    w = g.base
+    A, G, U = w.a(), w.b(), g.up()
+    assert_close(_run(A, G, U, w.M, w.N, w.K), oracle.swiglu(A, G, U), w.K, g.name)
