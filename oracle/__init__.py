@@ -12,6 +12,7 @@ gemm(A, B)                    full fp64 reference, shape (M, N)
 gemm_sampled(A, B, rows, cols) the same sum at the intersections rows x cols
 silu(x)                        x * sigmoid(x) = x / (1 + exp(-x)), fp64
 swiglu(A, Wg, Wu)              silu(A . Wg^T) * (A . Wu^T), fp64 (gated MLP)
+gemm_residual(A, B, R)         A . B^T + R, fp64 (a projection with its residual add)
 build()                        compile the C oracle (idempotent)
 
 A and B are uint16 arrays of bf16 bit patterns, A[M, lda] and B[N, ldb]; the
@@ -118,3 +119,18 @@ def swiglu(A: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, K: int | None = None,
     g = gemm(A, Wg, K=K, threads=threads)
     u = gemm(A, Wu, K=K, threads=threads)
     return silu(g) * u
+
+
+def _bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact fp64 values of bf16 bit patterns: the pattern is the high half of the
+    fp32 with the same value."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def gemm_residual(A: np.ndarray, B: np.ndarray, R: np.ndarray, K: int | None = None,
+                  threads: int | None = None) -> np.ndarray:
+    """A projection with its residual added: gemm(A, B) + R in fp64, R an [M, N]
+    (or wider-pitched [M, ldr]) array of bf16 bit patterns (first N columns)."""
+    C = gemm(A, B, K=K, threads=threads)
+    return C + _bf16_to_f64(R)[:, :C.shape[1]]
