@@ -507,9 +507,10 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         # decode rows first: right after seconds of power-capped GEMMs the
         # memory-bound rows measured up to 2 us slower per launch
         names = [n for n in syn.WORKLOADS if n.startswith("dec")] + ["sq2048", "mlp_up", "mlp_down", "sq8192"]
-        names += list(syn.GATED_WORKLOADS)
+        names += list(syn.GATED_WORKLOADS) + list(syn.RESIDUAL_WORKLOADS)
     gated_names = [n for n in names if n in syn.GATED_WORKLOADS]
-    names = [n for n in names if n not in syn.GATED_WORKLOADS]
+    resid_names = [n for n in names if n in syn.RESIDUAL_WORKLOADS]
+    names = [n for n in names if n not in syn.GATED_WORKLOADS and n not in syn.RESIDUAL_WORKLOADS]
     for name in names:
         w = syn.WORKLOADS[name]
         with torch.cuda.stream(stream):
@@ -577,6 +578,33 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         out.append(row)
         del As, Gs, Us, A, Wg, Wu, C
         torch.cuda.empty_cache()
+    for name in resid_names:
+        rw = syn.RESIDUAL_WORKLOADS[name]
+        w = rw.base
+        with torch.cuda.stream(stream):
+            A = draw(w.M, w.K, w.dist_a, w.seed_a)
+            B = draw(w.N, w.K, w.dist_b, w.seed_b)
+            R = draw(w.M, w.N, "normal:1", w.seed_a + 2000)
+            nrot = rotation_count(2 * (w.M * w.K + w.N * w.K + 2 * w.M * w.N), l2)
+            As = copies(A, nrot) if w.M > 64 else [A] * nrot
+            Bs, Rs = copies(B, nrot), copies(R, nrot)
+            C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=stream.device)
+        stream.synchronize()
+        fns = [(lambda a=a, b=b, r=r: sg.gemm_bf16_residual(a, b, r, C, stream=stream)) for a, b, r in zip(As, Bs, Rs)]
+        total = time_launches(torch, stream, fns, steps, 5)
+        med = total / steps
+        row = {"workload": name, "entry": "gemm_bf16_residual", "M": w.M, "N": w.N, "K": w.K, "us": med * 1e3}
+        if w.M > 64:
+            row["tflops"] = rw.flops / (med / 1e3) / 1e12
+            rpeak, rkey = tensor_peak(peaks, total)
+            row["frac_of_peak"] = row["tflops"] / rpeak
+            row["peak"] = rkey
+        else:
+            row["gbs"] = rw.decode_bytes / (med / 1e3) / 1e9
+            row["frac_of_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+        out.append(row)
+        del As, Bs, Rs, A, B, R, C
+        torch.cuda.empty_cache()
     return out
 
 
@@ -636,7 +664,8 @@ def run_rows_only(args, local):
     import synthetic as syn
 
     names = [n.strip() for n in args.rows_only.split(",") if n.strip()]
-    unknown = [n for n in names if n not in syn.WORKLOADS and n not in syn.GATED_WORKLOADS]
+    unknown = [n for n in names if n not in syn.WORKLOADS and n not in syn.GATED_WORKLOADS
+               and n not in syn.RESIDUAL_WORKLOADS]
     if unknown or not names:
         raise SystemExit(f"unknown workloads: {unknown or args.rows_only!r}")
     import torch

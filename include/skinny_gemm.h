@@ -149,6 +149,29 @@ SG_API int gemm_bf16_swiglu_path(const void *A, const void *Wg, const void *Wu, 
                           int64_t lda, int64_t ldw, int64_t ldc, int path, sg_stream_t stream);
 
 /*
+ * gemm_bf16_residual -- a projection with its residual added in the epilogue:
+ *
+ *     C[m, n] = sum_k A[m, k] B[n, k] + R[m, n],
+ *
+ * the down projection of the MLP block with the residual stream added (the pages'
+ * second fused MLP epilogue).  R is M x N bf16 with leading dimension ldr (>= N, a
+ * multiple of 8, 16-byte aligned); R may be C itself (in place, then ldr == ldc);
+ * any other overlap of R, C, A or B is undefined.  The sum is fp32 (the
+ * accumulator plus R's value) and is rounded to bf16 once.  The kernels are
+ * gemm_bf16's (the same automatic choice); K = 0 gives C = R.  Errors as
+ * gemm_bf16, plus SG_ERR_INVALID_ARG for a null R, ldr < N or ldr != ldc in place,
+ * and SG_ERR_MISALIGNED for a misaligned R or ldr.
+ */
+SG_API int gemm_bf16_residual(const void *A, const void *B, const void *R, void *C,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldr, int64_t ldc, sg_stream_t stream);
+
+/* gemm_bf16_residual with the kernel named (paths as gemm_bf16_path). */
+SG_API int gemm_bf16_residual_path(const void *A, const void *B, const void *R, void *C,
+                            int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldr, int64_t ldc, int path, sg_stream_t stream);
+
+/*
  * gemv_bf16_noalloc -- gemv_bf16 on the CUDA-core kernel (SG_PATH_CUDA_CORE),
  * for callers that cannot allocate device memory.  The pages have no
  * counterpart: this entry point exists for integration, not for the method.

@@ -98,6 +98,10 @@ def load(build_if_missing: bool = False):
     lib.gemm_bf16_swiglu.restype = ctypes.c_int
     lib.gemm_bf16_swiglu_path.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
     lib.gemm_bf16_swiglu_path.restype = ctypes.c_int
+    lib.gemm_bf16_residual.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i64, p]
+    lib.gemm_bf16_residual.restype = ctypes.c_int
+    lib.gemm_bf16_residual_path.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
+    lib.gemm_bf16_residual_path.restype = ctypes.c_int
     lib.sg_status_string.argtypes = [ctypes.c_int]
     lib.sg_status_string.restype = ctypes.c_char_p
     lib.sg_last_cuda_error.argtypes = []
@@ -232,6 +236,30 @@ def gemm_bf16_swiglu(A, Wg, Wu, C=None, stream=None, path: int = PATH_AUTO):
         st = load().gemm_bf16_swiglu_path(a_ptr, g_ptr, u_ptr, c_ptr, M, N, K, lda, ldg, ldc, path,
                                           _stream_handle(stream))
     _check(st, "gemm_bf16_swiglu")
+    return C
+
+
+def gemm_bf16_residual(A, B, R, C=None, stream=None, path: int = PATH_AUTO):
+    """C[M, N] = A @ B^T + R with the sum in fp32 and one bf16 rounding; R may be C
+    (in place)."""
+    torch = _torch()
+    a_ptr, lda = _operand(A, "A")
+    b_ptr, ldb = _operand(B, "B")
+    r_ptr, ldr = _operand(R, "R")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(R.shape) != (M, N):
+        raise ValueError(f"shapes: A {tuple(A.shape)}, B {tuple(B.shape)}, R {tuple(R.shape)}")
+    if C is None:
+        ld = -(-N // 8) * 8
+        C = torch.empty((M, ld), dtype=torch.bfloat16, device=A.device)[:, :N]
+    c_ptr, ldc = _operand(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    with torch.cuda.device(A.device):
+        st = load().gemm_bf16_residual_path(a_ptr, b_ptr, r_ptr, c_ptr, M, N, K, lda, ldb, ldr, ldc, path,
+                                            _stream_handle(stream))
+    _check(st, "gemm_bf16_residual")
     return C
 
 

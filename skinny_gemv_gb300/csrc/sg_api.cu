@@ -381,7 +381,8 @@ TcParams base_params(DeviceState& d, int64_t M, int64_t N, int64_t K, int64_t ld
 }
 
 int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                int64_t lda, int64_t ldb, int64_t ldc, bool pair, cudaStream_t stream) {
+                int64_t lda, int64_t ldb, int64_t ldc, bool pair, cudaStream_t stream, const void* R = nullptr,
+                int64_t ldr = 0) {
   sg_plan_info plan;
   plan_tc_gemm(M, N, K, d.sm_count, pair, &plan);
   CUtensorMap ta, tb, tc;
@@ -393,6 +394,8 @@ int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, 
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
   p.inject_extra_tx = g_inject_missing_tx.exchange(0);
+  p.R = static_cast<const uint16_t*>(R);
+  p.ldr = ldr;
   cudaError_t e = pair ? launch_tc_gemm_pair(ta, tb, tc, p, stream) : launch_tc_gemm(ta, tb, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
@@ -433,7 +436,8 @@ int run_tc_skinny_swiglu(DeviceState& d, int dev, const void* A, const void* Wg,
 }
 
 int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                  int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
+                  int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream, const void* R = nullptr,
+                  int64_t ldr = 0) {
   sg_plan_info plan;
   plan_tc_skinny(M, N, K, d.sm_count, &plan);
   CUtensorMap tw, tx, tc;
@@ -443,12 +447,15 @@ int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
+  p.R = static_cast<const uint16_t*>(R);
+  p.ldr = ldr;
   cudaError_t e = launch_tc_skinny(plan.tile_n, plan.tile_m, tw, tx, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
 int run_cc(DeviceState& d, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-           int64_t ldb, int64_t ldc, cudaStream_t stream, const void* B2 = nullptr) {
+           int64_t ldb, int64_t ldc, cudaStream_t stream, const void* B2 = nullptr, const void* R = nullptr,
+           int64_t ldr = 0) {
   // At most 8 activation rows per launch; larger M runs as consecutive row blocks.
   for (int64_t m0 = 0; m0 < M; m0 += 8) {
     const int64_t mb = std::min<int64_t>(8, M - m0);
@@ -470,27 +477,54 @@ int run_cc(DeviceState& d, const void* A, const void* B, void* C, int64_t M, int
     p.k_slice = plan.k_steps;
     p.partials = d.partials;
     p.counters = d.counters;
+    p.R = R ? static_cast<const uint16_t*>(R) + m0 * ldr : nullptr;
+    p.ldr = ldr;
     cudaError_t e = launch_cc_gemv(p, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return SG_OK;
 }
 
+// C := 0 (no residual) or C := R, the value of an empty sum plus the residual.
+int empty_sum(void* C, int64_t M, int64_t N, int64_t ldc, const void* R, int64_t ldr, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (R == nullptr)
+    e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, stream);
+  else if (R != C)
+    e = cudaMemcpy2DAsync(C, ldc * 2, R, ldr * 2, N * 2, M, cudaMemcpyDeviceToDevice, stream);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
 int skinny_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                    int64_t ldb, int64_t ldc, int path, cudaStream_t stream) {
+                    int64_t ldb, int64_t ldc, int path, cudaStream_t stream, const void* R = nullptr,
+                    int64_t ldr = 0) {
   DeviceState* d = nullptr;
   int dev = 0;
   int st = current_device_state(&d, &dev);
   if (st != SG_OK) return st;
-  if (K == 0) {
-    cudaError_t e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, stream);
-    return e == cudaSuccess ? SG_OK : cuda_fail(e);
-  }
+  if (K == 0) return empty_sum(C, M, N, ldc, R, ldr, stream);
   st = ensure_workspace(*d, stream);
   if (st != SG_OK) return st;
   if (path == SG_PATH_AUTO) path = choose_skinny_path(M);
-  if (path == SG_PATH_CUDA_CORE) return run_cc(*d, A, B, C, M, N, K, lda, ldb, ldc, stream);
-  return run_tc_skinny(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, stream);
+  if (path == SG_PATH_CUDA_CORE) return run_cc(*d, A, B, C, M, N, K, lda, ldb, ldc, stream, nullptr, R, ldr);
+  return run_tc_skinny(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, stream, R, ldr);
+}
+
+// gemm_bf16_path and gemm_bf16_residual_path after their argument checks.
+int gemm_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                  int64_t ldc, int path, cudaStream_t s, const void* R, int64_t ldr) {
+  if (path == SG_PATH_AUTO && M <= 64) return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, s, R, ldr);
+  if (path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE)
+    return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, path, s, R, ldr);
+  DeviceState* d = nullptr;
+  int dev = 0;
+  int st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  if (K == 0) return empty_sum(C, M, N, ldc, R, ldr, s);
+  st = ensure_workspace(*d, s);
+  if (st != SG_OK) return st;
+  const bool pair = path == SG_PATH_GEMM_PAIR || (path == SG_PATH_AUTO && auto_pair(M));
+  return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, pair, s, R, ldr);
 }
 
 }  // namespace
@@ -509,22 +543,24 @@ int gemm_bf16_path(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   if ((path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE) && M > 64) return SG_ERR_INVALID_ARG;
   int st = validate(A, B, C, M, N, K, lda, ldb, ldc);
   if (st != SG_OK || M == 0 || N == 0) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (path == SG_PATH_AUTO && M <= 64) return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, SG_PATH_AUTO, s);
-  if (path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE)
-    return skinny_dispatch(A, B, C, M, N, K, lda, ldb, ldc, path, s);
-  DeviceState* d = nullptr;
-  int dev = 0;
-  st = current_device_state(&d, &dev);
-  if (st != SG_OK) return st;
-  if (K == 0) {
-    cudaError_t e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, s);
-    return e == cudaSuccess ? SG_OK : cuda_fail(e);
-  }
-  st = ensure_workspace(*d, s);
-  if (st != SG_OK) return st;
-  const bool pair = path == SG_PATH_GEMM_PAIR || (path == SG_PATH_AUTO && auto_pair(M));
-  return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, pair, s);
+  return gemm_dispatch(A, B, C, M, N, K, lda, ldb, ldc, path, reinterpret_cast<cudaStream_t>(stream), nullptr, 0);
+}
+
+int gemm_bf16_residual_path(const void* A, const void* B, const void* R, void* C, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldr, int64_t ldc, int path, sg_stream_t stream) {
+  if (path < SG_PATH_AUTO || path > SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
+  if ((path == SG_PATH_CUDA_CORE || path == SG_PATH_TENSOR_CORE) && M > 64) return SG_ERR_INVALID_ARG;
+  int st = validate(A, B, C, M, N, K, lda, ldb, ldc);
+  if (st != SG_OK || M == 0 || N == 0) return st;
+  if (!R || ldr < N) return SG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(R) & 15u) || (ldr & 7)) return SG_ERR_MISALIGNED;
+  if (R == C && ldr != ldc) return SG_ERR_INVALID_ARG;  // in place only with the same layout
+  return gemm_dispatch(A, B, C, M, N, K, lda, ldb, ldc, path, reinterpret_cast<cudaStream_t>(stream), R, ldr);
+}
+
+int gemm_bf16_residual(const void* A, const void* B, const void* R, void* C, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldr, int64_t ldc, sg_stream_t stream) {
+  return gemm_bf16_residual_path(A, B, R, C, M, N, K, lda, ldb, ldr, ldc, SG_PATH_AUTO, stream);
 }
 
 int gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,

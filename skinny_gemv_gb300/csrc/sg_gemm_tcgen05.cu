@@ -124,6 +124,32 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Adds the residual R[row, col0 .. col0 + 31] to this thread's 32 values (only
+// elements with row < M and column < N are read; 16-byte vectors where all eight
+// are inside, single elements at the row's ragged end).  R may be C itself: each
+// element is read before the same thread's store writes it.
+__device__ __forceinline__ void add_residual_32(float* v, const uint16_t* R, int64_t ldr, int row, int col0, int M,
+                                                int N) {
+  if (row >= M) return;
+  const uint16_t* src = R + static_cast<int64_t>(row) * ldr + col0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (col0 + 8 * c + 8 <= N) {
+      const uint4 x = *reinterpret_cast<const uint4*>(src + 8 * c);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * c + 2 * i] += __uint_as_float(w[i] << 16);
+        v[8 * c + 2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (col0 + 8 * c + e < N) v[8 * c + e] += __uint_as_float(static_cast<uint32_t>(src[8 * c + e]) << 16);
+    }
+  }
+}
+
 // One warp writes 32 rows x 32 fp32 columns (lane = row) to C as bf16 (round to
 // nearest even): 64-byte-swizzled staging in one of two 2 KB buffers, then a TMA
 // store clipped at M and N.
@@ -391,19 +417,27 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
     constexpr int kEpiThreads = 32 * L::kEpiWarps;
 
     // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
-    auto emit_chunk = [&](const float* v, int tm, int tn, int j) {
+    auto emit_chunk = [&](float* v, int tm, int tn, int j) {
       if constexpr (!SWAP) {
-        store_rows_32x32(&tmC, v, tn * kOutCols + j * 32, tm * kTileRows + static_cast<int>(rank) * kBM + q * 32, staging,
-                         store_count, lane, p.M, p.N);
+        const int col0 = tn * kOutCols + j * 32;
+        const int row0 = tm * kTileRows + static_cast<int>(rank) * kBM + q * 32;
+        if (!GATED && p.R != nullptr) add_residual_32(v, p.R, p.ldr, row0 + lane, col0, p.M, p.N);
+        store_rows_32x32(&tmC, v, col0, row0, staging, store_count, lane, p.M, p.N);
       } else {
         // D[n][m]: this thread's row is weight row n, its columns activation rows
         // m; the staging tile is C's layout (row m, 64 consecutive n), so a warp's
         // 16 rows land in 32 contiguous bytes per m.
         if (holds_row) {
           __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(smem + L::kStagingOff);
+          const int n = tm * L::kARows + slot_row;  // output column (weight row)
 #pragma unroll
-          for (int e = 0; e < L::kChunk; ++e)
-            st[(j * L::kChunk + e) * L::kARows + slot_row] = __float2bfloat16_rn(v[e]);
+          for (int e = 0; e < L::kChunk; ++e) {
+            float x = v[e];
+            const int m = tn * BN + j * L::kChunk + e;  // output row (activation row)
+            if (!GATED && p.R != nullptr && m < p.M && n < p.N)
+              x += __uint_as_float(static_cast<uint32_t>(p.R[static_cast<int64_t>(m) * p.ldr + n]) << 16);
+            st[(j * L::kChunk + e) * L::kARows + slot_row] = __float2bfloat16_rn(x);
+          }
         }
       }
     };
@@ -734,9 +768,9 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
 #pragma unroll
             for (int e = 0; e < 32; ++e) acc[e] = silu_mul(acc[e], up[e]);
           }
-          store_rows_32x32(&tmC, acc, tn * kOutCols + j * 32,
-                           tm * kTileRows + static_cast<int>(rank) * kBM + fw * 64 + g * 32, fstaging,
-                           fstore_count, lane, p.M, p.N);
+          const int frow0 = tm * kTileRows + static_cast<int>(rank) * kBM + fw * 64 + g * 32;
+          if (!GATED && p.R != nullptr) add_residual_32(acc, p.R, p.ldr, frow0 + lane, tn * kOutCols + j * 32, p.M, p.N);
+          store_rows_32x32(&tmC, acc, tn * kOutCols + j * 32, frow0, fstaging, fstore_count, lane, p.M, p.N);
         }
       }
       if (fw == 0 && lane == 0) atomicExch(&p.counters[PAIR ? 2 * w.sk_index + static_cast<int>(rank) : w.sk_index], 0u);

@@ -51,6 +51,11 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
+// The residual R[m, n] as fp32 (0 without one); R may be C itself.
+__device__ __forceinline__ float residual(const CcParams& p, int64_t m, int64_t n) {
+  return p.R != nullptr ? __uint_as_float(static_cast<uint32_t>(p.R[m * p.ldr + n]) << 16) : 0.f;
+}
+
 // silu(g) * u = g / (1 + e^-g) * u in fp32 (a signed zero where e^-g is inf).
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
@@ -219,7 +224,9 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
       for (int w = 1; w < kCcWarps; ++w) s[gu] += src[w];
     }
     if (p.split_k == 1) {
-      C[static_cast<int64_t>(m) * p.ldc + row_lo + r] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0]);
+      const int64_t n = row_lo + r;
+      C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1])
+                                                                         : s[0] + residual(p, m, n));
     } else {
 #pragma unroll
       for (int gu = 0; gu < kPlanes; ++gu) part[(static_cast<int64_t>(gu) * p.M + m) * p.N + row_lo + r] = s[gu];
@@ -250,7 +257,8 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
         s[gu] = (sl == 0) ? x : s[gu] + x;
       }
     }
-    C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0]);
+    C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1])
+                                                                       : s[0] + residual(p, m, n));
   }
   if (threadIdx.x == 0) atomicExch(&p.counters[blockIdx.x], 0u);
 }

@@ -57,6 +57,8 @@ struct TcParams {
   DeviceError* err;
   uint64_t timeout_ns;
   uint32_t inject_extra_tx;  // failure injection: extra bytes expected on the first stage
+  const uint16_t* R;     // non-null: residual, C = A . B^T + R (R[m * ldr + n], may be C)
+  int64_t ldr;
 };
 
 // Non-swapped GEMM: A-operand = A (rows M), B-operand = B (rows N), BN = 256.
@@ -102,6 +104,8 @@ struct CcParams {
   int32_t k_slice;       // k elements per slice (multiple of 8)
   float* partials;       // split_k * M * N fp32 when split_k > 1
   uint32_t* counters;    // one per CTA row group
+  const uint16_t* R;     // non-null: residual added to the result (R[m * ldr + n], may be C)
+  int64_t ldr;
 };
 
 cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream);

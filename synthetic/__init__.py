@@ -211,6 +211,33 @@ GATED_WORKLOADS = {g.name: g for g in [GatedWorkload(WORKLOADS[n]) for n in
                                        ("mlp_up", "dec1_up", "dec2_up", "dec16_up", "dec64_up")]}
 
 
+@dataclasses.dataclass(frozen=True)
+class ResidualWorkload:
+    """One synthetic projection with its residual added, C = A . B^T + R: the
+    Llama MLP's down projection onto the residual stream R ~ N(0, 1), [M, N]."""
+    base: Workload
+
+    @property
+    def name(self) -> str:
+        return "resid_" + self.base.name
+
+    def r(self) -> np.ndarray:
+        return matrix(self.base.M, self.base.N, "normal:1", self.base.seed_a + 2000)
+
+    @property
+    def flops(self) -> int:
+        return self.base.flops
+
+    @property
+    def decode_bytes(self) -> int:
+        b = self.base
+        return 2 * (b.N * b.K + b.M * b.K + 2 * b.M * b.N)
+
+
+RESIDUAL_WORKLOADS = {r.name: r for r in [ResidualWorkload(WORKLOADS[n]) for n in
+                                          ("mlp_down", "dec1_down", "dec16_down", "dec64_down")]}
+
+
 def sample_indices(extent: int, count: int, seed: int) -> np.ndarray:
     """A sorted, seeded choice of ``count`` distinct indices in [0, extent)."""
     if count >= extent:
