@@ -445,11 +445,16 @@ int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C
   if (st == SG_OK) st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, plan.tile_n, plan.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE, dev);
   if (st != SG_OK) return st;
+  CUtensorMap tr;
+  if (R != nullptr) {
+    st = make_map(&tr, R, M, N, ldr, plan.tile_n, plan.tile_m, CU_TENSOR_MAP_SWIZZLE_NONE, dev);
+    if (st != SG_OK) return st;
+  }
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
   p.R = static_cast<const uint16_t*>(R);
   p.ldr = ldr;
-  cudaError_t e = launch_tc_skinny(plan.tile_n, plan.tile_m, tw, tx, tc, p, stream);
+  cudaError_t e = launch_tc_skinny(plan.tile_n, plan.tile_m, tw, tx, tc, p, stream, R ? &tr : nullptr);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 

@@ -84,7 +84,7 @@ struct TcLayout {
   static constexpr int kFixStagingBytes = kFixupWarps * kStagingBufs * kStagingBufBytes;
   static constexpr int kBarOff = kFixStagingOff + kFixStagingBytes;
   // full[S], empty[S], tmem_full[2], tmem_empty[2], teardown, fixup, job[kMaxJobs]
-  static constexpr int kNumBars = 2 * STAGES + 6 + kMaxJobs;
+  static constexpr int kNumBars = 2 * STAGES + 6 + kMaxJobs + 1;  // + the residual tile's load
   static constexpr int kRingBytes = STAGES * (kABytes + kBBytes);
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, sk flag
   static constexpr int kJobOff = kMiscOff + 16;            // kMaxJobs x {tm, tn, last, -}
@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
   uint64_t* teardown = bars + 2 * STAGES + 4;
   uint64_t* fixup_bar = bars + 2 * STAGES + 5;  // bulk loads of Stream-K partials
   uint64_t* job_bar = bars + 2 * STAGES + 6;    // Stream-K piece j handed to the fixup warps
+  uint64_t* resid_bar = job_bar + L::kMaxJobs;  // swapped path: the residual tile's TMA load
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 4);
   volatile uint32_t* sk_last = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 8);
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
     mbar_init(teardown, 1);
     mbar_init(fixup_bar, 1);
     for (int j = 0; j < L::kMaxJobs; ++j) mbar_init(&job_bar[j], 1);
+    mbar_init(resid_bar, 1);
     *abort_flag = 0;
     *sk_last = 0;
     fence_mbar_init();
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
-    if (GATED) tma_prefetch_desc(&tmW2);
+    tma_prefetch_desc(&tmW2);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -415,6 +417,10 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
     const bool holds_row = !SWAP || L::kARows == kBM || lane < 16;
     const int slot_row = (SWAP && L::kARows != kBM) ? q * 16 + lane : row;
     constexpr int kEpiThreads = 32 * L::kEpiWarps;
+    // Swapped path with a residual: tmW2 maps R like C, and begin_tile loads the
+    // tile's R values into the staging tile, which the chunks then add to and
+    // overwrite with their outputs.
+    const bool swap_resid = SWAP && !GATED && p.R != nullptr;
 
     // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
     auto emit_chunk = [&](float* v, int tm, int tn, int j) {
@@ -429,24 +435,33 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         // 16 rows land in 32 contiguous bytes per m.
         if (holds_row) {
           __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(smem + L::kStagingOff);
-          const int n = tm * L::kARows + slot_row;  // output column (weight row)
 #pragma unroll
           for (int e = 0; e < L::kChunk; ++e) {
+            __nv_bfloat16& o = st[(j * L::kChunk + e) * L::kARows + slot_row];
             float x = v[e];
-            const int m = tn * BN + j * L::kChunk + e;  // output row (activation row)
-            if (!GATED && p.R != nullptr && m < p.M && n < p.N)
-              x += __uint_as_float(static_cast<uint32_t>(p.R[static_cast<int64_t>(m) * p.ldr + n]) << 16);
-            st[(j * L::kChunk + e) * L::kARows + slot_row] = __float2bfloat16_rn(x);
+            if (swap_resid) x += __bfloat162float(o);  // R[m][n], loaded by begin_tile
+            o = __float2bfloat16_rn(x);
           }
         }
       }
     };
     // Swapped path: a tile's outputs are gathered in shared memory and written by
     // one TMA store (rows past M and columns past N are clipped by the copy).
-    auto begin_tile = [&]() {
+    uint32_t resid_phase = 0;
+    auto begin_tile = [&](int tm, int tn) {
       if constexpr (SWAP) {
         if (epi_tid == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
         named_bar_sync(2, kEpiThreads);
+        if (swap_resid) {
+          if (epi_tid == 0) {
+            mbar_arrive_expect_tx(resid_bar, static_cast<uint32_t>(BN * L::kARows * 2));
+            tma_load_2d(smem + L::kStagingOff, &tmW2, tm * L::kARows, tn * BN, resid_bar);
+          }
+          const bool landed = mbar_wait(resid_bar, resid_phase, p.timeout_ns, abort_flag);
+          if (!landed && !*abort_flag) record_error(p.err, kDevTimeoutFull, 4000);
+          if (bar_sync_or(2, kEpiThreads, !landed)) *abort_flag = 1;  // the tile is then stored unfinished
+          resid_phase ^= 1u;
+        }
       }
     };
     auto end_tile = [&](int tm, int tn) {
@@ -511,7 +526,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
       if (GATED && w.npieces == 1) {
         // Whole gated tile: output chunk j combines accumulator columns j * kChunk
         // (gate) and kOutCols + j * kChunk (up) of this thread's row.
-        begin_tile();
+        begin_tile(tm, tn);
 #pragma unroll 1
         for (int jo = 0; jo < kOutCols / L::kChunk; ++jo) {
           uint32_t rg[L::kChunk], ru[L::kChunk];
@@ -530,7 +545,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         // Whole tile: the TMEM load of chunk j + 1 is in flight while chunk j is
         // converted and stored.
         constexpr int kChunks = L::kColsPerEpiWarp / L::kChunk;
-        begin_tile();
+        begin_tile(tm, tn);
         uint32_t ra[L::kChunk], rb[L::kChunk];
         issue_chunk(tacc + chunk_lo * L::kChunk, ra);
         tmem_ld_wait(ra);
@@ -626,7 +641,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
           if (bar_sync_or(1, kEpiThreads, !landed)) {
             *abort_flag = 1;
           } else {
-            begin_tile();
+            begin_tile(tm, tn);
             const float4* rs = reinterpret_cast<const float4*>(ring);
             emit_summed([&](int j, float* acc) {
 #pragma unroll
@@ -654,7 +669,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
           // Loads in flight per batch: kBatch pieces x kBQuads float4 of one chunk.
           constexpr int kBatch = (kQuads <= 4 && !GATED) ? 4 : 2;  // pieces per batch (8-16 loads in flight)
           constexpr int kBQuads = kQuads;                // float4 per piece per batch: the whole chunk
-          begin_tile();
+          begin_tile(tm, tn);
           emit_summed([&](int j, float* acc) {
 #pragma unroll
             for (int e = 0; e < L::kChunk; ++e) acc[e] = 0.f;
@@ -842,10 +857,10 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 
 template <int BN, int ROWS>
 cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmC, const TcParams& p,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const CUtensorMap* tmR) {
   static_assert(TcLayout<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>::kMinBlocks == kSkinnyCtasPerSm,
                 "the skinny plan counts on two resident CTAs per SM");
-  return launch_variant<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>(tmW, tmX, tmC, p, stream);
+  return launch_variant<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>(tmW, tmX, tmC, p, stream, tmR);
 }
 
 template <int BN>
@@ -868,12 +883,12 @@ cudaError_t launch_tc_skinny_swiglu(int bn, const CUtensorMap& tmG, const CUtens
 }
 
 cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
+                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream, const CUtensorMap* tmR) {
   if (rows == 64) {
     switch (bn) {
-      case 16: return launch_skinny<16, 64>(tmW, tmX, tmC, p, stream);
-      case 32: return launch_skinny<32, 64>(tmW, tmX, tmC, p, stream);
-      case 64: return launch_skinny<64, 64>(tmW, tmX, tmC, p, stream);
+      case 16: return launch_skinny<16, 64>(tmW, tmX, tmC, p, stream, tmR);
+      case 32: return launch_skinny<32, 64>(tmW, tmX, tmC, p, stream, tmR);
+      case 64: return launch_skinny<64, 64>(tmW, tmX, tmC, p, stream, tmR);
       default: return cudaErrorInvalidValue;
     }
   }

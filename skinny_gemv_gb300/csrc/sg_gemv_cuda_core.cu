@@ -109,6 +109,18 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   grid_dependency_wait();  // no global access before the previous kernel has completed
 
   static_assert(R % 2 == 0, "weight rows are processed in pairs");
+  // Without a K split, each thread's outputs are known from the start: elements
+  // threadIdx.x + j * blockDim.x of the CTA's rows x M block (at most 8 of them:
+  // rows <= 256, M <= 8).  Their residuals are loaded now, behind the stream.
+  constexpr int kResidPer = 8;
+  float rres[kResidPer];
+  if (!GATED && p.R != nullptr && p.split_k == 1) {
+#pragma unroll
+    for (int j = 0; j < kResidPer; ++j) {
+      const int e = threadIdx.x + j * kCcWarps * 32;
+      rres[j] = e < (row_hi - row_lo) * p.M ? residual(p, e % p.M, row_lo + e / p.M) : 0.f;
+    }
+  }
   for (int r0 = row_lo; r0 < row_hi; r0 += kRowStep) {
     // acc[r / 2][m] holds the fp32 sums of weight rows r (x) and r + 1 (y) for
     // activation row m; one paired FMA updates both.
@@ -213,7 +225,11 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   const int rows = row_hi - row_lo;
   __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.C);
   float* part = p.partials + static_cast<int64_t>(slice) * kPlanes * p.M * p.N;
-  for (int e = threadIdx.x; e < rows * p.M; e += blockDim.x) {
+  // rows * M <= 256 * 8 = kResidPer * blockDim.x: element e = threadIdx.x + j * blockDim.x
+#pragma unroll
+  for (int j = 0; j < kResidPer; ++j) {
+    const int e = threadIdx.x + j * kCcWarps * 32;
+    if (e >= rows * p.M) break;
     const int r = e / p.M, m = e % p.M;
     float s[kPlanes];
 #pragma unroll
@@ -225,8 +241,8 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     }
     if (p.split_k == 1) {
       const int64_t n = row_lo + r;
-      C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1])
-                                                                         : s[0] + residual(p, m, n));
+      const float res = (!GATED && p.R != nullptr) ? rres[j] : 0.f;  // prefetched at the start
+      C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0] + res);
     } else {
 #pragma unroll
       for (int gu = 0; gu < kPlanes; ++gu) part[(static_cast<int64_t>(gu) * p.M + m) * p.N + row_lo + r] = s[gu];

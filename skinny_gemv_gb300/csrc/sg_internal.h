@@ -83,7 +83,8 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 // B-operand = activations A (rows M <= bn), bn in {16, 32, 64}; tmC stores C in
 // boxes of bn rows x `rows` columns.
 cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream);
+                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream,
+                             const CUtensorMap* tmR = nullptr);  // tmR: the residual, mapped like C
 
 
 // Gated swapped skinny GEMM: C = silu(X . G^T) * (X . U^T) for M <= bn activation
