@@ -172,6 +172,24 @@ SG_API int gemm_bf16_residual_path(const void *A, const void *B, const void *R, 
                             int64_t lda, int64_t ldb, int64_t ldr, int64_t ldc, int path, sg_stream_t stream);
 
 /*
+ * gemv_bf16_batched -- several skinny GEMMs that share their activations, in one
+ * launch: for i < count, C_i[m, n] = sum_k A[m, k] B_i[n, k] (1 <= M <= 64).
+ *
+ * The decode step's projections that read the same input (Q, K and V; several
+ * small weights of one layer) then cost one launch and fill the GPU together
+ * (the pages' "next" step: amortise the ~2 us a launch costs a decode step).  A is
+ * M x K (lda); B[i] is N[i] x K (ldb[i]); C[i] is M x N[i] (ldc[i]); count <= 8; the
+ * arrays are host arrays of device pointers and sizes.  path: SG_PATH_AUTO (the
+ * CUDA-core stream for M <= 2, else tcgen05), SG_PATH_CUDA_CORE or
+ * SG_PATH_TENSOR_CORE.  Each C_i is exactly what gemv_bf16 gives for (A, B_i)
+ * with the same kernel, up to the order of the fp32 sums.  Errors as gemv_bf16
+ * for each matrix, plus SG_ERR_INVALID_ARG for count outside 1..8 or null arrays.
+ */
+SG_API int gemv_bf16_batched(const void *A, int64_t M, int64_t K, int64_t lda,
+                      const void *const *B, const int64_t *N, const int64_t *ldb,
+                      void *const *C, const int64_t *ldc, int count, int path, sg_stream_t stream);
+
+/*
  * gemv_bf16_noalloc -- gemv_bf16 on the CUDA-core kernel (SG_PATH_CUDA_CORE),
  * for callers that cannot allocate device memory.  The pages have no
  * counterpart: this entry point exists for integration, not for the method.

@@ -102,6 +102,9 @@ def load(build_if_missing: bool = False):
     lib.gemm_bf16_residual.restype = ctypes.c_int
     lib.gemm_bf16_residual_path.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i64, ctypes.c_int, p]
     lib.gemm_bf16_residual_path.restype = ctypes.c_int
+    pp, p64 = ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int64)
+    lib.gemv_bf16_batched.argtypes = [p, i64, i64, i64, pp, p64, p64, pp, p64, ctypes.c_int, ctypes.c_int, p]
+    lib.gemv_bf16_batched.restype = ctypes.c_int
     lib.sg_status_string.argtypes = [ctypes.c_int]
     lib.sg_status_string.restype = ctypes.c_char_p
     lib.sg_last_cuda_error.argtypes = []
@@ -261,6 +264,34 @@ def gemm_bf16_residual(A, B, R, C=None, stream=None, path: int = PATH_AUTO):
                                             _stream_handle(stream))
     _check(st, "gemm_bf16_residual")
     return C
+
+
+def gemv_bf16_batched(A, Bs, Cs=None, stream=None, path: int = PATH_AUTO):
+    """C_i = A @ B_i^T for every weight B_i (all [N_i, K]) in one launch; returns
+    the list of C_i."""
+    torch = _torch()
+    a_ptr, lda = _operand(A, "A")
+    M, K = A.shape
+    n = len(Bs)
+    if Cs is None:
+        Cs = []
+        for B in Bs:
+            ld = -(-B.shape[0] // 8) * 8
+            Cs.append(torch.empty((M, ld), dtype=torch.bfloat16, device=A.device)[:, :B.shape[0]])
+    if len(Cs) != n:
+        raise ValueError("one output per weight")
+    bp, nn, lb, cp, lc = ((ctypes.c_void_p * n)(), (ctypes.c_int64 * n)(), (ctypes.c_int64 * n)(),
+                          (ctypes.c_void_p * n)(), (ctypes.c_int64 * n)())
+    for i, (B, C) in enumerate(zip(Bs, Cs)):
+        b_ptr, ldb = _operand(B, f"B[{i}]")
+        c_ptr, ldc = _operand(C, f"C[{i}]")
+        if B.shape[1] != K or tuple(C.shape) != (M, B.shape[0]):
+            raise ValueError(f"shapes of B[{i}] {tuple(B.shape)} / C[{i}] {tuple(C.shape)}")
+        bp[i], nn[i], lb[i], cp[i], lc[i] = b_ptr, B.shape[0], ldb, c_ptr, ldc
+    with torch.cuda.device(A.device):
+        st = load().gemv_bf16_batched(a_ptr, M, K, lda, bp, nn, lb, cp, lc, n, path, _stream_handle(stream))
+    _check(st, "gemv_bf16_batched")
+    return Cs
 
 
 def gemv_bf16(A, B, C=None, stream=None, path: int = PATH_AUTO):

@@ -490,6 +490,72 @@ int run_cc(DeviceState& d, const void* A, const void* B, void* C, int64_t M, int
   return SG_OK;
 }
 
+// One launch over `count` weight matrices against the same activations A: the
+// CUDA-core kernel over their concatenated output rows (row blocks may span two
+// matrices), or the swapped tcgen05 kernel over their concatenated 64-row tiles
+// (each tile inside one matrix).
+int run_batched(DeviceState& d, int dev, const void* A, int64_t M, int64_t K, int64_t lda, const void* const* B,
+                const int64_t* N, const int64_t* ldb, void* const* C, const int64_t* ldc, int count, int path,
+                cudaStream_t stream) {
+  if (path == SG_PATH_CUDA_CORE) {
+    int64_t ntot = 0;
+    for (int i = 0; i < count; ++i) ntot += N[i];
+    for (int64_t m0 = 0; m0 < M; m0 += 8) {
+      const int64_t mb = std::min<int64_t>(8, M - m0);
+      sg_plan_info plan;
+      plan_cc(mb, ntot, K, d.sm_count, &plan);
+      CcParams p{};
+      p.A = static_cast<const uint16_t*>(A) + m0 * lda;
+      p.M = static_cast<int32_t>(mb);
+      p.N = static_cast<int32_t>(ntot);
+      p.K = static_cast<int32_t>(K);
+      p.lda = lda;
+      p.grid_rows = plan.tiles_m;
+      p.split_k = plan.split_k;
+      p.k_slice = plan.k_steps;
+      p.partials = d.partials;
+      p.counters = d.counters;
+      p.nbatch = count;
+      int64_t r = 0;
+      for (int i = 0; i < count; ++i) {
+        p.row_begin[i] = static_cast<int32_t>(r);
+        r += N[i];
+        p.Bs[i] = static_cast<const uint16_t*>(B[i]);
+        p.Cs[i] = static_cast<uint16_t*>(C[i]) + m0 * ldc[i];
+        p.ldbs[i] = ldb[i];
+        p.ldcs[i] = ldc[i];
+      }
+      p.row_begin[count] = static_cast<int32_t>(r);
+      cudaError_t e = launch_cc_gemv(p, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return SG_OK;
+  }
+  // tensor cores: plan over the concatenated tiles
+  const int64_t rows = skinny_rows(M);
+  int64_t tiles = 0;
+  for (int i = 0; i < count; ++i) tiles += ceil_div(N[i], rows);
+  sg_plan_info plan;
+  plan_tc_skinny(M, tiles * rows, K, d.sm_count, &plan);
+  TcBatchMaps maps{};
+  CUtensorMap tx;
+  int st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  TcParams p = base_params(d, M, tiles * rows, K, 0, nullptr);
+  p.sched = sched_from_plan(plan);
+  p.nbatch = count;
+  int64_t t = 0;
+  for (int i = 0; i < count && st == SG_OK; ++i) {
+    p.tile_begin[i] = static_cast<int32_t>(t);
+    t += ceil_div(N[i], rows);
+    st = make_map(&maps.w[i], B[i], N[i], K, ldb[i], rows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+    if (st == SG_OK) st = make_map(&maps.c[i], C[i], M, N[i], ldc[i], plan.tile_n, rows, CU_TENSOR_MAP_SWIZZLE_NONE, dev);
+  }
+  if (st != SG_OK) return st;
+  p.tile_begin[count] = static_cast<int32_t>(t);
+  cudaError_t e = launch_tc_skinny(plan.tile_n, plan.tile_m, maps.w[0], tx, maps.c[0], p, stream, nullptr, &maps);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
 // C := 0 (no residual) or C := R, the value of an empty sum plus the residual.
 int empty_sum(void* C, int64_t M, int64_t N, int64_t ldc, const void* R, int64_t ldr, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
@@ -631,6 +697,49 @@ int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t ent
   else
     plan_tc_swiglu(M, N, K, num_sms, path == SG_PATH_GEMM_PAIR, out);
   return SG_OK;
+}
+
+int gemv_bf16_batched(const void* A, int64_t M, int64_t K, int64_t lda, const void* const* B, const int64_t* N,
+                      const int64_t* ldb, void* const* C, const int64_t* ldc, int count, int path, sg_stream_t stream) {
+  if (count < 1 || count > kMaxBatch || !B || !N || !ldb || !C || !ldc) return SG_ERR_INVALID_ARG;
+  if (path != SG_PATH_AUTO && path != SG_PATH_CUDA_CORE && path != SG_PATH_TENSOR_CORE) return SG_ERR_INVALID_ARG;
+  if (M > 64) return SG_ERR_INVALID_ARG;
+  int64_t ntot = 0;
+  for (int i = 0; i < count; ++i) {
+    const int st = validate(A, B[i], C[i], M, N[i], K, lda, ldb[i], ldc[i]);
+    if (st != SG_OK) return st;
+    ntot += N[i];
+  }
+  if (ntot > INT32_MAX / 2) return SG_ERR_INVALID_ARG;
+  if (M == 0 || ntot == 0) return SG_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState* d = nullptr;
+  int dev = 0;
+  int st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  if (K == 0) {
+    for (int i = 0; i < count && st == SG_OK; ++i)
+      if (N[i] > 0) st = empty_sum(C[i], M, N[i], ldc[i], nullptr, 0, s);
+    return st;
+  }
+  st = ensure_workspace(*d, s);
+  if (st != SG_OK) return st;
+  if (path == SG_PATH_AUTO) path = choose_skinny_path(M);
+  // matrices with no rows take no part
+  const void* b2[kMaxBatch];
+  void* c2[kMaxBatch];
+  int64_t n2[kMaxBatch], lb2[kMaxBatch], lc2[kMaxBatch];
+  int cnt = 0;
+  for (int i = 0; i < count; ++i)
+    if (N[i] > 0) {
+      b2[cnt] = B[i];
+      c2[cnt] = C[i];
+      n2[cnt] = N[i];
+      lb2[cnt] = ldb[i];
+      lc2[cnt] = ldc[i];
+      ++cnt;
+    }
+  return run_batched(*d, dev, A, M, K, lda, b2, n2, lb2, c2, lc2, cnt, path, s);
 }
 
 const char* sg_status_string(int status) {

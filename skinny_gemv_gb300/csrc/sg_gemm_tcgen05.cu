@@ -185,11 +185,17 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
                                   TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>::kMinBlocks)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW2,
-                   const TcParams p) {
+                   const TcParams p, const __grid_constant__ TcBatchMaps bmaps) {
   using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   constexpr bool SWAP = L::SWAP;
   // output columns per tile
   constexpr int kOutCols = (GATED && !SWAP) ? BN / 2 : BN;
+  // A batched swapped launch: weight tile tm is tile tm - tile_begin[i] of matrix i.
+  auto batch_of = [&](int tm) {
+    int i = 0;
+    while (i + 1 < p.nbatch && tm >= p.tile_begin[i + 1]) ++i;
+    return i;
+  };
   // Gated accumulators alternate blocks of kHalf gate columns and kHalf up
   // columns: one block each on the swapped path and in a single-CTA tile, and
   // per CTA of a pair (each CTA's B rows are 64 gate over 64 up rows).
@@ -274,7 +280,13 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         const WorkItem w = get_item(sched, unit, i);
         int32_t tm, tn;
         tile_coords(sched, w.tile, tm, tn);
-        const int arow = tm * kTileRows + static_cast<int>(rank) * L::kARows;
+        int arow = tm * kTileRows + static_cast<int>(rank) * L::kARows;
+        const CUtensorMap* wmap = &tmA;
+        if (SWAP && p.nbatch > 0) {
+          const int bi = batch_of(tm);
+          wmap = &bmaps.w[bi];
+          arow = (tm - p.tile_begin[bi]) * L::kARows;
+        }
         const int brow = tn * kOutCols + static_cast<int>(rank) * (GATED ? L::kBRowsPerCta / 2 : L::kBRowsPerCta);
         for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
           const uint32_t s = it % STAGES;
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
               const int kx = (ks * KSUB + j) * kBK;
               uint8_t* bdst = smem + L::kBOff + s * L::kBBytes + j * L::kBSub;
               uint8_t* adst = smem + L::kAOff + s * L::kABytes + j * L::kAMats * L::kASub;
-              tma_load_2d(adst, &tmA, kx, arow, &full[s]);
+              tma_load_2d(adst, wmap, kx, arow, &full[s]);
               if constexpr (SWAP && GATED) tma_load_2d(adst + L::kASub, &tmW2, kx, arow, &full[s]);
               if constexpr (GATED && !SWAP) {
                 // gate rows over up rows of the same output columns
@@ -469,7 +481,12 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         fence_proxy_async_smem();
         named_bar_sync(2, kEpiThreads);
         if (epi_tid == 0) {
-          tma_store_2d(&tmC, smem + L::kStagingOff, tm * L::kARows, tn * BN);
+          if (p.nbatch > 0) {
+            const int bi = batch_of(tm);
+            tma_store_2d(&bmaps.c[bi], smem + L::kStagingOff, (tm - p.tile_begin[bi]) * L::kARows, tn * BN);
+          } else {
+            tma_store_2d(&tmC, smem + L::kStagingOff, tm * L::kARows, tn * BN);
+          }
           bulk_commit_group();
         }
       }
@@ -807,7 +824,9 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
 
 template <int BN, int STAGES, int SWAP_ROWS, int KSUB, bool PAIR, bool GATED = false>
 cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
-                           cudaStream_t stream, const CUtensorMap* b2 = nullptr) {
+                           cudaStream_t stream, const CUtensorMap* b2 = nullptr,
+                           const TcBatchMaps* batch = nullptr) {
+  static const TcBatchMaps kNoBatch{};
   using L = TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   auto kern = tc_gemm_kernel<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GATED>;
   static bool configured = false;  // the attribute is per function, process-wide
@@ -830,7 +849,7 @@ cudaError_t launch_variant(const CUtensorMap& a, const CUtensorMap& b, const CUt
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, c, b2 ? *b2 : b, p);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, b2 ? *b2 : b, p, batch ? *batch : kNoBatch);
 }
 
 }  // namespace
@@ -857,10 +876,11 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 
 template <int BN, int ROWS>
 cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmC, const TcParams& p,
-                          cudaStream_t stream, const CUtensorMap* tmR) {
+                          cudaStream_t stream, const CUtensorMap* tmR, const TcBatchMaps* batch) {
   static_assert(TcLayout<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>::kMinBlocks == kSkinnyCtasPerSm,
                 "the skinny plan counts on two resident CTAs per SM");
-  return launch_variant<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>(tmW, tmX, tmC, p, stream, tmR);
+  return launch_variant<BN, skinny_stages(BN, ROWS), ROWS, skinny_ksub(ROWS), false>(tmW, tmX, tmC, p, stream, tmR,
+                                                                                     batch);
 }
 
 template <int BN>
@@ -883,12 +903,13 @@ cudaError_t launch_tc_skinny_swiglu(int bn, const CUtensorMap& tmG, const CUtens
 }
 
 cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream, const CUtensorMap* tmR) {
+                             const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream, const CUtensorMap* tmR,
+                             const TcBatchMaps* batch) {
   if (rows == 64) {
     switch (bn) {
-      case 16: return launch_skinny<16, 64>(tmW, tmX, tmC, p, stream, tmR);
-      case 32: return launch_skinny<32, 64>(tmW, tmX, tmC, p, stream, tmR);
-      case 64: return launch_skinny<64, 64>(tmW, tmX, tmC, p, stream, tmR);
+      case 16: return launch_skinny<16, 64>(tmW, tmX, tmC, p, stream, tmR, batch);
+      case 32: return launch_skinny<32, 64>(tmW, tmX, tmC, p, stream, tmR, batch);
+      case 64: return launch_skinny<64, 64>(tmW, tmX, tmC, p, stream, tmR, batch);
       default: return cudaErrorInvalidValue;
     }
   }

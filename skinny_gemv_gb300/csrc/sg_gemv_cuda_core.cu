@@ -51,6 +51,22 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
+// Weight row and output location of output row n (of the N rows): in a batched
+// launch, row n - row_begin[i] of matrix i.
+__device__ __forceinline__ const uint16_t* weight_row(const CcParams& p, int n) {
+  if (p.nbatch == 0) return p.B + static_cast<int64_t>(n) * p.ldb;
+  int i = 0;
+  while (i + 1 < p.nbatch && n >= p.row_begin[i + 1]) ++i;
+  return p.Bs[i] + static_cast<int64_t>(n - p.row_begin[i]) * p.ldbs[i];
+}
+
+__device__ __forceinline__ uint16_t* output_at(const CcParams& p, int m, int n) {
+  if (p.nbatch == 0) return p.C + static_cast<int64_t>(m) * p.ldc + n;
+  int i = 0;
+  while (i + 1 < p.nbatch && n >= p.row_begin[i + 1]) ++i;
+  return p.Cs[i] + static_cast<int64_t>(m) * p.ldcs[i] + (n - p.row_begin[i]);
+}
+
 // The residual R[m, n] as fp32 (0 without one); R may be C itself.
 __device__ __forceinline__ float residual(const CcParams& p, int64_t m, int64_t n) {
   return p.R != nullptr ? __uint_as_float(static_cast<uint32_t>(p.R[m * p.ldr + n]) << 16) : 0.f;
@@ -138,7 +154,7 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
         brow[r] = ((r & 1) ? p.B2 : p.B) + static_cast<int64_t>(row_ok[r] ? r0 + r / 2 : r0) * p.ldb;
       } else {
         row_ok[r] = r0 + r < row_hi;
-        brow[r] = p.B + static_cast<int64_t>(row_ok[r] ? r0 + r : r0) * p.ldb;
+        brow[r] = weight_row(p, row_ok[r] ? r0 + r : r0);
       }
     }
     for (int v = v_lo + lane; v < v_hi; v += 32 * U) {
@@ -223,7 +239,6 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   // (gu = 0 gate, 1 up; one plane when not gated).
   constexpr int kPlanes = GATED ? 2 : 1;
   const int rows = row_hi - row_lo;
-  __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(p.C);
   float* part = p.partials + static_cast<int64_t>(slice) * kPlanes * p.M * p.N;
   // rows * M <= 256 * 8 = kResidPer * blockDim.x: element e = threadIdx.x + j * blockDim.x
 #pragma unroll
@@ -242,7 +257,8 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     if (p.split_k == 1) {
       const int64_t n = row_lo + r;
       const float res = (!GATED && p.R != nullptr) ? rres[j] : 0.f;  // prefetched at the start
-      C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0] + res);
+      *reinterpret_cast<__nv_bfloat16*>(output_at(p, m, static_cast<int>(n))) =
+          __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0] + res);
     } else {
 #pragma unroll
       for (int gu = 0; gu < kPlanes; ++gu) part[(static_cast<int64_t>(gu) * p.M + m) * p.N + row_lo + r] = s[gu];
@@ -273,8 +289,8 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
         s[gu] = (sl == 0) ? x : s[gu] + x;
       }
     }
-    C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1])
-                                                                       : s[0] + residual(p, m, n));
+    *reinterpret_cast<__nv_bfloat16*>(output_at(p, m, n)) =
+        __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0] + residual(p, m, n));
   }
   if (threadIdx.x == 0) atomicExch(&p.counters[blockIdx.x], 0u);
 }

@@ -12,6 +12,9 @@ namespace sg {
 
 struct DeviceError;
 
+// Most weight matrices one batched skinny launch takes.
+constexpr int kMaxBatch = 8;
+
 constexpr int kBM = 128;  // MMA M (tile rows; weight rows on the swapped path)
 constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
 constexpr int kGemmBN = 256;
@@ -59,6 +62,16 @@ struct TcParams {
   uint32_t inject_extra_tx;  // failure injection: extra bytes expected on the first stage
   const uint16_t* R;     // non-null: residual, C = A . B^T + R (R[m * ldr + n], may be C)
   int64_t ldr;
+  // Batched swapped launch (nbatch > 0): weight tiles [tile_begin[i], tile_begin[i + 1])
+  // belong to matrix i, read through batch maps w[i] and stored through c[i].
+  int32_t nbatch;
+  int32_t tile_begin[kMaxBatch + 1];
+};
+
+// Tensor maps of a batched swapped launch: matrix i's weights and output.
+struct TcBatchMaps {
+  CUtensorMap w[kMaxBatch];
+  CUtensorMap c[kMaxBatch];
 };
 
 // Non-swapped GEMM: A-operand = A (rows M), B-operand = B (rows N), BN = 256.
@@ -84,7 +97,8 @@ cudaError_t launch_tc_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 // boxes of bn rows x `rows` columns.
 cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUtensorMap& tmX,
                              const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream,
-                             const CUtensorMap* tmR = nullptr);  // tmR: the residual, mapped like C
+                             const CUtensorMap* tmR = nullptr,  // tmR: the residual, mapped like C
+                             const TcBatchMaps* batch = nullptr);
 
 
 // Gated swapped skinny GEMM: C = silu(X . G^T) * (X . U^T) for M <= bn activation
@@ -107,6 +121,14 @@ struct CcParams {
   uint32_t* counters;    // one per CTA row group
   const uint16_t* R;     // non-null: residual added to the result (R[m * ldr + n], may be C)
   int64_t ldr;
+  // Batched launch (nbatch > 0): output rows [row_begin[i], row_begin[i + 1]) of the
+  // N rows belong to matrix i (weights Bs[i], ldbs[i]; outputs Cs[i], ldcs[i]).
+  int32_t nbatch;
+  int32_t row_begin[kMaxBatch + 1];
+  const uint16_t* Bs[kMaxBatch];
+  uint16_t* Cs[kMaxBatch];
+  int64_t ldbs[kMaxBatch];
+  int64_t ldcs[kMaxBatch];
 };
 
 cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream);
