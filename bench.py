@@ -507,10 +507,11 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         # decode rows first: right after seconds of power-capped GEMMs the
         # memory-bound rows measured up to 2 us slower per launch
         names = [n for n in syn.WORKLOADS if n.startswith("dec")] + ["sq2048", "mlp_up", "mlp_down", "sq8192"]
-        names += list(syn.GATED_WORKLOADS) + list(syn.RESIDUAL_WORKLOADS)
+        names += list(syn.GATED_WORKLOADS) + list(syn.RESIDUAL_WORKLOADS) + list(syn.BATCHED_WORKLOADS)
     gated_names = [n for n in names if n in syn.GATED_WORKLOADS]
     resid_names = [n for n in names if n in syn.RESIDUAL_WORKLOADS]
-    names = [n for n in names if n not in syn.GATED_WORKLOADS and n not in syn.RESIDUAL_WORKLOADS]
+    batched_names = [n for n in names if n in syn.BATCHED_WORKLOADS]
+    names = [n for n in names if n in syn.WORKLOADS]
     for name in names:
         w = syn.WORKLOADS[name]
         with torch.cuda.stream(stream):
@@ -605,6 +606,23 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         out.append(row)
         del As, Bs, Rs, A, B, R, C
         torch.cuda.empty_cache()
+    for name in batched_names:
+        bw = syn.BATCHED_WORKLOADS[name]
+        with torch.cuda.stream(stream):
+            A = draw(bw.M, bw.K, "normal:1", 4000 + bw.cfg)
+            Ws = [draw(n, bw.K, "normal:0.02", 4100 + bw.cfg + i) for i, n in enumerate(bw.Ns)]
+            nrot = rotation_count(2 * sum(bw.Ns) * bw.K, l2)
+            sets = [Ws] + [[w.clone() for w in Ws] for _ in range(nrot - 1)]
+            Cs = [torch.empty((bw.M, n), dtype=torch.bfloat16, device=stream.device) for n in bw.Ns]
+        stream.synchronize()
+        fns = [(lambda ws=ws: sg.gemv_bf16_batched(A, ws, Cs, stream=stream)) for ws in sets]
+        total = time_launches(torch, stream, fns, steps, 5)
+        med = total / steps
+        gbs = bw.decode_bytes / (med / 1e3) / 1e9
+        out.append({"workload": name, "entry": "gemv_bf16_batched", "M": bw.M, "N": list(bw.Ns), "K": bw.K,
+                    "us": med * 1e3, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]})
+        del sets, Ws, A, Cs
+        torch.cuda.empty_cache()
     return out
 
 
@@ -665,7 +683,7 @@ def run_rows_only(args, local):
 
     names = [n.strip() for n in args.rows_only.split(",") if n.strip()]
     unknown = [n for n in names if n not in syn.WORKLOADS and n not in syn.GATED_WORKLOADS
-               and n not in syn.RESIDUAL_WORKLOADS]
+               and n not in syn.RESIDUAL_WORKLOADS and n not in syn.BATCHED_WORKLOADS]
     if unknown or not names:
         raise SystemExit(f"unknown workloads: {unknown or args.rows_only!r}")
     import torch

@@ -238,6 +238,33 @@ RESIDUAL_WORKLOADS = {r.name: r for r in [ResidualWorkload(WORKLOADS[n]) for n i
                                           ("mlp_down", "dec1_down", "dec16_down", "dec64_down")]}
 
 
+@dataclasses.dataclass(frozen=True)
+class BatchedWorkload:
+    """Several weight matrices read against the same activations in one launch:
+    the Llama attention's Q, K and V projections (three 4096 x 4096 weights) for
+    M decode tokens."""
+    name: str
+    M: int
+    Ns: tuple
+    K: int
+    cfg: int
+
+    def a(self) -> np.ndarray:
+        return matrix(self.M, self.K, "normal:1", SEED_A_BASE + self.cfg)
+
+    def bs(self) -> list:
+        return [matrix(n, self.K, "normal:0.02", SEED_B_BASE + self.cfg + 100 * i) for i, n in enumerate(self.Ns)]
+
+    @property
+    def decode_bytes(self) -> int:
+        n = sum(self.Ns)
+        return 2 * (n * self.K + self.M * self.K + self.M * n)
+
+
+BATCHED_WORKLOADS = {w.name: w for w in [BatchedWorkload(f"qkv_dec{m}", m, (4096, 4096, 4096), 4096, 40 + m)
+                                         for m in (1, 16, 64)]}
+
+
 def sample_indices(extent: int, count: int, seed: int) -> np.ndarray:
     """A sorted, seeded choice of ``count`` distinct indices in [0, extent)."""
     if count >= extent:

@@ -66,3 +66,12 @@ def test_empty_matrices_and_errors():
         sg.gemv_bf16_batched(A, [B1] * 9)   # more than 8 matrices
     with pytest.raises(sg.SgError):
         sg.gemv_bf16_batched(torch.randn(65, 64, device="cuda").bfloat16(), [B1])   # M > 64
+
+
+@pytest.mark.parametrize("w", list(syn.BATCHED_WORKLOADS.values()), ids=lambda w: w.name)
+def test_qkv_workloads(w):
+    # the bench's Q/K/V rows: three 4096 x 4096 weights, M = 1, 16, 64
+    A, Bs = w.a(), w.bs()
+    got = _run(A, Bs, w.K, sg.PATH_AUTO)
+    for i, (B, C) in enumerate(zip(Bs, got)):
+        assert_close(C, oracle.gemm(A, B), w.K, f"{w.name} matrix {i}")
