@@ -271,6 +271,9 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
   // first works out its first copy, so only the copy itself waits.
   grid_launch_dependents();
 
+  // Swapped path with a residual, one tile per CTA: the producer fetches the
+  // tile's residual values at the start instead of the epilogue at the end.
+  const bool resid_early = SWAP && !PAIR && !GATED && p.R != nullptr && sched.split > 0;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -328,8 +331,20 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
                 tma_load_2d(bdst, &tmB, kx, brow, &full[s]);
               }
             }
+            if (SWAP && !GATED && it == 0 && resid_early) {
+              // One tile per CTA: the residual tile goes into the store staging
+              // right behind the first weight stage.
+              mbar_arrive_expect_tx(resid_bar, static_cast<uint32_t>(BN * L::kARows * 2));
+              tma_load_2d(smem + L::kStagingOff, &tmW2, tm * L::kARows, tn * BN, resid_bar);
+            }
           }
         }
+      }
+      if (resid_early && it > 0) {
+        // The residual load lands before the CTA exits, whether or not this CTA
+        // finishes the tile.
+        volatile uint32_t never = 0;
+        mbar_wait(resid_bar, 0, p.timeout_ns, &never);
       }
       if (!ok && rank == 0) {
         // Unwinding: let the loads already issued land before the CTA exits.
@@ -465,7 +480,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         if (epi_tid == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
         named_bar_sync(2, kEpiThreads);
         if (swap_resid) {
-          if (epi_tid == 0) {
+          if (epi_tid == 0 && !resid_early) {
             mbar_arrive_expect_tx(resid_bar, static_cast<uint32_t>(BN * L::kARows * 2));
             tma_load_2d(smem + L::kStagingOff, &tmW2, tm * L::kARows, tn * BN, resid_bar);
           }
