@@ -291,6 +291,10 @@ typedef struct {
     double wave_efficiency; /* of one tile per CTA, (ctas/slots)/ceil(ctas/slots) */
     int32_t cluster_size; /* CTAs per schedule unit: 2 for SG_PATH_GEMM_PAIR, else 1 */
     int32_t ctas_per_sm;  /* CTAs the kernel keeps resident on one SM */
+    int32_t prefetch_steps; /* weights each CTA pulls into L2 before it waits for the
+                               previous work in the stream (a hint; reads nothing into
+                               the result): k-steps on the tensor-core skinny path, row
+                               passes (0 or 1) on the CUDA-core path; else 0 */
 } sg_plan_info;
 
 /*

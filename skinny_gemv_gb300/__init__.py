@@ -54,7 +54,7 @@ class PlanInfo(ctypes.Structure):
                 ("sk_tiles", ctypes.c_int32), ("sk_units", ctypes.c_int64), ("group_m", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32),
                 ("wave_efficiency", ctypes.c_double), ("cluster_size", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("prefetch_steps", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

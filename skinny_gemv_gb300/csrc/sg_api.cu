@@ -303,6 +303,11 @@ void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o, b
     o->split_k = 0;
   }
   o->wave_efficiency = wave_efficiency(o->grid, slots);
+  // Early L2 reads of the first weights pay when the next launch's CTAs can only
+  // start as this one's leave (the grid fills most slots); with many slots free,
+  // they start at once and compete with the running launch's stream (measured
+  // slower at N = 11,008 and 12,288, K = 4,096: 172 and 192 CTAs on 304 slots).
+  o->prefetch_steps = o->grid * 10 >= kPreWaitMinFill * slots ? kPreWaitSteps : 0;
 }
 
 // CUDA-core plan: two CTAs per SM, each owning a contiguous block of weight rows
@@ -338,6 +343,7 @@ void plan_cc(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o, bool gat
   o->k_steps = static_cast<int32_t>(k_slice);  // elements per K slice
   o->grid = static_cast<int32_t>(rows_grid * split);
   o->wave_efficiency = wave_efficiency(o->grid, 2 * static_cast<int64_t>(sms));
+  o->prefetch_steps = o->grid * 10 >= kPreWaitMinFill * target ? 1 : 0;  // one row pass
 }
 
 // The CUDA-core kernel spends M/2 paired fp32 FMAs per weight element; measured
@@ -431,6 +437,7 @@ int run_tc_skinny_swiglu(DeviceState& d, int dev, const void* A, const void* Wg,
   if (st != SG_OK) return st;
   TcParams p = base_params(d, M, N, K, ldc, C);
   p.sched = sched_from_plan(plan);
+  p.prewait_steps = plan.prefetch_steps;
   cudaError_t e = launch_tc_skinny_swiglu(plan.tile_n, tg, tu, tx, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
@@ -454,6 +461,7 @@ int run_tc_skinny(DeviceState& d, int dev, const void* A, const void* B, void* C
   p.sched = sched_from_plan(plan);
   p.R = static_cast<const uint16_t*>(R);
   p.ldr = ldr;
+  p.prewait_steps = plan.prefetch_steps;
   cudaError_t e = launch_tc_skinny(plan.tile_n, plan.tile_m, tw, tx, tc, p, stream, R ? &tr : nullptr);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
@@ -484,6 +492,7 @@ int run_cc(DeviceState& d, const void* A, const void* B, void* C, int64_t M, int
     p.counters = d.counters;
     p.R = R ? static_cast<const uint16_t*>(R) + m0 * ldr : nullptr;
     p.ldr = ldr;
+    p.prewait = plan.prefetch_steps;
     cudaError_t e = launch_cc_gemv(p, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -515,6 +524,7 @@ int run_batched(DeviceState& d, int dev, const void* A, int64_t M, int64_t K, in
       p.k_slice = plan.k_steps;
       p.partials = d.partials;
       p.counters = d.counters;
+      p.prewait = plan.prefetch_steps;
       p.nbatch = count;
       int64_t r = 0;
       for (int i = 0; i < count; ++i) {
@@ -542,6 +552,7 @@ int run_batched(DeviceState& d, int dev, const void* A, int64_t M, int64_t K, in
   int st = make_map(&tx, A, M, K, lda, plan.tile_n, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   TcParams p = base_params(d, M, tiles * rows, K, 0, nullptr);
   p.sched = sched_from_plan(plan);
+  p.prewait_steps = plan.prefetch_steps;
   p.nbatch = count;
   int64_t t = 0;
   for (int i = 0; i < count && st == SG_OK; ++i) {

@@ -268,8 +268,12 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
   // The set-up above touched no global memory, so it may overlap the previous
   // kernel's tail.  Each role waits for the previous kernel before its first
   // global access (and before any bounded wait starts its clock); the producer
-  // first works out its first copy, so only the copy itself waits.
-  grid_launch_dependents();
+  // first works out its first copy, so only the copy itself waits.  The GEMM
+  // lets the next launch start its set-up at once; the swapped kernel, which
+  // streams weights at the memory system's limit, only once its producer has
+  // issued its last copy, so the next launch's early weight reads fill its tail
+  // instead of competing with its stream.
+  if constexpr (!SWAP) grid_launch_dependents();
 
   // Swapped path with a residual, one tile per CTA: the producer fetches the
   // tile's residual values at the start instead of the epilogue at the end.
@@ -277,6 +281,29 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      if (SWAP && nitems > 0 && p.prewait_steps > 0) {
+        // Before the wait for the previous launch (whose tail this CTA may
+        // overlap), the first weight boxes are pulled into L2; the ring's loads
+        // then find them there.
+        const WorkItem w = get_item(sched, unit, 0);
+        int32_t tm, tn;
+        tile_coords(sched, w.tile, tm, tn);
+        int arow = tm * kTileRows;
+        const CUtensorMap* wmap = &tmA;
+        if (p.nbatch > 0) {
+          const int bi = batch_of(tm);
+          wmap = &bmaps.w[bi];
+          arow = (tm - p.tile_begin[bi]) * L::kARows;
+        }
+        const int kend = min(w.k1, w.k0 + p.prewait_steps);
+        for (int ks = w.k0; ks < kend; ++ks) {
+          const int nsub = min(KSUB, kboxes - ks * KSUB);
+          for (int j = 0; j < nsub; ++j) {
+            tma_prefetch_l2_2d(wmap, (ks * KSUB + j) * kBK, arow);
+            if constexpr (GATED) tma_prefetch_l2_2d(&tmW2, (ks * KSUB + j) * kBK, arow);
+          }
+        }
+      }
       uint32_t it = 0;
       bool ok = true;
       for (int i = 0; i < nitems && ok; ++i) {
@@ -340,6 +367,7 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
           }
         }
       }
+      if constexpr (SWAP) grid_launch_dependents();
       if (resid_early && it > 0) {
         // The residual load lands before the CTA exits, whether or not this CTA
         // finishes the tile.

@@ -121,8 +121,18 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   const int v_lo = kb / 8 + (warp * nvec) / kCcWarps;
   const int v_hi = kb / 8 + ((warp + 1) * nvec) / kCcWarps;
   const int tail_k = kb + nvec * 8;  // [tail_k, ke): fewer than 8 elements, warp 0
-  grid_launch_dependents();
-  grid_dependency_wait();  // no global access before the previous kernel has completed
+  if (p.prewait && lane < R && v_hi > v_lo) {
+    // The first row pass's weights of this warp's k range, pulled into L2 while
+    // the previous launch may still be finishing (a hint: L2 is the point of
+    // coherence, so nothing read here can be stale once the wait returns).
+    const int r = lane;
+    const int n = row_lo + (GATED ? r / 2 : r);
+    if (n < row_hi) {
+      const uint16_t* row = GATED ? ((r & 1) ? p.B2 : p.B) + static_cast<int64_t>(n) * p.ldb : weight_row(p, n);
+      bulk_prefetch_l2(row + 8 * v_lo, static_cast<uint32_t>(v_hi - v_lo) * 16u);
+    }
+  }
+  grid_dependency_wait();  // no global load before the previous kernel has completed
 
   static_assert(R % 2 == 0, "weight rows are processed in pairs");
   // Without a K split, each thread's outputs are known from the start: elements
@@ -138,6 +148,9 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     }
   }
   for (int r0 = row_lo; r0 < row_hi; r0 += kRowStep) {
+    // The next launch may start its set-up (and early prefetch) once every CTA is
+    // on its last row pass.
+    if (r0 + kRowStep >= row_hi) grid_launch_dependents();
     // acc[r / 2][m] holds the fp32 sums of weight rows r (x) and r + 1 (y) for
     // activation row m; one paired FMA updates both.
     float2 acc[R / 2][MT];

@@ -47,6 +47,11 @@ constexpr int skinny_stages_gated(int bn) {
 // Smallest K range a split piece of the skinny path gets (each piece's partial
 // sum is written, counted and read back once).
 constexpr int kSkinnyMinPieceK = 512;
+// Swapped skinny kernel: k-steps of weights each CTA pulls into L2 before it waits
+// for the previous launch in the stream, when the grid holds at least
+// kPreWaitMinFill tenths of the resident slots.
+constexpr int kPreWaitSteps = 8;
+constexpr int kPreWaitMinFill = 7;
 // tcgen05 kernels: warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps.
 
 // Everything a tcgen05 launch needs besides its tensor maps.
@@ -66,6 +71,9 @@ struct TcParams {
   // belong to matrix i, read through batch maps w[i] and stored through c[i].
   int32_t nbatch;
   int32_t tile_begin[kMaxBatch + 1];
+  // Swapped kernel: k-steps of its first weight tile each CTA prefetches into L2
+  // before it waits for the previous launch.
+  int32_t prewait_steps;
 };
 
 // Tensor maps of a batched swapped launch: matrix i's weights and output.
@@ -129,6 +137,9 @@ struct CcParams {
   uint16_t* Cs[kMaxBatch];
   int64_t ldbs[kMaxBatch];
   int64_t ldcs[kMaxBatch];
+  // Non-zero: each warp prefetches its k range of the CTA's first row pass into L2
+  // before it waits for the previous launch.
+  int32_t prewait;
 };
 
 cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream);

@@ -211,6 +211,16 @@ def test_skinny_tensor_core_plan(lib, M, N, K):
             assert info["sk_tiles"] == T % 304  # only the remainder is split
     # the weights are read once: each weight tile's k-steps are covered exactly once
     assert sum(k1 - k0 for row in items for (_, k0, k1, *_) in row) == info["tiles_m"] * info["k_steps"]
+    # early L2 reads of the first 8 k-steps only when the grid fills 70% of the slots
+    assert info["prefetch_steps"] == (8 if info["grid"] * 10 >= 7 * 304 else 0)
+
+
+def test_prefetch_only_on_skinny_paths(lib):
+    assert sg.plan(4096, 4096, 4096, 152, 0)["prefetch_steps"] == 0
+    assert sg.plan(128, 4096, 4096, 152, 0)["prefetch_steps"] == 0
+    assert sg.plan(16, 11008, 4096, 152, 0)["prefetch_steps"] == 0  # 172 CTAs on 304 slots
+    assert sg.plan(16, 4096, 11008, 152, 0)["prefetch_steps"] == 8  # 64 tiles x 4 pieces
+    assert sg.plan(1, 11008, 4096, 152, 0)["prefetch_steps"] == 1
 
 
 def test_auto_path_choice(lib):
@@ -234,6 +244,7 @@ def test_cuda_core_plan(lib, N, K):
     assert info["grid"] == blocks * info["split_k"]
     if blocks >= 304:
         assert info["split_k"] == 1
+    assert info["prefetch_steps"] == (1 if info["grid"] * 10 >= 7 * 304 else 0)
     # every row belongs to exactly one block: [b*N/blocks, (b+1)*N/blocks)
     bounds = [(b * N) // blocks for b in range(blocks + 1)]
     assert bounds[0] == 0 and bounds[-1] == N and all(x < y for x, y in zip(bounds, bounds[1:]))
