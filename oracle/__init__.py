@@ -13,6 +13,11 @@ gemm_sampled(A, B, rows, cols) the same sum at the intersections rows x cols
 silu(x)                        x * sigmoid(x) = x / (1 + exp(-x)), fp64
 swiglu(A, Wg, Wu)              silu(A . Wg^T) * (A . Wu^T), fp64 (gated MLP)
 gemm_residual(A, B, R)         A . B^T + R, fp64 (a projection with its residual add)
+e2m1_value(codes)              fp64 values of E2M1 (FP4) codes
+e4m3_value(codes)              fp64 values of E4M3 (FP8) codes
+nvfp4_dequant(P, S, K)         packed FP4 rows times their 16-element block scales, fp64
+gemm_nvfp4(A, SFA, B, SFB, K)  alpha * dequant(A) . dequant(B)^T in fp64 (NVFP4 GEMM)
+gemm_nvfp4_sampled(...)        the same at chosen rows x columns
 build()                        compile the C oracle (idempotent)
 
 A and B are uint16 arrays of bf16 bit patterns, A[M, lda] and B[N, ldb]; the
@@ -134,3 +139,71 @@ def gemm_residual(A: np.ndarray, B: np.ndarray, R: np.ndarray, K: int | None = N
     (or wider-pitched [M, ldr]) array of bf16 bit patterns (first N columns)."""
     C = gemm(A, B, K=K, threads=threads)
     return C + _bf16_to_f64(R)[:, :C.shape[1]]
+
+
+# ------------------------------------------------------------------ NVFP4
+# The dense W4A4 GEMM of the gemm3 benchmarks page ("Implementations": packed
+# NVFP4 operands, E4M3 scales over 16-element blocks, alpha): each element is an
+# E2M1 code times the E4M3 scale of its block, and the GEMM is the plain sum of
+# their products, here in fp64 after decoding every code exactly.
+
+def e2m1_value(codes) -> np.ndarray:
+    """E2M1 (FP4): bit 3 sign, bits 2-1 exponent e (bias 1), bit 0 mantissa m.
+    e = 0 is subnormal, m * 2**-1; otherwise (1 + m/2) * 2**(e - 1).  There is no
+    infinity or NaN: the largest magnitude is 6."""
+    c = np.asarray(codes).astype(np.int64) & 0xF
+    sign = np.where((c >> 3) & 1, -1.0, 1.0)
+    e = (c >> 1) & 3
+    m = (c & 1).astype(np.float64)
+    mag = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e - 1.0))
+    return sign * mag
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """E4M3 (FP8, the variant with no infinities): bit 7 sign, bits 6-3 exponent e
+    (bias 7), bits 2-0 mantissa m.  e = 0 is subnormal, (m/8) * 2**-6; e = 15 with
+    m = 7 is NaN; otherwise (1 + m/8) * 2**(e - 7), up to 448."""
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def nvfp4_unpack(packed: np.ndarray, K: int) -> np.ndarray:
+    """E2M1 codes [rows, K] of packed rows: element k is in byte k // 2, the low
+    nibble for even k and the high nibble for odd k."""
+    b = np.ascontiguousarray(packed, dtype=np.uint8)[:, :K // 2].astype(np.int64)
+    out = np.empty((b.shape[0], K), dtype=np.int64)
+    out[:, 0::2] = b & 0xF
+    out[:, 1::2] = b >> 4
+    return out
+
+
+def nvfp4_dequant(packed: np.ndarray, scales: np.ndarray, K: int) -> np.ndarray:
+    """fp64 values x[r, k] = e2m1(code[r, k]) * e4m3(scale[r, k // 16]); `scales` is
+    plain row-major, one code per 16 elements (first K // 16 columns)."""
+    assert K % 16 == 0
+    v = e2m1_value(nvfp4_unpack(packed, K))
+    s = e4m3_value(np.asarray(scales)[:, :K // 16])
+    return v * np.repeat(s, 16, axis=1)
+
+
+def gemm_nvfp4(A: np.ndarray, SFA: np.ndarray, B: np.ndarray, SFB: np.ndarray, K: int,
+               alpha: float = 1.0) -> np.ndarray:
+    """C[m, n] = alpha * sum_k a[m, k] sa[m, k // 16] b[n, k] sb[n, k // 16] in fp64,
+    not rounded to fp16.  A [M, >= K/2] and B [N, >= K/2] are packed codes, SFA and
+    SFB plain row-major scale codes.  The sum over k is numpy's fp64 matmul of the
+    decoded values (every product is exact in fp64)."""
+    return float(alpha) * (nvfp4_dequant(A, SFA, K) @ nvfp4_dequant(B, SFB, K).T)
+
+
+def gemm_nvfp4_sampled(A, SFA, B, SFB, rows, cols, K: int, alpha: float = 1.0) -> np.ndarray:
+    """gemm_nvfp4 at the intersections rows x cols only."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    a = nvfp4_dequant(np.asarray(A)[rows], np.asarray(SFA)[rows], K)
+    b = nvfp4_dequant(np.asarray(B)[cols], np.asarray(SFB)[cols], K)
+    return float(alpha) * (a @ b.T)

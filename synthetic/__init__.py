@@ -271,3 +271,77 @@ def sample_indices(extent: int, count: int, seed: int) -> np.ndarray:
         return np.arange(extent, dtype=np.int64)
     keys = splitmix64(seed, 0, extent)
     return np.sort(np.argsort(keys, kind="stable")[:count]).astype(np.int64)
+
+
+# ------------------------------------------------------------------ NVFP4 inputs
+# Packed FP4 operands and their E4M3 block scales, drawn as raw codes: every byte
+# of a packed row is uniform over 0..255 (two uniform E2M1 codes, signed zeros
+# included), every scale code uniform over 0x28..0x3F (E4M3 values 0.25 .. 1.875),
+# so sums over K = 4096 stay far inside the fp16 output range.  The pages give no
+# distribution for their NVFP4 operands; this is the plain reading.
+NVFP4_SCALE_LO = 0x28
+NVFP4_SCALE_HI = 0x3F
+
+
+def nvfp4_codes(rows: int, K: int, seed: int, ld: int | None = None) -> np.ndarray:
+    """rows x ld bytes: the first K/2 of each row hold K packed E2M1 codes; padding
+    bytes are 0xFF (a pair of -6 codes, so a kernel that reads padding shows it)."""
+    assert K % 2 == 0
+    ld = K // 2 if ld is None else ld
+    assert ld >= K // 2
+    core = (splitmix64(seed, 0, rows * (K // 2)) >> np.uint64(56)).astype(np.uint8).reshape(rows, K // 2)
+    if ld == K // 2:
+        return core
+    out = np.full((rows, ld), 0xFF, dtype=np.uint8)
+    out[:, :K // 2] = core
+    return out
+
+
+def nvfp4_scales(rows: int, K: int, seed: int, ld: int | None = None) -> np.ndarray:
+    """rows x ld plain row-major E4M3 scale codes, one per 16 elements of K."""
+    assert K % 16 == 0
+    nblk = K // 16
+    ld = nblk if ld is None else ld
+    span = NVFP4_SCALE_HI - NVFP4_SCALE_LO + 1
+    u = splitmix64(seed, 1 << 40, rows * nblk) >> np.uint64(32)
+    core = (NVFP4_SCALE_LO + (u % np.uint64(span))).astype(np.uint8).reshape(rows, nblk)
+    out = np.zeros((rows, ld), dtype=np.uint8)
+    out[:, :nblk] = core
+    return out
+
+
+@dataclasses.dataclass(frozen=True)
+class Nvfp4Workload:
+    """C[M,N] = alpha (A . SFA) . (B . SFB)^T with packed NVFP4 operands, E4M3
+    scales over 16-element blocks and FP16 output: the square shapes of the gemm3
+    benchmarks page (4096^3 .. 32768^3) and a small one the oracle finishes fast."""
+    name: str
+    M: int
+    N: int
+    K: int
+    cfg: int
+    alpha: float = 1.0
+
+    def a(self) -> np.ndarray:
+        return nvfp4_codes(self.M, self.K, SEED_A_BASE + self.cfg)
+
+    def b(self) -> np.ndarray:
+        return nvfp4_codes(self.N, self.K, SEED_B_BASE + self.cfg)
+
+    def sfa(self) -> np.ndarray:
+        return nvfp4_scales(self.M, self.K, SEED_A_BASE + 500 + self.cfg)
+
+    def sfb(self) -> np.ndarray:
+        return nvfp4_scales(self.N, self.K, SEED_B_BASE + 500 + self.cfg)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+NVFP4_WORKLOADS = {w.name: w for w in [
+    Nvfp4Workload("fp4_sq512", 512, 512, 512, 60),
+    Nvfp4Workload("fp4_sq4096", 4096, 4096, 4096, 61),
+    Nvfp4Workload("fp4_sq8192", 8192, 8192, 8192, 62),
+    Nvfp4Workload("fp4_sq16384", 16384, 16384, 16384, 63),
+]}
