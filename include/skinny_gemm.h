@@ -190,6 +190,60 @@ SG_API int gemv_bf16_batched(const void *A, int64_t M, int64_t K, int64_t lda,
                       void *const *C, const int64_t *ldc, int count, int path, sg_stream_t stream);
 
 /*
+ * gemm_nvfp4 -- dense W4A4 block-scaled GEMM with FP16 output:
+ *
+ *   C[m, n] = alpha * sum_k a[m, k] sa[m, k/16] b[n, k] sb[n, k/16]
+ *
+ * the operation the gemm3 benchmarks page times ("Implementations": packed NVFP4
+ * operands, E4M3 scales over 16-element blocks, alpha = 1, FP16 output), on the
+ * tcgen05 block-scaled MMA.
+ *
+ * Operands (device pointers):
+ *   A    M rows of K/2 bytes, pitch lda bytes: element a[m, k] is the E2M1 code in
+ *        byte k/2 of row m, the low nibble for even k (E2M1: sign, 2 exponent bits
+ *        with bias 1, 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6).
+ *   B    N rows of K/2 bytes, pitch ldb bytes, the same encoding (a weight matrix
+ *        [out, in], as for gemm_bf16).
+ *   SFA  E4M3 scales of A in scale atoms (below); sa[m, j] scales a[m, 16j .. 16j+15].
+ *   SFB  E4M3 scales of B in scale atoms.
+ *   C    M x N fp16 (IEEE binary16 bit patterns), pitch ldc elements.
+ * A scale atom is 512 bytes holding 128 rows x 4 blocks (64 of K): row r, block j
+ * at byte (r % 32) * 16 + (r / 32) * 4 + j.  For a matrix of `rows` rows, atom
+ * (row block R, k chunk c) sits at byte (R * ceil(K/64) + c) * 512 of its buffer,
+ * nvfp4_scale_bytes(rows, K) bytes in all.  nvfp4_pack_scales builds this layout
+ * from plain row-major scales.  Atom bytes past K/16 blocks or past the last row
+ * must hold finite scales (nvfp4_pack_scales writes 0): the kernel multiplies them
+ * by zero-filled operands, and a NaN scale would make the product NaN.
+ *
+ * Arithmetic: every product is exact in fp32 (at most 12 significant bits), the
+ * sums are fp32 in an unspecified order, then multiplied by alpha and rounded to
+ * fp16 (nearest even).  Results are the same on every run.
+ *
+ * Requirements: K a multiple of 16; lda, ldb >= K/2 and multiples of 16; ldc >= N
+ * and a multiple of 8; A, B, SFA, SFB, C 16-byte aligned.  Errors: SG_ERR_INVALID_ARG
+ * (negative or too large sizes, K % 16 != 0, short pitches, null pointers),
+ * SG_ERR_MISALIGNED, SG_ERR_UNSUPPORTED_DEVICE, SG_ERR_CUDA, SG_ERR_TIMEOUT (on
+ * the next sg_check_device_errors).  M = 0 or N = 0: no work.  K = 0: C := 0.
+ * Asynchronous on `stream`; graph-capturable after a first call.
+ */
+SG_API int gemm_nvfp4(const void *A, const void *SFA, const void *B, const void *SFB, void *C,
+                      int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                      float alpha, sg_stream_t stream);
+
+/* Bytes of a scale-atom buffer for `rows` rows and K elements of K (-1 if negative). */
+SG_API int64_t nvfp4_scale_bytes(int64_t rows, int64_t K);
+
+/*
+ * nvfp4_pack_scales -- the repacking step: plain row-major E4M3 scales (rows x
+ * K/16 bytes, pitch ld bytes) to the scale atoms gemm_nvfp4 reads
+ * (nvfp4_scale_bytes(rows, K) bytes; padding written as 0).  One kernel on
+ * `stream`; device pointers.  Errors: SG_ERR_INVALID_ARG (negative sizes,
+ * K % 16 != 0, ld < K/16, null pointers when rows * K > 0), SG_ERR_CUDA.
+ */
+SG_API int nvfp4_pack_scales(const void *plain, int64_t rows, int64_t K, int64_t ld, void *atoms,
+                             sg_stream_t stream);
+
+/*
  * gemv_bf16_noalloc -- gemv_bf16 on the CUDA-core kernel (SG_PATH_CUDA_CORE),
  * for callers that cannot allocate device memory.  The pages have no
  * counterpart: this entry point exists for integration, not for the method.
@@ -310,6 +364,10 @@ SG_API int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t ent
  * tile_n gate and tile_n up weight rows); tensor-core skinny plans: tile_m
  * counts outputs (each from one gate and one up weight row). */
 SG_API int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
+
+/* The plan gemm_nvfp4 uses: 128 x 256 tiles, 256 of K per stage, whole tiles
+ * round-robin over one CTA per SM (tile_k counts fp4 elements). */
+SG_API int sg_plan_nvfp4(int64_t M, int64_t N, int64_t K, int32_t num_sms, sg_plan_info *out);
 
 /*
  * sg_plan_item -- work item `index` of CTA `cta` under a tcgen05 plan from sg_plan:

@@ -105,6 +105,14 @@ def load(build_if_missing: bool = False):
     pp, p64 = ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int64)
     lib.gemv_bf16_batched.argtypes = [p, i64, i64, i64, pp, p64, p64, pp, p64, ctypes.c_int, ctypes.c_int, p]
     lib.gemv_bf16_batched.restype = ctypes.c_int
+    lib.gemm_nvfp4.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_float, p]
+    lib.gemm_nvfp4.restype = ctypes.c_int
+    lib.nvfp4_scale_bytes.argtypes = [i64, i64]
+    lib.nvfp4_scale_bytes.restype = i64
+    lib.nvfp4_pack_scales.argtypes = [p, i64, i64, i64, p, p]
+    lib.nvfp4_pack_scales.restype = ctypes.c_int
+    lib.sg_plan_nvfp4.argtypes = [i64, i64, i64, i32, ctypes.POINTER(PlanInfo)]
+    lib.sg_plan_nvfp4.restype = ctypes.c_int
     lib.sg_status_string.argtypes = [ctypes.c_int]
     lib.sg_status_string.restype = ctypes.c_char_p
     lib.sg_last_cuda_error.argtypes = []
@@ -266,6 +274,65 @@ def gemm_bf16_residual(A, B, R, C=None, stream=None, path: int = PATH_AUTO):
     return C
 
 
+def _bytes_operand(t, name: str):
+    torch = _torch()
+    if t.dtype != torch.uint8 or t.dim() != 2 or not t.is_cuda:
+        raise ValueError(f"{name} must be a 2-D uint8 CUDA tensor, got {t.dtype} {tuple(t.shape)} {t.device}")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    return t.data_ptr(), max(t.stride(0), t.shape[1])
+
+
+def nvfp4_scale_bytes(rows: int, K: int) -> int:
+    """Bytes of the scale-atom buffer gemm_nvfp4 reads for `rows` rows."""
+    return int(load().nvfp4_scale_bytes(rows, K))
+
+
+def nvfp4_pack_scales(plain, K: int | None = None, atoms=None, stream=None):
+    """Plain row-major E4M3 scale codes (uint8 [rows, >= K/16]) to the scale atoms
+    gemm_nvfp4 reads (a flat uint8 tensor); padding is written as 0."""
+    torch = _torch()
+    p_ptr, ld = _bytes_operand(plain, "plain")
+    rows = plain.shape[0]
+    K = 16 * plain.shape[1] if K is None else K
+    n = nvfp4_scale_bytes(rows, K)
+    if atoms is None:
+        atoms = torch.empty(max(n, 1), dtype=torch.uint8, device=plain.device)
+    if atoms.dtype != torch.uint8 or not atoms.is_cuda or atoms.numel() < n or not atoms.is_contiguous():
+        raise ValueError(f"atoms must be a contiguous uint8 CUDA tensor of at least {n} bytes")
+    with torch.cuda.device(plain.device):
+        st = load().nvfp4_pack_scales(p_ptr, rows, K, ld, atoms.data_ptr(), _stream_handle(stream))
+    _check(st, "nvfp4_pack_scales")
+    return atoms
+
+
+def gemm_nvfp4(A, SFA, B, SFB, K: int | None = None, C=None, alpha: float = 1.0, stream=None):
+    """C[M, N] (fp16) = alpha * (A . SFA) @ (B . SFB)^T for packed E2M1 operands
+    (uint8 [M, >= K/2] and [N, >= K/2]) and their E4M3 scale atoms (from
+    nvfp4_pack_scales)."""
+    torch = _torch()
+    a_ptr, lda = _bytes_operand(A, "A")
+    b_ptr, ldb = _bytes_operand(B, "B")
+    M, N = A.shape[0], B.shape[0]
+    K = 2 * A.shape[1] if K is None else K
+    if 2 * A.shape[1] < K or 2 * B.shape[1] < K:
+        raise ValueError(f"K = {K} needs {K // 2} bytes per row: A {tuple(A.shape)}, B {tuple(B.shape)}")
+    for t, rows, name in ((SFA, M, "SFA"), (SFB, N, "SFB")):
+        if t.dtype != torch.uint8 or not t.is_cuda or t.numel() < nvfp4_scale_bytes(rows, K):
+            raise ValueError(f"{name} must hold nvfp4_scale_bytes({rows}, {K}) uint8 scale-atom bytes")
+    if C is None:
+        ld = -(-N // 8) * 8
+        C = torch.empty((M, ld), dtype=torch.float16, device=A.device)[:, :N]
+    if C.dtype != torch.float16 or tuple(C.shape) != (M, N) or not C.is_cuda or (N > 1 and C.stride(1) != 1):
+        raise ValueError(f"C must be a float16 CUDA tensor of shape {(M, N)}")
+    ldc = max(C.stride(0), N)
+    with torch.cuda.device(A.device):
+        st = load().gemm_nvfp4(a_ptr, SFA.data_ptr(), b_ptr, SFB.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc,
+                               float(alpha), _stream_handle(stream))
+    _check(st, "gemm_nvfp4")
+    return C
+
+
 def gemv_bf16_batched(A, Bs, Cs=None, stream=None, path: int = PATH_AUTO):
     """C_i = A @ B_i^T for every weight B_i (all [N_i, K]) in one launch; returns
     the list of C_i."""
@@ -309,6 +376,14 @@ def gemv_bf16_noalloc(A, B, C=None, stream=None):
 def plan(M: int, N: int, K: int, num_sms: int, entry: int = 0) -> dict:
     info = PlanInfo()
     _check(load().sg_plan(M, N, K, num_sms, entry, ctypes.byref(info)), "sg_plan")
+    d = info.as_dict()
+    d["_struct"] = info
+    return d
+
+
+def plan_nvfp4(M: int, N: int, K: int, num_sms: int) -> dict:
+    info = PlanInfo()
+    _check(load().sg_plan_nvfp4(M, N, K, num_sms, ctypes.byref(info)), "sg_plan_nvfp4")
     d = info.as_dict()
     d["_struct"] = info
     return d

@@ -133,9 +133,10 @@ struct MapKey {
   uint64_t cols, rows, ld;
   uint32_t box_cols, box_rows, swizzle;
   int dev;
+  uint32_t elem_bytes;  // 2: bf16 / fp16 elements, 1: bytes (packed fp4)
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && cols == o.cols && rows == o.rows && ld == o.ld && box_cols == o.box_cols &&
-           box_rows == o.box_rows && swizzle == o.swizzle && dev == o.dev;
+           box_rows == o.box_rows && swizzle == o.swizzle && dev == o.dev && elem_bytes == o.elem_bytes;
   }
 };
 
@@ -151,9 +152,11 @@ int g_map_used = 0, g_map_next = 0;
 
 // A 2-D bf16 tensor of `rows` rows x `cols` columns with a row pitch of `ld`
 // elements, read or written in boxes of box_rows x box_cols.
+// 2-D tensor map of a row-major matrix of 16-bit elements (elem_bytes 2) or of
+// bytes (elem_bytes 1); cols, ld and box_cols count elements.
 int make_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows,
-             uint32_t box_cols, CUtensorMapSwizzle swz, int dev) {
-  const MapKey key{ptr, cols, rows, ld, box_cols, box_rows, static_cast<uint32_t>(swz), dev};
+             uint32_t box_cols, CUtensorMapSwizzle swz, int dev, uint32_t elem_bytes = 2) {
+  const MapKey key{ptr, cols, rows, ld, box_cols, box_rows, static_cast<uint32_t>(swz), dev, elem_bytes};
   {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (int i = 0; i < g_map_used; ++i)
@@ -165,11 +168,12 @@ int make_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, ui
   EncodeTiledFn enc = get_encoder();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint64_t strides[1] = {ld * elem_bytes};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
-  const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  const CUresult r = enc(&m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
@@ -567,6 +571,57 @@ int run_batched(DeviceState& d, int dev, const void* A, int64_t M, int64_t K, in
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
+// NVFP4 plan: 128 x 256 tiles, 256 of K per stage, whole tiles round-robin over
+// one CTA per SM in a grouped raster.
+void plan_nvfp4(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+  std::memset(o, 0, sizeof *o);
+  o->path = SG_PATH_GEMM;
+  o->tile_m = kF4TileM;
+  o->tile_n = kF4TileN;
+  o->tile_k = kF4StageK;
+  o->stages = kF4Stages;
+  o->cluster_size = 1;
+  o->ctas_per_sm = 1;
+  Schedule s{};
+  s.tiles_m = static_cast<int32_t>(ceil_div(M, kF4TileM));
+  s.tiles_n = static_cast<int32_t>(ceil_div(N, kF4TileN));
+  s.k_steps = static_cast<int32_t>(ceil_div(K, kF4StageK));
+  s.group_m = std::max<int32_t>(1, std::min<int32_t>(s.tiles_m, 8));
+  const int64_t T = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
+  s.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(T, sms)));
+  s.dp_tiles = static_cast<int32_t>(T);
+  fill_sched(o, s);
+  o->split_k = 0;
+  o->wave_efficiency = wave_efficiency(T, sms);
+}
+
+int run_nvfp4(DeviceState& d, int dev, const void* A, const void* SFA, const void* B, const void* SFB, void* C,
+              int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, float alpha,
+              cudaStream_t stream) {
+  sg_plan_info plan;
+  plan_nvfp4(M, N, K, d.sm_count, &plan);
+  CUtensorMap ta, tb;
+  int st = make_map(&ta, A, M, K / 2, lda, kF4TileM, 128, CU_TENSOR_MAP_SWIZZLE_128B, dev, 1);
+  if (st == SG_OK) st = make_map(&tb, B, N, K / 2, ldb, kF4TileN, 128, CU_TENSOR_MAP_SWIZZLE_128B, dev, 1);
+  if (st != SG_OK) return st;
+  F4Params p{};
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.kc = static_cast<int32_t>(ceil_div(K, 64));
+  p.rb_n = static_cast<int32_t>(ceil_div(N, 128));
+  p.ldc = ldc;
+  p.C = static_cast<uint16_t*>(C);
+  p.SFA = static_cast<const uint8_t*>(SFA);
+  p.SFB = static_cast<const uint8_t*>(SFB);
+  p.alpha = alpha;
+  p.sched = sched_from_plan(plan);
+  p.err = d.err;
+  p.timeout_ns = g_timeout_ns.load();
+  const cudaError_t e = launch_f4_gemm(ta, tb, p, stream);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
 // C := 0 (no residual) or C := R, the value of an empty sum plus the residual.
 int empty_sum(void* C, int64_t M, int64_t N, int64_t ldc, const void* R, int64_t ldr, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
@@ -694,6 +749,51 @@ int gemm_bf16_swiglu_path(const void* A, const void* Wg, const void* Wu, void* C
 int gemm_bf16_swiglu(const void* A, const void* Wg, const void* Wu, void* C, int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldw, int64_t ldc, sg_stream_t stream) {
   return gemm_bf16_swiglu_path(A, Wg, Wu, C, M, N, K, lda, ldw, ldc, SG_PATH_AUTO, stream);
+}
+
+int64_t nvfp4_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return -1;
+  return ceil_div(rows, 128) * ceil_div(K, 64) * kF4AtomBytes;
+}
+
+int nvfp4_pack_scales(const void* plain, int64_t rows, int64_t K, int64_t ld, void* atoms, sg_stream_t stream) {
+  if (rows < 0 || K < 0 || K % 16 != 0 || ld < K / 16) return SG_ERR_INVALID_ARG;
+  if (rows == 0 || K == 0) return SG_OK;
+  if (!plain || !atoms) return SG_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  const int st = current_device_state(&d, nullptr);
+  if (st != SG_OK) return st;
+  const cudaError_t e = launch_f4_pack_scales(static_cast<const uint8_t*>(plain), rows, K, ld,
+                                              static_cast<uint8_t*>(atoms), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
+int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int64_t M, int64_t N,
+               int64_t K, int64_t lda, int64_t ldb, int64_t ldc, float alpha, sg_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return SG_ERR_INVALID_ARG;
+  if (K % 16 != 0) return SG_ERR_INVALID_ARG;  // whole 16-element scale blocks
+  if (M == 0 || N == 0) return SG_OK;
+  if (!C || (K > 0 && (!A || !B || !SFA || !SFB))) return SG_ERR_INVALID_ARG;
+  if (ldc < N || lda < K / 2 || ldb < K / 2) return SG_ERR_INVALID_ARG;
+  auto misaligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+  if (misaligned(C) || (ldc & 7)) return SG_ERR_MISALIGNED;
+  if (K > 0 && (misaligned(A) || misaligned(B) || misaligned(SFA) || misaligned(SFB) || (lda & 15) || (ldb & 15)))
+    return SG_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState* d = nullptr;
+  int dev = 0;
+  int st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  if (K == 0) return empty_sum(C, M, N, ldc, nullptr, 0, s);  // +0.0 in fp16 is all zero bits
+  st = ensure_workspace(*d, s);
+  if (st != SG_OK) return st;
+  return run_nvfp4(*d, dev, A, SFA, B, SFB, C, M, N, K, lda, ldb, ldc, alpha, s);
+}
+
+int sg_plan_nvfp4(int64_t M, int64_t N, int64_t K, int32_t num_sms, sg_plan_info* out) {
+  if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
+  plan_nvfp4(M, N, K, num_sms, out);
+  return SG_OK;
 }
 
 int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info* out) {

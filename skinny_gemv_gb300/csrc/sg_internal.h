@@ -144,6 +144,39 @@ struct CcParams {
 
 cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- NVFP4 GEMM
+// Tiles of 128 x 256 outputs; a stage is 256 fp4 of K (128 bytes per row, 4 MMAs
+// of K = 64) with its scale atoms.  A scale atom is 512 bytes holding the E4M3
+// scales of 128 rows x 4 blocks of 16 (64 of K): row r, block j at byte
+// (r % 32) * 16 + (r / 32) * 4 + j; atom (row block R, k chunk c) of a matrix with
+// kc = ceil(K / 64) chunks sits at byte (R * kc + c) * 512.
+constexpr int kF4TileM = 128;
+constexpr int kF4TileN = 256;
+constexpr int kF4StageK = 256;
+constexpr int kF4Stages = 4;
+constexpr int kF4AtomBytes = 512;
+
+struct F4Params {
+  int32_t M, N, K;
+  int32_t kc;            // 64-element k chunks: ceil(K / 64)
+  int32_t rb_n;          // 128-row blocks of B: ceil(N / 128)
+  int64_t ldc;           // elements
+  uint16_t* C;           // fp16 bit patterns
+  const uint8_t* SFA;    // scale atoms of A (ceil(M / 128) * kc of them)
+  const uint8_t* SFB;    // scale atoms of B (rb_n * kc of them)
+  float alpha;
+  Schedule sched;        // whole tiles, round-robin
+  DeviceError* err;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_f4_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const F4Params& p, cudaStream_t stream);
+
+// Plain row-major scales (rows x K/16 bytes, pitch ld) to scale atoms; padding
+// bytes (rows past `rows`, blocks past K/16) are written as 0.
+cudaError_t launch_f4_pack_scales(const uint8_t* plain, int64_t rows, int64_t K, int64_t ld, uint8_t* atoms,
+                                  cudaStream_t stream);
+
 // Dynamic shared memory of the CUDA-core kernel for M rows over grid_rows row blocks.
 int cc_smem_bytes(int64_t M, int64_t N, int grid_rows, bool gated = false);
 

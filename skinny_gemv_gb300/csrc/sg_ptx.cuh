@@ -273,6 +273,29 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= (A . SFA) . (B . SFB)^T for packed FP4 (E2M1) operands with one
+// E4M3 scale per 16 elements of K (kind::mxf4nvf4, scale_vec::4X), fp32 D, one
+// CTA, K = 64 per instruction.  Scale row r of A is read from TMEM lane r, column
+// sfa + r / 32 (byte j: k block j); scale row n of B from column sfb + n / 32 of
+// the lane n % 32 in every lane quarter.
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies 32 rows x 16 bytes of shared memory (described by `sdesc`) into TMEM
+// lanes 0-31 at columns [col, col + 4) and repeats them in the other three lane
+// quarters: lane l + 32 q, column col + t holds bytes 4t .. 4t + 3 of row l.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed (the MMA's reads of shared memory included).
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -422,6 +445,27 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr) {
   d |= static_cast<uint64_t>(1u) << 46;
   d |= static_cast<uint64_t>(2u) << 61;
   return d;
+}
+
+// Shared-memory descriptor of an unswizzled tile of 16-byte rows stored one
+// after another (8-row core matrices 128 B apart), the source layout of
+// tc_cp_32x128b_warpx4.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;  // layout 0: no swizzle
+}
+
+// Instruction descriptor for kind::mxf4nvf4 (E2M1 A and B, E4M3 scales, fp32 D),
+// both operands K-major, dense:
+//   bits 7-9 A format (1 = E2M1), 10-12 B format (1 = E2M1), 15/16 A/B major
+//   (0 = K), 17-22 N >> 3, 23 scale format (0 = E4M3), 24-28 M >> 4; the scale
+//   data IDs (bits 4-5 and 29-30) are 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4_f32(uint32_t m, uint32_t n) {
+  return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 D, both operands

@@ -282,3 +282,50 @@ def test_swiglu_path_choice(lib):
     out = sg.PlanInfo()
     assert lib.sg_plan_swiglu(65, 8, 8, 152, sg.PATH_TENSOR_CORE, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
     assert lib.sg_plan_swiglu(8, 8, 8, 152, 7, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ NVFP4
+@pytest.mark.parametrize("args,code", [
+    # (A, SFA, B, SFB, C, M, N, K, lda, ldb, ldc)
+    ((16, 16, 16, 16, 16, 8, 8, 24, 16, 16, 8), sg.SG_ERR_INVALID_ARG),   # K % 16
+    ((16, 16, 16, 16, 16, -1, 8, 32, 16, 16, 8), sg.SG_ERR_INVALID_ARG),  # negative M
+    ((16, 16, 16, 16, 0, 8, 8, 32, 16, 16, 8), sg.SG_ERR_INVALID_ARG),    # null C
+    ((16, 0, 16, 16, 16, 8, 8, 32, 16, 16, 8), sg.SG_ERR_INVALID_ARG),    # null SFA
+    ((16, 16, 16, 16, 16, 8, 8, 64, 16, 32, 8), sg.SG_ERR_INVALID_ARG),   # lda < K/2
+    ((16, 16, 16, 16, 16, 8, 16, 32, 16, 16, 8), sg.SG_ERR_INVALID_ARG),  # ldc < N
+    ((24, 16, 16, 16, 16, 8, 8, 32, 16, 16, 8), sg.SG_ERR_MISALIGNED),    # A
+    ((16, 20, 16, 16, 16, 8, 8, 32, 16, 16, 8), sg.SG_ERR_MISALIGNED),    # SFA
+    ((16, 16, 16, 16, 16, 8, 8, 32, 24, 16, 8), sg.SG_ERR_MISALIGNED),    # lda % 16
+    ((16, 16, 16, 16, 16, 8, 8, 32, 16, 16, 12), sg.SG_ERR_MISALIGNED),   # ldc % 8
+])
+def test_nvfp4_argument_errors_before_any_cuda_call(lib, args, code):
+    assert lib.gemm_nvfp4(*args, 1.0, None) == code
+
+
+def test_nvfp4_empty_is_noop(lib):
+    assert lib.gemm_nvfp4(None, None, None, None, None, 0, 8, 32, 16, 16, 8, 1.0, None) == sg.SG_OK
+    assert lib.gemm_nvfp4(None, None, None, None, None, 8, 0, 32, 16, 16, 8, 1.0, None) == sg.SG_OK
+    assert lib.nvfp4_pack_scales(None, 0, 64, 4, None, None) == sg.SG_OK
+    assert lib.nvfp4_pack_scales(None, 8, 24, 4, None, None) == sg.SG_ERR_INVALID_ARG  # K % 16
+    assert lib.nvfp4_pack_scales(None, 8, 64, 3, None, None) == sg.SG_ERR_INVALID_ARG  # ld < K/16
+
+
+def test_nvfp4_scale_bytes(lib):
+    assert sg.nvfp4_scale_bytes(1, 16) == 512
+    assert sg.nvfp4_scale_bytes(128, 64) == 512
+    assert sg.nvfp4_scale_bytes(129, 64) == 1024
+    assert sg.nvfp4_scale_bytes(4096, 4096) == 32 * 64 * 512
+    assert sg.nvfp4_scale_bytes(300, 1040) == 3 * 17 * 512
+    assert sg.nvfp4_scale_bytes(0, 64) == 0 and sg.nvfp4_scale_bytes(-1, 64) == -1
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 8192, 8192), (300, 500, 1040), (1, 1, 16),
+                                   (128, 256, 256), (16384, 16384, 16384)])
+def test_nvfp4_plan_covers_every_tile_once(lib, M, N, K):
+    info = sg.plan_nvfp4(M, N, K, 152)
+    assert (info["tile_m"], info["tile_n"], info["tile_k"]) == (128, 256, 256)
+    assert info["tiles_m"] == -(-M // 128) and info["tiles_n"] == -(-N // 256) and info["k_steps"] == -(-K // 256)
+    T = info["tiles_m"] * info["tiles_n"]
+    assert info["grid"] == min(T, 152) and info["sk_tiles"] == 0 and info["dp_tiles"] == T
+    items = _check_plan_coverage(info)
+    assert all(k0 == 0 and k1 == info["k_steps"] for row in items for (_, k0, k1, *_) in row)
