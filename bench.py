@@ -182,6 +182,8 @@ def measured_peaks() -> dict:
 # SM clock drops from 2070 MHz to ~1870 MHz within ~40 ms of dense GEMMs), so its
 # tensor roof is the sustained cuBLAS figure; shorter runs use the burst figure.
 SUSTAINED_AFTER_MS = 50.0
+# Nominal dense tensor rates per GB300: FP4 13.5 PFLOP/s against bf16 2.25.
+FP4_PER_BF16 = 6.0
 
 
 def tensor_peak(peaks: dict, timed_ms: float):
@@ -508,6 +510,8 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         # memory-bound rows measured up to 2 us slower per launch
         names = [n for n in syn.WORKLOADS if n.startswith("dec")] + ["sq2048", "mlp_up", "mlp_down", "sq8192"]
         names += list(syn.GATED_WORKLOADS) + list(syn.RESIDUAL_WORKLOADS) + list(syn.BATCHED_WORKLOADS)
+        names += ["fp4_sq4096", "fp4_sq8192", "fp4_sq16384"]
+    fp4_names = [n for n in names if n in syn.NVFP4_WORKLOADS]
     gated_names = [n for n in names if n in syn.GATED_WORKLOADS]
     resid_names = [n for n in names if n in syn.RESIDUAL_WORKLOADS]
     batched_names = [n for n in names if n in syn.BATCHED_WORKLOADS]
@@ -623,6 +627,38 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
                     "us": med * 1e3, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]})
         del sets, Ws, A, Cs
         torch.cuda.empty_cache()
+    for name in fp4_names:
+        fw = syn.NVFP4_WORKLOADS[name]
+        with torch.cuda.stream(stream):
+            gen.manual_seed(5000 + fw.cfg)
+            dev = stream.device
+
+            def codes(rows, cols):
+                return torch.randint(0, 256, (rows, cols), generator=gen, device=dev, dtype=torch.uint8)
+
+            def scales(rows):
+                plain = torch.randint(syn.NVFP4_SCALE_LO, syn.NVFP4_SCALE_HI + 1, (rows, fw.K // 16), generator=gen,
+                                      device=dev, dtype=torch.uint8)
+                return sg.nvfp4_pack_scales(plain, fw.K, stream=stream)
+
+            per_set = (fw.M + fw.N) * fw.K // 2
+            nrot = rotation_count(per_set, l2)
+            sets = [(codes(fw.M, fw.K // 2), scales(fw.M), codes(fw.N, fw.K // 2), scales(fw.N)) for _ in range(nrot)]
+            C = torch.empty((fw.M, fw.N), dtype=torch.float16, device=dev)
+        stream.synchronize()
+        fns = [(lambda a=a, sa=sa, b=b, sb=sb: sg.gemm_nvfp4(a, sa, b, sb, K=fw.K, C=C, alpha=fw.alpha, stream=stream))
+               for a, sa, b, sb in sets]
+        total = time_launches(torch, stream, fns, steps, 5)
+        med = total / steps
+        row = {"workload": name, "entry": "gemm_nvfp4", "M": fw.M, "N": fw.N, "K": fw.K, "us": med * 1e3,
+               "tflops": fw.flops / (med / 1e3) / 1e12}
+        rpeak, rkey = tensor_peak(peaks, total)
+        # FP4 roof: the measured bf16 roof times the nominal dense FP4 / bf16 ratio (13.5 / 2.25)
+        row["frac_of_peak"] = row["tflops"] / (FP4_PER_BF16 * rpeak)
+        row["peak"] = f"{FP4_PER_BF16:g} x {rkey}"
+        out.append(row)
+        del sets, C
+        torch.cuda.empty_cache()
     return out
 
 
@@ -683,7 +719,8 @@ def run_rows_only(args, local):
 
     names = [n.strip() for n in args.rows_only.split(",") if n.strip()]
     unknown = [n for n in names if n not in syn.WORKLOADS and n not in syn.GATED_WORKLOADS
-               and n not in syn.RESIDUAL_WORKLOADS and n not in syn.BATCHED_WORKLOADS]
+               and n not in syn.RESIDUAL_WORKLOADS and n not in syn.BATCHED_WORKLOADS
+               and n not in syn.NVFP4_WORKLOADS]
     if unknown or not names:
         raise SystemExit(f"unknown workloads: {unknown or args.rows_only!r}")
     import torch

@@ -148,6 +148,16 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Descriptors of stage 0; a stage adds its byte offset >> 4, a K = 64 step
+      // 32 bytes of the swizzle row (+2), an atom 512 bytes (+32).  Every address
+      // stays below 256 KB, so the sums never carry out of the 14-bit field.
+      const uint32_t base = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc_sw128(base);
+      const uint64_t b_desc0 = smem_desc_sw128(base + kF4ABytes);
+      const uint64_t sfa_desc0 = smem_desc_rows16(base + kF4SfaOff);
+      const uint64_t sfb_desc0 = smem_desc_rows16(base + kF4SfbOff);
+      constexpr uint64_t kStageUnits = kF4StageBytes >> 4;
+      constexpr uint64_t kAtomUnits = kF4AtomBytes >> 4;
       uint32_t it = 0;
       bool ok = true;
       for (int i = 0; i < nitems && ok; ++i) {
@@ -167,19 +177,24 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             break;
           }
           tc_fence_after();
-          const int nch = min(4, p.kc - ks * 4);
-          const uint8_t* st = smem + s * kF4StageBytes;
-          const uint32_t sf_col = tmem_base + kF4TileN + s * kF4SfCols;
-          for (int kk = 0; kk < nch; ++kk) {
-            tc_cp_32x128b_warpx4(sf_col + 4 * kk, smem_desc_rows16(smem_u32(st + kF4SfaOff + kk * kF4AtomBytes)));
-            for (int rb = 0; rb < 2; ++rb)
-              tc_cp_32x128b_warpx4(sf_col + 16 + 8 * kk + 4 * rb,
-                                   smem_desc_rows16(smem_u32(st + kF4SfbOff + (rb * 4 + kk) * kF4AtomBytes)));
+          const uint64_t so = s * kStageUnits;
+          const uint32_t sfc = tmem_base + kF4TileN + s * kF4SfCols;
+          // per K = 64 chunk: its A scales, the B scales of both row blocks, then
+          // the MMA (a copy is ordered before a later MMA of the same thread)
+          auto chunk = [&](int kk) {
+            tc_cp_32x128b_warpx4(sfc + 4 * kk, sfa_desc0 + so + kk * kAtomUnits);
+            tc_cp_32x128b_warpx4(sfc + 16 + 8 * kk, sfb_desc0 + so + kk * kAtomUnits);
+            tc_cp_32x128b_warpx4(sfc + 20 + 8 * kk, sfb_desc0 + so + (4 + kk) * kAtomUnits);
+            tc_mma_nvf4(tmem_base, a_desc0 + so + 2 * kk, b_desc0 + so + 2 * kk, kIdesc, sfc + 4 * kk,
+                        sfc + 16 + 8 * kk, (ks > 0 || kk > 0) ? 1u : 0u);
+          };
+          if (ks + 1 < k_stages || p.kc % 4 == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) chunk(kk);
+          } else {
+            const int nch = p.kc - ks * 4;  // the last stage's chunks that hold data
+            for (int kk = 0; kk < nch; ++kk) chunk(kk);
           }
-          const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + kF4ABytes);
-          for (int kk = 0; kk < nch; ++kk)  // +32 bytes per 64 fp4 of K inside the swizzle row
-            tc_mma_nvf4(tmem_base, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
-                        sf_col + 4 * kk, sf_col + 16 + 8 * kk, (ks > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&empty[s]);  // the slot (and its scale columns) are free once these MMAs are done
         }
         if (!ok) break;
