@@ -18,6 +18,10 @@ e4m3_value(codes)              fp64 values of E4M3 (FP8) codes
 nvfp4_dequant(P, S, K)         packed FP4 rows times their 16-element block scales, fp64
 gemm_nvfp4(A, SFA, B, SFB, K)  alpha * dequant(A) . dequant(B)^T in fp64 (NVFP4 GEMM)
 gemm_nvfp4_sampled(...)        the same at chosen rows x columns
+attention(Q, K, V, ...)        softmax(scale Q K^T, causal mask) V per head, fp64, with
+                               the log-sum-exp of each row's scores
+attention_combine(parts)       merges attention over disjoint key ranges by their
+                               log-sum-exps (the split-KV combine step)
 build()                        compile the C oracle (idempotent)
 
 A and B are uint16 arrays of bf16 bit patterns, A[M, lda] and B[N, ldb]; the
@@ -207,3 +211,81 @@ def gemm_nvfp4_sampled(A, SFA, B, SFB, rows, cols, K: int, alpha: float = 1.0) -
     a = nvfp4_dequant(np.asarray(A)[rows], np.asarray(SFA)[rows], K)
     b = nvfp4_dequant(np.asarray(B)[cols], np.asarray(SFB)[cols], K)
     return float(alpha) * (a @ b.T)
+
+
+# Scaled dot-product attention of one decoder layer, the fused kernel the
+# spark-kernels page builds ("attention": flash attention with the online
+# softmax, causal tiles above the diagonal skipped, a split-KV schedule merged
+# by a combine step, and a short-query tile for decode).  The oracle is the
+# definition written out, per (batch, head), in fp64:
+#
+#   s[i, j] = scale * sum_d q[i, d] k[j, d]          for visible keys j
+#   p[i, j] = exp(s[i, j] - max_j s[i, j]),  l[i] = sum_j p[i, j]
+#   o[i, :] = sum_j p[i, j] v[j, :] / l[i],  lse[i] = log(l[i]) + max_j s[i, j]
+#
+# Key j is visible to query i when j < Sk and, if causal, j <= i + (Sk - Sq): the
+# queries are the last Sq positions of a sequence whose first Sk positions are the
+# keys (a decode step against a cache when Sq < Sk; the usual lower triangle when
+# Sq = Sk).  A query with no visible key gets o = 0 and lse = -inf.  Grouped
+# query heads share key/value heads: query head h reads key/value head
+# h // (H // Hkv).
+
+def _bf16_tensor(x: np.ndarray) -> np.ndarray:
+    """fp64 values of a bf16 bit-pattern array of any shape."""
+    return (np.asarray(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, causal: bool = False,
+              scale: float | None = None, return_lse: bool = False):
+    """Attention of Q [B, Sq, H, D] against K, V [B, Sk, Hkv, D] (bf16 bit patterns
+    as uint16, or float arrays taken as exact values); returns fp64 O [B, Sq, H, D]
+    and, with return_lse, the fp64 log-sum-exp [B, H, Sq] of each row's scaled
+    scores.  scale defaults to 1 / sqrt(D)."""
+    def val(x):
+        x = np.asarray(x)
+        return _bf16_tensor(x) if x.dtype == np.uint16 else x.astype(np.float64)
+    q, k, v = val(Q), val(K), val(V)
+    Bt, Sq, H, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    assert k.shape == (Bt, Sk, Hkv, D) and v.shape == k.shape and H % Hkv == 0
+    sc = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    group = H // Hkv
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    visible = np.ones((Sq, Sk), dtype=bool) if not causal else (j <= i + (Sk - Sq))
+    O = np.zeros((Bt, Sq, H, D))
+    lse = np.full((Bt, H, Sq), -np.inf)
+    for b in range(Bt):
+        for h in range(H):
+            kh = h // group
+            s = sc * (q[b, :, h, :] @ k[b, :, kh, :].T)
+            s = np.where(visible, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            rows = np.isfinite(m[:, 0])
+            p = np.where(visible, np.exp(s - np.where(rows[:, None], m, 0.0)), 0.0)
+            l = p.sum(axis=1)
+            o = p @ v[b, :, kh, :]
+            O[b, rows, h, :] = o[rows] / l[rows, None]
+            lse[b, h, rows] = np.log(l[rows]) + m[rows, 0]
+    return (O, lse) if return_lse else O
+
+
+def attention_combine(parts) -> tuple[np.ndarray, np.ndarray]:
+    """Merges attention results over disjoint key ranges: parts is a sequence of
+    (O_p [B, Sq, H, D], lse_p [B, H, Sq]).  With L = log(sum_p exp(lse_p)), the
+    result is O = sum_p exp(lse_p - L) O_p and L itself; a part with lse = -inf
+    (no visible key) has weight 0."""
+    Os = [np.asarray(o, dtype=np.float64) for o, _ in parts]
+    Ls = [np.asarray(l, dtype=np.float64) for _, l in parts]
+    m = np.max(np.stack(Ls), axis=0)
+    finite = np.isfinite(m)
+    m0 = np.where(finite, m, 0.0)
+    w = [np.where(np.isfinite(l), np.exp(l - m0), 0.0) for l in Ls]
+    tot = np.sum(np.stack(w), axis=0)
+    L = np.where(finite, np.log(np.where(finite, tot, 1.0)) + m0, -np.inf)
+    O = np.zeros_like(Os[0])
+    for o, wi in zip(Os, w):
+        # weights [B, H, Sq] -> [B, Sq, H, 1]
+        wt = np.where(finite, wi / np.where(finite, tot, 1.0), 0.0)
+        O += o * np.transpose(wt, (0, 2, 1))[..., None]
+    return O, L

@@ -345,3 +345,55 @@ NVFP4_WORKLOADS = {w.name: w for w in [
     Nvfp4Workload("fp4_sq8192", 8192, 8192, 8192, 62),
     Nvfp4Workload("fp4_sq16384", 16384, 16384, 16384, 63),
 ]}
+
+
+@dataclasses.dataclass(frozen=True)
+class AttentionWorkload:
+    """Attention of one decoder layer: Q [B, Sq, H, 128] against K, V [B, Sk, Hkv,
+    128], all N(0, 1) rounded to bf16 (query/key/value activations of unit scale),
+    token-major with heads x head_dim contiguous.  The spark-kernels page's shapes:
+    4096 tokens and 32 heads of 128, causal and not, and one decode query against
+    a 4096-token cache."""
+    name: str
+    B: int
+    Sq: int
+    Sk: int
+    H: int
+    Hkv: int
+    causal: bool
+    cfg: int
+    D: int = 128
+
+    def _t(self, S: int, heads: int, seed: int) -> np.ndarray:
+        return matrix(self.B * S, heads * self.D, "normal", seed).reshape(self.B, S, heads, self.D)
+
+    def q(self) -> np.ndarray:
+        return self._t(self.Sq, self.H, SEED_A_BASE + 700 + self.cfg)
+
+    def k(self) -> np.ndarray:
+        return self._t(self.Sk, self.Hkv, SEED_B_BASE + 700 + self.cfg)
+
+    def v(self) -> np.ndarray:
+        return self._t(self.Sk, self.Hkv, SEED_B_BASE + 800 + self.cfg)
+
+    @property
+    def flops(self) -> int:
+        """4 B H D x (visible query-key pairs): two products of 2 FLOP per pair and
+        dimension (the causal count is the halved one the page quotes)."""
+        if self.causal:
+            pairs = sum(min(self.Sk, i + (self.Sk - self.Sq) + 1) for i in range(self.Sq))
+        else:
+            pairs = self.Sq * self.Sk
+        return 4 * self.B * self.H * self.D * pairs
+
+    @property
+    def kv_bytes(self) -> int:
+        return 2 * 2 * self.B * self.Sk * self.Hkv * self.D
+
+
+ATTENTION_WORKLOADS = {w.name: w for w in [
+    AttentionWorkload("attn_small", 2, 300, 300, 4, 4, True, 70),
+    AttentionWorkload("attn_causal_4096", 1, 4096, 4096, 32, 32, True, 71),
+    AttentionWorkload("attn_4096", 1, 4096, 4096, 32, 32, False, 72),
+    AttentionWorkload("attn_decode_4096", 1, 1, 4096, 32, 32, True, 73),
+]}
