@@ -244,6 +244,48 @@ SG_API int nvfp4_pack_scales(const void *plain, int64_t rows, int64_t K, int64_t
                              sg_stream_t stream);
 
 /*
+ * attention_bf16 -- fused scaled dot-product attention (forward), the attention
+ * kernel of the spark-kernels page ("attention": flash attention with the online
+ * softmax, S = Q K^T and O += P V on the tensor cores, P rounded to bf16 for the
+ * second product, causal tiles above the diagonal skipped):
+ *
+ *   O[b, i, h, :] = sum_j softmax_j(scale * Q[b, i, h, :] . K[b, j, g, :]) V[b, j, g, :]
+ *
+ * over the keys j visible to query i, with g = h / (heads / kv_heads) (grouped
+ * query heads share a key/value head).  Key j is visible when j < seq_k and, if
+ * `causal` is non-zero, j <= i + (seq_k - seq_q): the queries are the last seq_q
+ * positions of a sequence whose first seq_k positions are the keys (the lower
+ * triangle when seq_q = seq_k, a decode step against a cache when seq_q < seq_k).
+ * A query that sees no key gets O = 0.
+ *
+ * Layout (device pointers, bf16 bit patterns, row-major):
+ *   Q  batch * seq_q rows (token b * seq_q + i) of heads * head_dim elements:
+ *      head h at columns [h * head_dim, (h + 1) * head_dim); row pitch ldq.
+ *   K, V  batch * seq_k rows (token b * seq_k + j) of kv_heads * head_dim
+ *      elements, pitches ldk and ldv.
+ *   O  like Q, pitch ldo (written; Q, K, V only read).
+ * The caller owns every buffer; nothing is allocated per call (the library's
+ * per-device workspace is allocated on a first call).  K and V must be finite:
+ * keys past seq_k inside a tile are masked, but their values are multiplied by 0.
+ *
+ * Arithmetic: scores and the softmax in fp32 (exp2 of log2-scaled scores), the
+ * weights rounded to bf16 for the P V product, fp32 accumulation, one bf16
+ * rounding of O (nearest even).  Results are the same on every run.
+ *
+ * Requirements: head_dim = 128; heads a multiple of kv_heads; ldq, ldo >= heads *
+ * head_dim and ldk, ldv >= kv_heads * head_dim, all multiples of 8; pointers
+ * 16-byte aligned; scale finite.  Errors: SG_ERR_INVALID_ARG (negative sizes,
+ * head_dim != 128, heads % kv_heads != 0, short pitches, null pointers, sizes past
+ * 32-bit row indices), SG_ERR_MISALIGNED, SG_ERR_UNSUPPORTED_DEVICE, SG_ERR_CUDA,
+ * SG_ERR_TIMEOUT (on the next sg_check_device_errors).  batch, seq_q or heads = 0:
+ * no work.  seq_k = 0: O := 0.  Asynchronous on `stream`; graph-capturable after
+ * a first call.
+ */
+SG_API int attention_bf16(const void *Q, const void *K, const void *V, void *O, int64_t batch, int64_t seq_q,
+                          int64_t seq_k, int64_t heads, int64_t kv_heads, int64_t head_dim, int64_t ldq,
+                          int64_t ldk, int64_t ldv, int64_t ldo, int causal, float scale, sg_stream_t stream);
+
+/*
  * gemv_bf16_noalloc -- gemv_bf16 on the CUDA-core kernel (SG_PATH_CUDA_CORE),
  * for callers that cannot allocate device memory.  The pages have no
  * counterpart: this entry point exists for integration, not for the method.

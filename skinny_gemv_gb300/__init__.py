@@ -112,6 +112,8 @@ def load(build_if_missing: bool = False):
     lib.nvfp4_pack_scales.argtypes = [p, i64, i64, i64, p, p]
     lib.nvfp4_pack_scales.restype = ctypes.c_int
     lib.sg_plan_nvfp4.argtypes = [i64, i64, i64, i32, ctypes.POINTER(PlanInfo)]
+    lib.attention_bf16.argtypes = [p, p, p, p] + [i64] * 10 + [ctypes.c_int, ctypes.c_float, p]
+    lib.attention_bf16.restype = ctypes.c_int
     lib.sg_plan_nvfp4.restype = ctypes.c_int
     lib.sg_status_string.argtypes = [ctypes.c_int]
     lib.sg_status_string.restype = ctypes.c_char_p
@@ -331,6 +333,43 @@ def gemm_nvfp4(A, SFA, B, SFB, K: int | None = None, C=None, alpha: float = 1.0,
                                float(alpha), _stream_handle(stream))
     _check(st, "gemm_nvfp4")
     return C
+
+
+def _tokens_heads(t, name: str):
+    """A [B, S, heads, D] bfloat16 CUDA tensor whose (heads, D) block is dense:
+    returns (pointer, token pitch in elements)."""
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_cuda:
+        raise ValueError(f"{name} must be a 4-D [batch, seq, heads, head_dim] bfloat16 CUDA tensor, "
+                         f"got {t.dtype} {tuple(t.shape)} {t.device}")
+    Bt, S, H, D = t.shape
+    if (D > 1 and t.stride(3) != 1) or (H > 1 and t.stride(2) != D) or (Bt > 1 and S > 0 and t.stride(0) != S * t.stride(1)):
+        raise ValueError(f"{name} must have dense heads x head_dim rows and batches of whole rows")
+    return t.data_ptr(), max(t.stride(1), H * D)
+
+
+def attention_bf16(Q, K, V, O=None, causal: bool = False, scale: float | None = None, stream=None):
+    """O = softmax(scale Q K^T, causal mask) V per head for Q [B, Sq, H, 128] and
+    K, V [B, Sk, Hkv, 128] (bfloat16); returns O [B, Sq, H, 128]."""
+    torch = _torch()
+    q_ptr, ldq = _tokens_heads(Q, "Q")
+    k_ptr, ldk = _tokens_heads(K, "K")
+    v_ptr, ldv = _tokens_heads(V, "V")
+    Bt, Sq, H, D = Q.shape
+    Sk, Hkv = K.shape[1], K.shape[2]
+    if tuple(K.shape) != (Bt, Sk, Hkv, D) or tuple(V.shape) != tuple(K.shape):
+        raise ValueError(f"K and V must be [{Bt}, seq_k, kv_heads, {D}], got {tuple(K.shape)} and {tuple(V.shape)}")
+    if O is None:
+        O = torch.empty((Bt, Sq, H, D), dtype=torch.bfloat16, device=Q.device)
+    if tuple(O.shape) != (Bt, Sq, H, D):
+        raise ValueError(f"O must be [{Bt}, {Sq}, {H}, {D}]")
+    o_ptr, ldo = _tokens_heads(O, "O")
+    scale = D ** -0.5 if scale is None else float(scale)
+    with torch.cuda.device(Q.device):
+        st = load().attention_bf16(q_ptr, k_ptr, v_ptr, o_ptr, Bt, Sq, Sk, H, Hkv, D, ldq, ldk, ldv, ldo,
+                                   1 if causal else 0, scale, _stream_handle(stream))
+    _check(st, "attention_bf16")
+    return O
 
 
 def gemv_bf16_batched(A, Bs, Cs=None, stream=None, path: int = PATH_AUTO):

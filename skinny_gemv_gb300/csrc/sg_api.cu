@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -664,6 +665,31 @@ int gemm_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N, i
   return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, pair, s, R, ldr);
 }
 
+int run_attention(DeviceState& d, int dev, const void* Q, const void* K, const void* V, void* O, int64_t B,
+                  int64_t Sq, int64_t Sk, int64_t H, int64_t Hkv, int64_t ldq, int64_t ldk, int64_t ldv,
+                  int64_t ldo, int causal, float scale, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  int st = make_map(&tq, Q, B * Sq, H * kAttnHeadDim, ldq, kAttnTile, 64, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tk, K, B * Sk, Hkv * kAttnHeadDim, ldk, kAttnTile, 64, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st == SG_OK) st = make_map(&tv, V, B * Sk, Hkv * kAttnHeadDim, ldv, kAttnTile, 64, CU_TENSOR_MAP_SWIZZLE_128B, dev);
+  if (st != SG_OK) return st;
+  AttnParams p{};
+  p.B = static_cast<int32_t>(B);
+  p.Sq = static_cast<int32_t>(Sq);
+  p.Sk = static_cast<int32_t>(Sk);
+  p.H = static_cast<int32_t>(H);
+  p.Hkv = static_cast<int32_t>(Hkv);
+  p.q_tiles = static_cast<int32_t>(ceil_div(Sq, kAttnTile));
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.O = static_cast<uint16_t*>(O);
+  p.ldo = ldo;
+  p.err = d.err;
+  p.timeout_ns = g_timeout_ns.load();
+  const cudaError_t e = launch_attention(tq, tk, tv, p, stream);
+  return e == cudaSuccess ? SG_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 void set_last_cuda_error(int e) { g_last_cuda_error = e; }
@@ -864,6 +890,40 @@ const char* sg_status_string(int status) {
     case SG_ERR_OUT_OF_MEMORY: return "SG_ERR_OUT_OF_MEMORY: workspace allocation failed";
     default: return "unknown sg_status";
   }
+}
+
+int attention_bf16(const void* Q, const void* K, const void* V, void* O, int64_t batch, int64_t seq_q,
+                   int64_t seq_k, int64_t heads, int64_t kv_heads, int64_t head_dim, int64_t ldq, int64_t ldk,
+                   int64_t ldv, int64_t ldo, int causal, float scale, sg_stream_t stream) {
+  if (batch < 0 || seq_q < 0 || seq_k < 0 || heads < 0 || kv_heads < 0) return SG_ERR_INVALID_ARG;
+  if (head_dim != kAttnHeadDim || !std::isfinite(scale)) return SG_ERR_INVALID_ARG;
+  if (batch == 0 || seq_q == 0 || heads == 0) return SG_OK;
+  if (kv_heads == 0 || heads % kv_heads != 0) return SG_ERR_INVALID_ARG;
+  // every row index and grid size in int32
+  const int64_t tiles = ceil_div(seq_q, kAttnTile) * heads * batch;
+  if (batch * seq_q > INT32_MAX || batch * seq_k > INT32_MAX || heads * head_dim > INT32_MAX || tiles > INT32_MAX)
+    return SG_ERR_INVALID_ARG;
+  if (!O || ldo < heads * head_dim) return SG_ERR_INVALID_ARG;
+  if (seq_k > 0 && (!Q || !K || !V || ldq < heads * head_dim || ldk < kv_heads * head_dim ||
+                    ldv < kv_heads * head_dim))
+    return SG_ERR_INVALID_ARG;
+  auto misaligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+  if (misaligned(O) || (ldo & 7)) return SG_ERR_MISALIGNED;
+  if (seq_k > 0 && (misaligned(Q) || misaligned(K) || misaligned(V) || (ldq & 7) || (ldk & 7) || (ldv & 7)))
+    return SG_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState* d = nullptr;
+  int dev = 0;
+  int st = current_device_state(&d, &dev);
+  if (st != SG_OK) return st;
+  if (seq_k == 0) {  // no query sees a key: O = 0
+    const cudaError_t e = cudaMemset2DAsync(O, ldo * 2, 0, heads * head_dim * 2, batch * seq_q, s);
+    return e == cudaSuccess ? SG_OK : cuda_fail(e);
+  }
+  st = ensure_workspace(*d, s);
+  if (st != SG_OK) return st;
+  return run_attention(*d, dev, Q, K, V, O, batch, seq_q, seq_k, heads, kv_heads, ldq, ldk, ldv, ldo, causal,
+                       scale, s);
 }
 
 int sg_last_cuda_error(void) { return g_last_cuda_error; }

@@ -1,0 +1,395 @@
+// Fused scaled dot-product attention (forward) on the 5th-generation tensor
+// cores, head dimension 128, bf16 in and out, fp32 softmax and accumulation:
+//
+//   O[i] = sum_j softmax_j(scale * q_i . k_j over the keys visible to i) v_j
+//
+// the attention kernel of the spark-kernels page ("attention": flash attention,
+// the online softmax between two tensor-core products S = Q K^T and O += P V, P
+// rounded to bf16 for the second product, causal tiles above the diagonal never
+// loaded, the heaviest query tiles launched first).
+//
+// One CTA per (128-row query tile, head, batch).  Roles:
+//   warp 0     TMA producer: the Q tile once (two 64-column boxes, 128-byte
+//              swizzle), then per key block a K tile and a V tile (128 keys x
+//              128 columns each) into a 2-stage ring
+//   warp 1     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into one
+//              of two 128-column TMEM buffers (K-major A and B), then, once the
+//              softmax has written P_j, O += P_j V_j into a third 128-column
+//              buffer; V is the B operand in MN-major form (the key rows of the
+//              V tile as written by TMA), so nothing is transposed
+//   warps 2-5  softmax, one query row per thread (its TMEM lane): S row -> scale,
+//              mask, running max m and sum l -> P row as bf16 into shared memory
+//              in the 128-byte-swizzled K-major layout the MMA reads; when m grows
+//              the O row is rescaled in TMEM (load, multiply, store) after the
+//              previous P V product completed; at the end O / l is rounded to
+//              bf16 and stored
+// S_{j+1} is issued before P_j V_j, so the next block's Q K^T overlaps the
+// softmax of this one.
+//
+// Key j is visible to query i when j < Sk and, for a causal launch, j <= i +
+// (Sk - Sq).  A row that sees no key gets O = 0.  Scores are kept in log2 units
+// (scale * log2 e folded into one multiply) and exponentiated with exp2f.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "sg_internal.h"
+#include "sg_ptx.cuh"
+
+namespace sg {
+namespace {
+
+constexpr int kAtStages = 2;
+constexpr int kAtThreads = 192;
+constexpr int kAtSoftmaxThreads = 128;
+constexpr int kAtBox = kAttnTile * 128;              // 128 rows x 128 bytes (64 bf16)
+constexpr int kAtQOff = 0;                           // Q: two boxes (d 0-63, 64-127)
+constexpr int kAtKvOff = 2 * kAtBox;                 // per stage: K boxes 0, 1 then V boxes 0, 1
+constexpr int kAtStageBytes = 4 * kAtBox;
+constexpr int kAtPOff = kAtKvOff + kAtStages * kAtStageBytes;  // P: two boxes (keys 0-63, 64-127)
+constexpr int kAtBarOff = kAtPOff + 2 * kAtBox;
+constexpr int kAtNumBars = 1 + 3 * kAtStages + 2 + 3;          // q, k[], v[], kv_empty[], s[2], p, o, teardown
+constexpr int kAtMiscOff = kAtBarOff + kAtNumBars * 8;
+constexpr int kAtSmem = kAtMiscOff + 16 + 1024;
+constexpr int kAtTmemCols = 512;                     // S buffers at 0 and 128, O at 256
+constexpr uint32_t kAtOCol = 256;
+static_assert(kAtSmem <= 232448, "shared memory budget");
+static_assert(kAttnHeadDim == 128 && kAttnTile == 128, "the tile shapes below assume 128");
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Number of 128-key blocks query tile t must visit.
+__device__ __forceinline__ int attn_blocks(const AttnParams& p, int q0) {
+  int kend = p.Sk;
+  if (p.causal) kend = min(p.Sk, min(q0 + kAttnTile, p.Sq) + (p.Sk - p.Sq));
+  return kend > 0 ? (kend + kAttnTile - 1) / kAttnTile : 0;
+}
+
+__global__ void __launch_bounds__(kAtThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + kAtBarOff);
+  uint64_t* k_full = q_full + 1;
+  uint64_t* v_full = k_full + kAtStages;
+  uint64_t* kv_empty = v_full + kAtStages;
+  uint64_t* s_full = kv_empty + kAtStages;  // [2]
+  uint64_t* p_ready = s_full + 2;
+  uint64_t* o_ready = p_ready + 1;
+  uint64_t* teardown = o_ready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAtMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kAtMiscOff + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  // Query tiles in decreasing order: under a causal mask the last tiles see the
+  // most keys, so they start first and the short ones fill the tail.
+  const int hb = static_cast<int>(blockIdx.x) % (p.H * p.B);
+  const int t = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / (p.H * p.B);
+  const int h = hb % p.H;
+  const int b = hb / p.H;
+  const int kvh = h / (p.H / p.Hkv);
+  const int q0 = t * kAttnTile;
+  const int nblk = attn_blocks(p, q0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kAtStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_ready, kAtSoftmaxThreads);
+    mbar_init(o_ready, 1);
+    mbar_init(teardown, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kAtTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  grid_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      grid_dependency_wait();
+      const int32_t qy = b * p.Sq + q0;
+      if (nblk > 0) {  // a tile that sees no key loads nothing
+        mbar_arrive_expect_tx(q_full, 2u * kAtBox);
+        tma_load_2d(smem + kAtQOff, &tmQ, h * kAttnHeadDim, qy, q_full);
+        tma_load_2d(smem + kAtQOff + kAtBox, &tmQ, h * kAttnHeadDim + 64, qy, q_full);
+      }
+      int j = 0;
+      for (; j < nblk; ++j) {
+        const uint32_t s = j % kAtStages;
+        const uint32_t ph = (j / kAtStages) & 1u;
+        if (!mbar_wait(&kv_empty[s], ph ^ 1u, p.timeout_ns, abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kDevTimeoutEmpty, j);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + kAtKvOff + s * kAtStageBytes;
+        const int32_t ky = b * p.Sk + j * kAttnTile;
+        const int32_t kx = kvh * kAttnHeadDim;
+        mbar_arrive_expect_tx(&k_full[s], 2u * kAtBox);
+        tma_load_2d(st, &tmK, kx, ky, &k_full[s]);
+        tma_load_2d(st + kAtBox, &tmK, kx + 64, ky, &k_full[s]);
+        mbar_arrive_expect_tx(&v_full[s], 2u * kAtBox);
+        tma_load_2d(st + 2 * kAtBox, &tmV, kx, ky, &v_full[s]);
+        tma_load_2d(st + 3 * kAtBox, &tmV, kx + 64, ky, &v_full[s]);
+      }
+      if (*abort_flag) {
+        // Unwinding: let the copies already issued land before the CTA exits.
+        volatile uint32_t never = 0;
+        if (nblk > 0) mbar_wait(q_full, 0, p.timeout_ns, &never);
+        for (int i = (j > kAtStages ? j - kAtStages : 0); i < j; ++i) {
+          mbar_wait(&k_full[i % kAtStages], (i / kAtStages) & 1u, p.timeout_ns, &never);
+          mbar_wait(&v_full[i % kAtStages], (i / kAtStages) & 1u, p.timeout_ns, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kAttnTile, kAttnTile);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kAttnTile, kAttnHeadDim) | (1u << 16);  // B MN-major
+      const uint32_t base = smem_u32(smem);
+      bool ok = nblk == 0 || mbar_wait(q_full, 0, p.timeout_ns, abort_flag);
+      if (!ok && !*abort_flag) record_error(p.err, kDevTimeoutFull, 0);
+      // S_j = Q K_j^T: K = 128 in 8 steps of 16 (32 bytes of a swizzle row; the
+      // second 64 columns are the next box).
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t s = j % kAtStages;
+        if (!mbar_wait(&k_full[s], (j / kAtStages) & 1u, p.timeout_ns, abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kDevTimeoutFull, j);
+          return false;
+        }
+        tc_fence_after();
+        const uint32_t kaddr = base + kAtKvOff + s * kAtStageBytes;
+        const uint32_t dst = tmem_base + static_cast<uint32_t>(j & 1) * kAttnTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtBox + (kk & 3) * 32;
+          tc_mma_bf16(dst, smem_desc_sw128(base + kAtQOff + off), smem_desc_sw128(kaddr + off), kIdescS,
+                      kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[j & 1]);
+        return true;
+      };
+      if (ok && nblk > 0) ok = issue_s(0);
+      for (int j = 0; j < nblk && ok; ++j) {
+        // The S buffer of block j + 1 was last read by the softmax of block j - 1,
+        // which finished before p_ready of j - 1 (waited for below last round).
+        if (j + 1 < nblk && !(ok = issue_s(j + 1))) break;
+        if (!mbar_wait(p_ready, static_cast<uint32_t>(j) & 1u, p.timeout_ns, abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kDevTimeoutTmemEmpty, j);
+          ok = false;
+          break;
+        }
+        const uint32_t s = j % kAtStages;
+        if (!mbar_wait(&v_full[s], (j / kAtStages) & 1u, p.timeout_ns, abort_flag)) {
+          if (!*abort_flag) record_error(p.err, kDevTimeoutFull, j);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // O += P_j V_j: K = 128 keys in 8 steps of 16 keys; P is K-major (32 bytes
+        // of a swizzle row per step), V MN-major (two 8-key atoms, 2048 bytes, per
+        // step; the d columns 64-127 are the next box, kAtBox further on).
+        const uint32_t vaddr = base + kAtKvOff + s * kAtStageBytes + 2 * kAtBox;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t poff = (kk >> 2) * kAtBox + (kk & 3) * 32;
+          tc_mma_bf16(tmem_base + kAtOCol, smem_desc_sw128(base + kAtPOff + poff),
+                      smem_desc_sw128_mn(vaddr + kk * 2048, kAtBox), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(o_ready);
+        tc_commit(&kv_empty[s]);
+      }
+      if (!ok) *abort_flag = 1;
+      if (*abort_flag) {
+        // Unwinding: wait for every tcgen05 operation issued so far before TMEM is freed.
+        tc_commit(teardown);
+        volatile uint32_t never = 0;
+        if (!mbar_wait(teardown, 0, p.timeout_ns, &never)) record_error(p.err, kDevTimeoutTeardown, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int q = warp & 3;                // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;           // query row of the tile = TMEM lane
+    const int i = q0 + r;                  // query index in the sequence
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // keys [0, lim) are visible to this query (rows past Sq compute garbage and
+    // store nothing)
+    const int lim = p.causal ? min(p.Sk, i + (p.Sk - p.Sq) + 1) : p.Sk;
+    uint8_t* prow = smem + kAtPOff + r * 128;
+    float m_run = -INFINITY;  // running max of the log2-scaled scores
+    float l_run = 0.f;        // running sum of the bf16-rounded weights
+    bool ok = true;
+    for (int j = 0; j < nblk; ++j) {
+      const uint64_t limit = p.timeout_ns + 20000ull * static_cast<uint64_t>(j + 1);
+      ok = mbar_wait(&s_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, limit, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j & 1) * kAttnTile + 32 * c, sv[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
+      // scale into log2 units, mask, row max
+      const int kv = lim - j * kAttnTile;  // keys of this block visible: [0, kv)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x = (32 * c + e < kv) ? __uint_as_float(sv[c][e]) * p.scale_log2 : -INFINITY;
+          sv[c][e] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m_run - m_use);  // 0 while nothing was visible yet
+      // weights, rounded to bf16 (the P V product's operand); l sums the rounded values
+      uint32_t pk[64];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = exp2f(__uint_as_float(sv[c][2 * e]) - m_use);
+          const float p1 = exp2f(__uint_as_float(sv[c][2 * e + 1]) - m_use);
+          const uint32_t w = pack_bf16x2(p0, p1);
+          pk[16 * c + e] = w;
+          rs += bf16_lo(w) + bf16_hi(w);
+        }
+      l_run = l_run * alpha + rs;
+      m_run = m_new;
+      if (j > 0) {
+        // P_{j-1} V_{j-1} must be complete before O is rescaled and P rewritten.
+        ok = mbar_wait(o_ready, static_cast<uint32_t>(j - 1) & 1u, limit, abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
+            tmem_ld_wait(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P row into the 128-byte-swizzled K-major tile: keys 64 c2 .. 64 c2 + 63 in
+      // box c2, 16-byte chunk cc of the row at position cc ^ (r % 8).
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const int c2 = ch >> 3, cc = ch & 7;
+        uint4* dst = reinterpret_cast<uint4*>(prow + c2 * kAtBox + ((cc ^ (r & 7)) << 4));
+        *dst = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();  // the MMA reads P through the async proxy
+      tc_fence_before();         // order the O stores before the MMA thread's next products
+      mbar_arrive(p_ready);
+    }
+    if (!ok) *abort_flag = 1;
+    // epilogue: O / l, rounded to bf16, one 256-byte row per thread
+    bool have_o = ok && nblk > 0;
+    if (have_o) {
+      const uint64_t limit = p.timeout_ns + 20000ull * static_cast<uint64_t>(nblk + 1);
+      have_o = mbar_wait(o_ready, static_cast<uint32_t>(nblk - 1) & 1u, limit, abort_flag);
+      have_o = __all_sync(0xFFFFFFFFu, have_o);
+      if (!have_o) {
+        if (!*abort_flag) record_error(p.err, kDevTimeoutTmemFull, nblk);
+        *abort_flag = 1;
+      }
+      tc_fence_after();
+    }
+    grid_dependency_wait();
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    uint16_t* orow = p.O + static_cast<int64_t>(b * p.Sq + i) * p.ldo + h * kAttnHeadDim;
+    const bool store = i < p.Sq && !*abort_flag;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ov[32];
+      if (have_o) {
+        tmem_ld_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
+        tmem_ld_wait(ov);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ov[e] = 0u;
+      }
+      if (store) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(ov[8 * g + 0]) * inv, __uint_as_float(ov[8 * g + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(ov[8 * g + 2]) * inv, __uint_as_float(ov[8 * g + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(ov[8 * g + 4]) * inv, __uint_as_float(ov[8 * g + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(ov[8 * g + 6]) * inv, __uint_as_float(ov[8 * g + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * g) = v;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kAtTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnParams& p, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t grid = static_cast<int64_t>(p.q_tiles) * p.H * p.B;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kAtThreads, 1, 1);
+  cfg.dynamicSmemBytes = kAtSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel, tmQ, tmK, tmV, p);
+}
+
+}  // namespace sg

@@ -177,6 +177,28 @@ cudaError_t launch_f4_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_f4_pack_scales(const uint8_t* plain, int64_t rows, int64_t K, int64_t ld, uint8_t* atoms,
                                   cudaStream_t stream);
 
+// ---------------------------------------------------------------- attention
+// Fused attention forward for head dimension 128: query tiles of 128 rows, key
+// blocks of 128.  Q rows are tokens b * Sq + i with head h at columns
+// [128 h, 128 h + 128); K and V rows are tokens b * Sk + j with kv head g at
+// columns [128 g, 128 g + 128).
+constexpr int kAttnTile = 128;
+constexpr int kAttnHeadDim = 128;
+
+struct AttnParams {
+  int32_t B, Sq, Sk, H, Hkv;
+  int32_t q_tiles;       // ceil(Sq / 128)
+  int32_t causal;        // key j visible to query i iff j <= i + (Sk - Sq)
+  float scale_log2;      // softmax scale x log2(e)
+  uint16_t* O;           // bf16 output, rows b * Sq + i, head h at columns 128 h
+  int64_t ldo;           // elements between consecutive rows of O
+  DeviceError* err;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnParams& p, cudaStream_t stream);
+
 // Dynamic shared memory of the CUDA-core kernel for M rows over grid_rows row blocks.
 int cc_smem_bytes(int64_t M, int64_t N, int grid_rows, bool gated = false);
 

@@ -329,3 +329,29 @@ def test_nvfp4_plan_covers_every_tile_once(lib, M, N, K):
     assert info["grid"] == min(T, 152) and info["sk_tiles"] == 0 and info["dp_tiles"] == T
     items = _check_plan_coverage(info)
     assert all(k0 == 0 and k1 == info["k_steps"] for row in items for (_, k0, k1, *_) in row)
+
+
+# ------------------------------------------------------------------ attention
+@pytest.mark.parametrize("args,code", [
+    # (Q, K, V, O, batch, seq_q, seq_k, heads, kv_heads, head_dim, ldq, ldk, ldv, ldo, causal, scale)
+    ((16, 16, 16, 16, 1, 8, 8, 2, 2, 64, 128, 128, 128, 128, 1, 0.1), sg.SG_ERR_INVALID_ARG),   # head_dim != 128
+    ((16, 16, 16, 16, 1, 8, 8, 3, 2, 128, 384, 256, 256, 384, 1, 0.1), sg.SG_ERR_INVALID_ARG),  # heads % kv_heads
+    ((16, 16, 16, 16, -1, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1), sg.SG_ERR_INVALID_ARG),  # negative batch
+    ((16, 16, 16, 0, 1, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1), sg.SG_ERR_INVALID_ARG),    # null O
+    ((16, 0, 16, 16, 1, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1), sg.SG_ERR_INVALID_ARG),    # null K
+    ((16, 16, 16, 16, 1, 8, 8, 2, 2, 128, 255, 256, 256, 256, 1, 0.1), sg.SG_ERR_INVALID_ARG),  # short ldq
+    ((16, 16, 16, 16, 1, 8, 8, 2, 1, 128, 256, 127, 128, 256, 1, 0.1), sg.SG_ERR_INVALID_ARG),  # short ldk
+    ((16, 16, 16, 16, 1, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, float("inf")), sg.SG_ERR_INVALID_ARG),
+    ((24, 16, 16, 16, 1, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1), sg.SG_ERR_MISALIGNED),   # Q
+    ((16, 16, 16, 16, 1, 8, 8, 2, 2, 128, 260, 256, 256, 256, 1, 0.1), sg.SG_ERR_MISALIGNED),   # ldq % 8
+    ((16, 16, 16, 16, 1, 8, 8, 2, 2, 128, 256, 256, 256, 260, 1, 0.1), sg.SG_ERR_MISALIGNED),   # ldo % 8
+])
+def test_attention_argument_errors_before_any_cuda_call(lib, args, code):
+    assert lib.attention_bf16(*args[:14], args[14], args[15], None) == code
+
+
+def test_attention_empty_is_noop(lib):
+    # no batch, no queries or no heads: nothing to do, nothing dereferenced
+    assert lib.attention_bf16(None, None, None, None, 0, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1, None) == sg.SG_OK
+    assert lib.attention_bf16(None, None, None, None, 1, 0, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1, None) == sg.SG_OK
+    assert lib.attention_bf16(None, None, None, None, 1, 8, 8, 0, 0, 128, 256, 256, 256, 256, 1, 0.1, None) == sg.SG_OK
