@@ -665,6 +665,24 @@ int gemm_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N, i
   return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, pair, s, R, ldr);
 }
 
+// Key splits of an attention launch: when the (query tile, head, batch) units
+// leave SMs idle, each unit's key blocks are cut into n_splits equal runs (one
+// CTA each, at most one CTA per SM in all), provided the fp32 partial outputs
+// and log-sum-exps fit the workspace's partial slots.
+void attn_splits(int64_t B, int64_t Sq, int64_t Sk, int64_t H, int causal, int sms, int32_t* n_splits,
+                 int32_t* split_blocks) {
+  const int64_t units = ceil_div(Sq, kAttnTile) * H * B;
+  const int64_t max_blocks = ceil_div(Sk, kAttnTile);  // the last query tile sees the most keys
+  (void)causal;
+  int64_t n = units >= sms ? 1 : std::max<int64_t>(1, sms / units);
+  n = std::min<int64_t>(n, std::min<int64_t>(max_blocks, 32));
+  const int64_t per_split_bytes = B * Sq * H * (kAttnHeadDim + 1) * 4 + 256;
+  while (n > 1 && n * per_split_bytes > static_cast<int64_t>(kPartialBytes)) --n;
+  const int64_t bps = ceil_div(max_blocks, n);
+  *n_splits = static_cast<int32_t>(ceil_div(max_blocks, bps));
+  *split_blocks = static_cast<int32_t>(bps);
+}
+
 int run_attention(DeviceState& d, int dev, const void* Q, const void* K, const void* V, void* O, int64_t B,
                   int64_t Sq, int64_t Sk, int64_t H, int64_t Hkv, int64_t ldq, int64_t ldk, int64_t ldv,
                   int64_t ldo, int causal, float scale, cudaStream_t stream) {
@@ -686,7 +704,11 @@ int run_attention(DeviceState& d, int dev, const void* Q, const void* K, const v
   p.ldo = ldo;
   p.err = d.err;
   p.timeout_ns = g_timeout_ns.load();
-  const cudaError_t e = launch_attention(tq, tk, tv, p, stream);
+  attn_splits(B, Sq, Sk, H, causal, d.sm_count, &p.n_splits, &p.split_blocks);
+  p.part_lse = d.partials;
+  p.part_o = d.partials + ceil_div(static_cast<int64_t>(p.n_splits) * B * Sq * H, 64) * 64;
+  cudaError_t e = launch_attention(tq, tk, tv, p, stream);
+  if (e == cudaSuccess && p.n_splits > 1) e = launch_attn_combine(p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 

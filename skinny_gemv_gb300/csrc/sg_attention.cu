@@ -28,7 +28,7 @@
 //
 // Key j is visible to query i when j < Sk and, for a causal launch, j <= i +
 // (Sk - Sq).  A row that sees no key gets O = 0.  Scores are kept in log2 units
-// (scale * log2 e folded into one multiply) and exponentiated with exp2f.
+// (scale * log2 e folded into one multiply) and exponentiated with ex2.approx.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -62,6 +62,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 2^x by the ex2.approx instruction (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -92,13 +99,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   const int lane = threadIdx.x % 32;
   // Query tiles in decreasing order: under a causal mask the last tiles see the
   // most keys, so they start first and the short ones fill the tail.
-  const int hb = static_cast<int>(blockIdx.x) % (p.H * p.B);
-  const int t = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / (p.H * p.B);
+  const int split = static_cast<int>(blockIdx.x) % p.n_splits;
+  const int unit = static_cast<int>(blockIdx.x) / p.n_splits;
+  const int hb = unit % (p.H * p.B);
+  const int t = p.q_tiles - 1 - unit / (p.H * p.B);
   const int h = hb % p.H;
   const int b = hb / p.H;
   const int kvh = h / (p.H / p.Hkv);
   const int q0 = t * kAttnTile;
-  const int nblk = attn_blocks(p, q0);
+  // this CTA's key blocks [j_begin, j_begin + nblk)
+  const int tile_blocks = attn_blocks(p, q0);
+  const int j_begin = split * p.split_blocks;
+  const int nblk = max(0, min(tile_blocks - j_begin, p.split_blocks));
+  // softmax warps whose 32 rows hold at least one query (the others idle)
+  const int active_quarters = min(4, (p.Sq - q0 + 31) / 32);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -109,7 +123,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_ready, kAtSoftmaxThreads);
+    mbar_init(p_ready, 32u * static_cast<uint32_t>(active_quarters));
     mbar_init(o_ready, 1);
     mbar_init(teardown, 1);
     *abort_flag = 0;
@@ -150,7 +164,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           break;
         }
         uint8_t* st = smem + kAtKvOff + s * kAtStageBytes;
-        const int32_t ky = b * p.Sk + j * kAttnTile;
+        const int32_t ky = b * p.Sk + (j_begin + j) * kAttnTile;
         const int32_t kx = kvh * kAttnHeadDim;
         mbar_arrive_expect_tx(&k_full[s], 2u * kAtBox);
         tma_load_2d(st, &tmK, kx, ky, &k_full[s]);
@@ -243,12 +257,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     // keys [0, lim) are visible to this query (rows past Sq compute garbage and
     // store nothing)
-    const int lim = p.causal ? min(p.Sk, i + (p.Sk - p.Sq) + 1) : p.Sk;
+    const int lim = (p.causal ? min(p.Sk, i + (p.Sk - p.Sq) + 1) : p.Sk) - j_begin * kAttnTile;
+    const bool active = q < active_quarters;
     uint8_t* prow = smem + kAtPOff + r * 128;
     float m_run = -INFINITY;  // running max of the log2-scaled scores
     float l_run = 0.f;        // running sum of the bf16-rounded weights
     bool ok = true;
-    for (int j = 0; j < nblk; ++j) {
+    for (int j = 0; j < nblk && active; ++j) {
       const uint64_t limit = p.timeout_ns + 20000ull * static_cast<uint64_t>(j + 1);
       ok = mbar_wait(&s_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, limit, abort_flag);
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -259,33 +274,53 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j & 1) * kAttnTile + 32 * c, sv[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
-      // scale into log2 units, mask, row max
+      // scale into log2 units, mask (only blocks that reach past the row's
+      // visible keys), row max over 8 independent partial maxima
       const int kv = lim - j * kAttnTile;  // keys of this block visible: [0, kv)
-      float mx = -INFINITY;
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+      if (kv >= kAttnTile) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x = (32 * c + e < kv) ? __uint_as_float(sv[c][e]) * p.scale_log2 : -INFINITY;
-          sv[c][e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(sv[c][e]) * p.scale_log2;
+            sv[c][e] = __float_as_uint(x);
+            mx8[e & 7] = fmaxf(mx8[e & 7], x);
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = (32 * c + e < kv) ? __uint_as_float(sv[c][e]) * p.scale_log2 : -INFINITY;
+            sv[c][e] = __float_as_uint(x);
+            mx8[e & 7] = fmaxf(mx8[e & 7], x);
+          }
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_run, mx);
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m_run - m_use);  // 0 while nothing was visible yet
-      // weights, rounded to bf16 (the P V product's operand); l sums the rounded values
+      const float alpha = fast_exp2(m_run - m_use);  // 0 while nothing was visible yet
+      // weights, rounded to bf16 (the P V product's operand); l sums the rounded
+      // values (8 independent partial sums, added in a fixed order)
       uint32_t pk[64];
-      float rs = 0.f;
+      float rs8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = exp2f(__uint_as_float(sv[c][2 * e]) - m_use);
-          const float p1 = exp2f(__uint_as_float(sv[c][2 * e + 1]) - m_use);
+          const float p0 = fast_exp2(__uint_as_float(sv[c][2 * e]) - m_use);
+          const float p1 = fast_exp2(__uint_as_float(sv[c][2 * e + 1]) - m_use);
           const uint32_t w = pack_bf16x2(p0, p1);
           pk[16 * c + e] = w;
-          rs += bf16_lo(w) + bf16_hi(w);
+          rs8[e & 7] += bf16_lo(w) + bf16_hi(w);
         }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       l_run = l_run * alpha + rs;
       m_run = m_new;
       if (j > 0) {
@@ -321,7 +356,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
     if (!ok) *abort_flag = 1;
     // epilogue: O / l, rounded to bf16, one 256-byte row per thread
-    bool have_o = ok && nblk > 0;
+    bool have_o = ok && nblk > 0 && active;
     if (have_o) {
       const uint64_t limit = p.timeout_ns + 20000ull * static_cast<uint64_t>(nblk + 1);
       have_o = mbar_wait(o_ready, static_cast<uint32_t>(nblk - 1) & 1u, limit, abort_flag);
@@ -335,9 +370,33 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     grid_dependency_wait();
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     uint16_t* orow = p.O + static_cast<int64_t>(b * p.Sq + i) * p.ldo + h * kAttnHeadDim;
-    const bool store = i < p.Sq && !*abort_flag;
+    const bool store = active && i < p.Sq && !*abort_flag;
+    if (p.n_splits > 1) {
+      // normalised fp32 part and the log2-sum-exp of this split's scores
+      const int64_t prow = (static_cast<int64_t>(split) * p.B * p.Sq + b * p.Sq + i) * p.H + h;
+      if (store) p.part_lse[prow] = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+      float* po = p.part_o + prow * kAttnHeadDim;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4 && active; ++c) {
+        uint32_t ov[32];
+        if (have_o) {
+          tmem_ld_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
+          tmem_ld_wait(ov);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+        if (store) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<float4*>(po + 32 * c + 4 * g) =
+                make_float4(__uint_as_float(ov[4 * g]) * inv, __uint_as_float(ov[4 * g + 1]) * inv,
+                            __uint_as_float(ov[4 * g + 2]) * inv, __uint_as_float(ov[4 * g + 3]) * inv);
+        }
+      }
+    }
+#pragma unroll 1
+    for (int c = 0; c < 4 && active && p.n_splits == 1; ++c) {
       uint32_t ov[32];
       if (have_o) {
         tmem_ld_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
@@ -368,7 +427,58 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   }
 }
 
+// One warp per (output row, head): weights 2^(lse_s - max) over the splits
+// (lane s holds split s), then each lane sums 4 of the 128 columns over the
+// splits in split order and stores them as bf16.  A row no split saw is 0.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Sq * p.H;
+  grid_dependency_wait();
+  if (unit >= rows) return;
+  const int64_t row = unit / p.H;  // b * Sq + i
+  const int h = static_cast<int>(unit % p.H);
+  const int64_t split_stride = rows;
+  const float l = lane < p.n_splits ? p.part_lse[lane * split_stride + unit] : -INFINITY;
+  float mx = l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  const float w = mx == -INFINITY ? 0.f : fast_exp2(l - mx);
+  float tot = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < p.n_splits; ++sp) {
+    const float ws = __shfl_sync(0xFFFFFFFFu, w, sp);
+    if (ws == 0.f) continue;
+    const float4 v = *reinterpret_cast<const float4*>(p.part_o + (sp * split_stride + unit) * kAttnHeadDim + 4 * lane);
+    acc.x += ws * v.x;
+    acc.y += ws * v.y;
+    acc.z += ws * v.z;
+    acc.w += ws * v.w;
+  }
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  uint2 out;
+  out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(p.O + row * p.ldo + h * kAttnHeadDim + 4 * lane) = out;
+}
+
 }  // namespace
+
+cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.B) * p.Sq * p.H;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p);
+}
 
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, cudaStream_t stream) {
@@ -378,7 +488,7 @@ cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, con
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t grid = static_cast<int64_t>(p.q_tiles) * p.H * p.B;
+  const int64_t grid = static_cast<int64_t>(p.q_tiles) * p.H * p.B * p.n_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kAtThreads, 1, 1);

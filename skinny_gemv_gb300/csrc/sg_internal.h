@@ -192,9 +192,21 @@ struct AttnParams {
   float scale_log2;      // softmax scale x log2(e)
   uint16_t* O;           // bf16 output, rows b * Sq + i, head h at columns 128 h
   int64_t ldo;           // elements between consecutive rows of O
+  // Split along the keys (n_splits > 1): CTA split s of a tile takes key blocks
+  // [s * split_blocks, (s + 1) * split_blocks) and writes its normalised fp32
+  // output part_o[((s * B * Sq + row) * H + h) * 128 + d] and the log2-sum-exp
+  // of its scores part_lse[(s * B * Sq + row) * H + h] (-inf: no visible key);
+  // attn_combine merges the splits.
+  int32_t n_splits;
+  int32_t split_blocks;
+  float* part_o;
+  float* part_lse;
   DeviceError* err;
   uint64_t timeout_ns;
 };
+
+// Merges the n_splits partial results of a split launch into O (bf16).
+cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream);
 
 cudaError_t launch_attention(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, cudaStream_t stream);

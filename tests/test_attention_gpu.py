@@ -80,9 +80,11 @@ def test_zero_queries_average_values(Sq, Sk, causal):
     Vb = bf16(rng.integers(-8, 9, size=(B, Sk, H, D)).astype(np.float64))
     got = run(Qb, Kb, Vb, causal)
     ref = oracle.attention(Qb, Kb, Vb, causal=causal)
-    # every weight is exactly 1: O = (fp32 sum of small integers) / count, rounded once to bf16
+    # every weight is exactly 1: O is the mean of small integers, rounded to bf16 (one
+    # bf16 step); a key split merges per-split means with fp32 weights from
+    # exp2/log2 approximations, which moves a result by ~1e-6 at most
     want = oracle._bf16_tensor(bf16(ref))
-    step = np.maximum(np.abs(want), 2.0 ** -126) * 2.0 ** -7
+    step = np.abs(want) * 2.0 ** -7 + 1e-5
     assert np.all(np.abs(got - want) <= step), f"max |d| {np.abs(got - want).max()}"
 
 
