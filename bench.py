@@ -511,7 +511,9 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         names = [n for n in syn.WORKLOADS if n.startswith("dec")] + ["sq2048", "mlp_up", "mlp_down", "sq8192"]
         names += list(syn.GATED_WORKLOADS) + list(syn.RESIDUAL_WORKLOADS) + list(syn.BATCHED_WORKLOADS)
         names += ["fp4_sq4096", "fp4_sq8192", "fp4_sq16384"]
+        names += ["attn_causal_4096", "attn_4096", "attn_decode_4096"]
     fp4_names = [n for n in names if n in syn.NVFP4_WORKLOADS]
+    attn_names = [n for n in names if n in syn.ATTENTION_WORKLOADS]
     gated_names = [n for n in names if n in syn.GATED_WORKLOADS]
     resid_names = [n for n in names if n in syn.RESIDUAL_WORKLOADS]
     batched_names = [n for n in names if n in syn.BATCHED_WORKLOADS]
@@ -659,6 +661,51 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         out.append(row)
         del sets, C
         torch.cuda.empty_cache()
+    for name in attn_names:
+        aw = syn.ATTENTION_WORKLOADS[name]
+        with torch.cuda.stream(stream):
+            gen.manual_seed(6000 + aw.cfg)
+            dev = stream.device
+
+            def act(S, heads):
+                return torch.randn((aw.B, S, heads, aw.D), generator=gen, device=dev).to(torch.bfloat16)
+
+            per_set = 2 * aw.D * aw.B * (2 * aw.Sq * aw.H + 2 * aw.Sk * aw.Hkv)
+            nrot = rotation_count(per_set, l2)
+            sets = [(act(aw.Sq, aw.H), act(aw.Sk, aw.Hkv), act(aw.Sk, aw.Hkv), act(aw.Sq, aw.H)) for _ in range(nrot)]
+        stream.synchronize()
+        fns = [(lambda q=q, k=k, v=v, o=o: sg.attention_bf16(q, k, v, O=o, causal=aw.causal, stream=stream))
+               for q, k, v, o in sets]
+        total = time_launches(torch, stream, fns, steps, 5)
+        med = total / steps
+        row = {"workload": name, "entry": "attention_bf16", "B": aw.B, "Sq": aw.Sq, "Sk": aw.Sk, "H": aw.H,
+               "Hkv": aw.Hkv, "D": aw.D, "causal": aw.causal, "us": med * 1e3}
+        if aw.Sq >= 128:  # prefill: tensor-bound, FLOPs over the visible pairs
+            row["tflops"] = aw.flops / (med / 1e3) / 1e12
+            rpeak, rkey = tensor_peak(peaks, total)
+            row["frac_of_peak"] = row["tflops"] / rpeak
+            row["peak"] = rkey
+        else:  # decode: K and V streamed once
+            byts = aw.kv_bytes + 2 * 2 * aw.B * aw.Sq * aw.H * aw.D
+            row["gbs"] = byts / (med / 1e3) / 1e9
+            row["frac_of_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+        # torch's own scaled_dot_product_attention on the same inputs, for context
+        q0, k0, v0, _ = sets[0]
+        tq, tk, tv = (t.transpose(1, 2) for t in (q0, k0, v0))
+        sdpa_causal = aw.causal and aw.Sq == aw.Sk
+        if aw.causal and aw.Sq != aw.Sk and aw.Sq != 1:
+            sdpa_causal = None  # bottom-right causal has no plain sdpa flag
+        if sdpa_causal is not None:
+            try:
+                with torch.cuda.stream(stream):
+                    tfn = [lambda: torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=sdpa_causal)]
+                    row["torch_sdpa_us"] = time_launches(torch, stream, tfn, min(steps, 50), 3) / min(steps, 50) * 1e3
+            except RuntimeError as e:  # a comparison only: never fail the bench on it
+                row["torch_sdpa_us"] = None
+                row["torch_sdpa_error"] = str(e).splitlines()[0][:120]
+        out.append(row)
+        del sets
+        torch.cuda.empty_cache()
     return out
 
 
@@ -720,7 +767,7 @@ def run_rows_only(args, local):
     names = [n.strip() for n in args.rows_only.split(",") if n.strip()]
     unknown = [n for n in names if n not in syn.WORKLOADS and n not in syn.GATED_WORKLOADS
                and n not in syn.RESIDUAL_WORKLOADS and n not in syn.BATCHED_WORKLOADS
-               and n not in syn.NVFP4_WORKLOADS]
+               and n not in syn.NVFP4_WORKLOADS and n not in syn.ATTENTION_WORKLOADS]
     if unknown or not names:
         raise SystemExit(f"unknown workloads: {unknown or args.rows_only!r}")
     import torch

@@ -8,23 +8,27 @@
 // rounded to bf16 for the second product, causal tiles above the diagonal never
 // loaded, the heaviest query tiles launched first).
 //
-// One CTA per (128-row query tile, head, batch).  Roles:
+// One CTA per (128-row query tile, head, batch), or per key split of one.
+// Roles:
 //   warp 0     TMA producer: the Q tile once (two 64-column boxes, 128-byte
 //              swizzle), then per key block a K tile and a V tile (128 keys x
-//              128 columns each) into a 2-stage ring
+//              128 columns each) into a 3-stage ring
 //   warp 1     TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T into one
-//              of two 128-column TMEM buffers (K-major A and B), then, once the
-//              softmax has written P_j, O += P_j V_j into a third 128-column
-//              buffer; V is the B operand in MN-major form (the key rows of the
-//              V tile as written by TMA), so nothing is transposed
-//   warps 2-5  softmax, one query row per thread (its TMEM lane): S row -> scale,
-//              mask, running max m and sum l -> P row as bf16 into shared memory
-//              in the 128-byte-swizzled K-major layout the MMA reads; when m grows
-//              the O row is rescaled in TMEM (load, multiply, store) after the
-//              previous P V product completed; at the end O / l is rounded to
-//              bf16 and stored
-// S_{j+1} is issued before P_j V_j, so the next block's Q K^T overlaps the
-// softmax of this one.
+//              of two 128-column TMEM buffers (K-major A and B from shared
+//              memory), then, once the softmax has written P_j, O += P_j V_j with
+//              P read from TMEM and V the B operand in MN-major form (the key rows
+//              of the V tile as TMA wrote them), so nothing is transposed
+//   warps 2-9  softmax, two threads per query row (the row's TMEM lane; warps w
+//              and w + 4 share a lane quarter and take 64 columns each, swapping
+//              row maxima through shared memory): S row -> scale, mask, running
+//              max and sum -> P row as bf16 into one of two TMEM P buffers; at the
+//              end O / l is rounded to bf16 and stored
+// TMEM columns: S buffers [0, 128) and [128, 256), O [256, 384), P buffers
+// [384, 448) and [448, 512) (bf16 pairs).  The tensor core runs S_{j+1} and
+// P_j V_j while the softmax works on block j + 1: the softmax never waits for a
+// P V product unless the row max grew by more than 2^8 since the max its weights
+// are taken against, when O must be rescaled first (the weights themselves stay
+// below 2^8, which bf16 and the fp32 sums hold exactly enough).
 //
 // Key j is visible to query i when j < Sk and, for a causal launch, j <= i +
 // (Sk - Sq).  A row that sees no key gets O = 0.  Scores are kept in log2 units
@@ -40,26 +44,33 @@
 namespace sg {
 namespace {
 
-constexpr int kAtStages = 2;
-constexpr int kAtThreads = 192;
-constexpr int kAtSoftmaxThreads = 128;
-constexpr int kAtBox = kAttnTile * 128;              // 128 rows x 128 bytes (64 bf16)
-constexpr int kAtQOff = 0;                           // Q: two boxes (d 0-63, 64-127)
-constexpr int kAtKvOff = 2 * kAtBox;                 // per stage: K boxes 0, 1 then V boxes 0, 1
+constexpr int kAtStages = 3;
+constexpr int kAtThreads = 320;           // warp 0 producer, warp 1 MMA, warps 2-9 softmax
+constexpr int kAtBox = kAttnTile * 128;   // 128 rows x 128 bytes (64 bf16)
+constexpr int kAtQOff = 0;                // Q: two boxes (d 0-63, 64-127)
+constexpr int kAtKvOff = 2 * kAtBox;      // per stage: K boxes 0, 1 then V boxes 0, 1
 constexpr int kAtStageBytes = 4 * kAtBox;
-constexpr int kAtPOff = kAtKvOff + kAtStages * kAtStageBytes;  // P: two boxes (keys 0-63, 64-127)
-constexpr int kAtBarOff = kAtPOff + 2 * kAtBox;
-constexpr int kAtNumBars = 1 + 3 * kAtStages + 2 + 3;          // q, k[], v[], kv_empty[], s[2], p, o, teardown
-constexpr int kAtMiscOff = kAtBarOff + kAtNumBars * 8;
+constexpr int kAtBarOff = kAtKvOff + kAtStages * kAtStageBytes;
+// q, k[], v[], kv_empty[], s_full[2], p_ready[2], pv_done[2], teardown
+constexpr int kAtNumBars = 1 + 3 * kAtStages + 2 + 2 + 2 + 1;
+constexpr int kAtXchgOff = kAtBarOff + kAtNumBars * 8;  // row maxima / sums swapped by the two halves
+constexpr int kAtMiscOff = kAtXchgOff + 256 * 4;
 constexpr int kAtSmem = kAtMiscOff + 16 + 1024;
-constexpr int kAtTmemCols = 512;                     // S buffers at 0 and 128, O at 256
+constexpr int kAtTmemCols = 512;
 constexpr uint32_t kAtOCol = 256;
+constexpr uint32_t kAtPCol = 384;         // P buffer b at kAtPCol + 64 b
+constexpr float kAtRescaleLog2 = 8.f;     // O is rescaled once the row max grows past the reference by this
 static_assert(kAtSmem <= 232448, "shared memory budget");
 static_assert(kAttnHeadDim == 128 && kAttnTile == 128, "the tile shapes below assume 128");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Named barrier `id` over `threads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // 2^x by the ex2.approx instruction (relative error about 2^-22; 2^-inf = 0).
@@ -89,9 +100,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint64_t* v_full = k_full + kAtStages;
   uint64_t* kv_empty = v_full + kAtStages;
   uint64_t* s_full = kv_empty + kAtStages;  // [2]
-  uint64_t* p_ready = s_full + 2;
-  uint64_t* o_ready = p_ready + 1;
-  uint64_t* teardown = o_ready + 1;
+  uint64_t* p_ready = s_full + 2;   // [2]: block j on p_ready[j & 1]
+  uint64_t* pv_done = p_ready + 2;  // [2]: P_j V_j complete, on pv_done[j & 1]
+  uint64_t* teardown = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAtMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kAtMiscOff + 4);
 
@@ -123,8 +134,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_ready, 32u * static_cast<uint32_t>(active_quarters));
-    mbar_init(o_ready, 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&p_ready[u], 64u * static_cast<uint32_t>(active_quarters));
+      mbar_init(&pv_done[u], 1);
+    }
     mbar_init(teardown, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -216,7 +229,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // The S buffer of block j + 1 was last read by the softmax of block j - 1,
         // which finished before p_ready of j - 1 (waited for below last round).
         if (j + 1 < nblk && !(ok = issue_s(j + 1))) break;
-        if (!mbar_wait(p_ready, static_cast<uint32_t>(j) & 1u, p.timeout_ns, abort_flag)) {
+        if (!mbar_wait(&p_ready[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p.timeout_ns, abort_flag)) {
           if (!*abort_flag) record_error(p.err, kDevTimeoutTmemEmpty, j);
           ok = false;
           break;
@@ -228,17 +241,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           break;
         }
         tc_fence_after();
-        // O += P_j V_j: K = 128 keys in 8 steps of 16 keys; P is K-major (32 bytes
-        // of a swizzle row per step), V MN-major (two 8-key atoms, 2048 bytes, per
+        // O += P_j V_j: K = 128 keys in 8 steps of 16 keys; P from TMEM (8 columns
+        // of bf16 pairs per step), V MN-major (two 8-key atoms, 2048 bytes, per
         // step; the d columns 64-127 are the next box, kAtBox further on).
         const uint32_t vaddr = base + kAtKvOff + s * kAtStageBytes + 2 * kAtBox;
+        const uint32_t pcol = tmem_base + kAtPCol + static_cast<uint32_t>(j & 1) * 64;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t poff = (kk >> 2) * kAtBox + (kk & 3) * 32;
-          tc_mma_bf16(tmem_base + kAtOCol, smem_desc_sw128(base + kAtPOff + poff),
-                      smem_desc_sw128_mn(vaddr + kk * 2048, kAtBox), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(o_ready);
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_bf16_ts(tmem_base + kAtOCol, pcol + kk * 8, smem_desc_sw128_mn(vaddr + kk * 2048, kAtBox), kIdescO,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&pv_done[j & 1]);
         tc_commit(&kv_empty[s]);
       }
       if (!ok) *abort_flag = 1;
@@ -251,38 +263,47 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    // Two warps per TMEM lane quarter: warps 2-5 take columns 0-63 of their rows,
+    // warps 6-9 columns 64-127; the two threads of a row swap their row maxima
+    // through shared memory once per block (named barrier 1 + quarter).
     const int q = warp & 3;                // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;      // which 64 columns of the row
     const int r = q * 32 + lane;           // query row of the tile = TMEM lane
     const int i = q0 + r;                  // query index in the sequence
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    // keys [0, lim) are visible to this query (rows past Sq compute garbage and
-    // store nothing)
-    const int lim = (p.causal ? min(p.Sk, i + (p.Sk - p.Sq) + 1) : p.Sk) - j_begin * kAttnTile;
+    const uint32_t col0 = static_cast<uint32_t>(half * 64);
+    // [2 halves][128 rows]: a value written for block j is read before the partner
+    // passes the pair barrier at the start of block j + 1, so one buffer serves
+    float* xchg = reinterpret_cast<float*>(smem + kAtXchgOff);
+    // keys [0, lim) of this CTA's range are visible to this query (rows past Sq
+    // compute garbage and store nothing)
+    const int lim = (p.causal ? min(p.Sk, i + (p.Sk - p.Sq) + 1) : p.Sk) - j_begin * kAttnTile - half * 64;
     const bool active = q < active_quarters;
-    uint8_t* prow = smem + kAtPOff + r * 128;
-    float m_run = -INFINITY;  // running max of the log2-scaled scores
-    float l_run = 0.f;        // running sum of the bf16-rounded weights
+    float m_run = -INFINITY;  // the row's reference max (log2 units) the weights are taken against
+    float l_run = 0.f;        // running sum of this thread's bf16-rounded weights
     bool ok = true;
     for (int j = 0; j < nblk && active; ++j) {
       const uint64_t limit = p.timeout_ns + 20000ull * static_cast<uint64_t>(j + 1);
       ok = mbar_wait(&s_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, limit, abort_flag);
-      ok = __all_sync(0xFFFFFFFFu, ok);
+      // both warps of the pair take the same decision (so both reach the same barriers)
+      ok = !bar_sync_or(1 + q, 64, !ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv[4][32];
+      uint32_t sv[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j & 1) * kAttnTile + 32 * c, sv[c]);
+      for (int c = 0; c < 2; ++c)
+        tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(j & 1) * kAttnTile + col0 + 32 * c, sv[c]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
-      // scale into log2 units, mask (only blocks that reach past the row's
-      // visible keys), row max over 8 independent partial maxima
-      const int kv = lim - j * kAttnTile;  // keys of this block visible: [0, kv)
+      for (int c = 0; c < 2; ++c) tmem_ld_wait(sv[c]);
+      // scale into log2 units, mask (only where the block reaches past the row's
+      // visible keys), max over 8 independent partial maxima
+      const int kv = lim - j * kAttnTile;  // columns of this half visible: [0, kv)
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-      if (kv >= kAttnTile) {
+      if (kv >= 64) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float x = __uint_as_float(sv[c][e]) * p.scale_log2;
@@ -291,7 +312,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           }
       } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float x = (32 * c + e < kv) ? __uint_as_float(sv[c][e]) * p.scale_log2 : -INFINITY;
@@ -299,19 +320,27 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             mx8[e & 7] = fmaxf(mx8[e & 7], x);
           }
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m_run, mx);
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // the row max: this half's and the other half's
+      float* xb = xchg;
+      xb[half * 128 + r] = mx;
+      named_bar_sync(1 + q, 64);
+      mx = fmaxf(mx, xb[(half ^ 1) * 128 + r]);
+      // The reference moves only when the row max passes it by more than 2^8 (so
+      // on the first block that shows a key); the two halves decide alike.
+      const bool move = mx > m_run + kAtRescaleLog2;
+      const float m_new = move ? mx : m_run;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = fast_exp2(m_run - m_use);  // 0 while nothing was visible yet
+      const float alpha = move ? fast_exp2(m_run - m_use) : 1.f;  // 0 while nothing was visible yet
       // weights, rounded to bf16 (the P V product's operand); l sums the rounded
       // values (8 independent partial sums, added in a fixed order)
-      uint32_t pk[64];
+      uint32_t pk[32];
       float rs8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float p0 = fast_exp2(__uint_as_float(sv[c][2 * e]) - m_use);
@@ -323,44 +352,48 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       l_run = l_run * alpha + rs;
       m_run = m_new;
-      if (j > 0) {
-        // P_{j-1} V_{j-1} must be complete before O is rescaled and P rewritten.
-        ok = mbar_wait(o_ready, static_cast<uint32_t>(j - 1) & 1u, limit, abort_flag);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+      // P buffer j & 1 was read by P_{j-2} V_{j-2}; rescaling O needs P_{j-1} V_{j-1}
+      // done.  Rows (and so `need`) are the same in both warps of the pair.
+      const bool need = j > 0 && __any_sync(0xFFFFFFFFu, move);
+      bool okw = true;
+      if (j >= 2) okw = mbar_wait(&pv_done[j & 1], (static_cast<uint32_t>(j - 2) >> 1) & 1u, limit, abort_flag);
+      if (need && okw)
+        okw = mbar_wait(&pv_done[(j - 1) & 1], (static_cast<uint32_t>(j - 1) >> 1) & 1u, limit, abort_flag);
+      ok = !bar_sync_or(1 + q, 64, !okw);
+      if (!ok) break;
+      tc_fence_after();
+      if (need) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
-            tmem_ld_wait(ov);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(lane_base + kAtOCol + col0 + 32 * c, ov);
+          tmem_ld_wait(ov);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
-          }
-          tmem_st_wait();
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st_32x32b_x32(lane_base + kAtOCol + col0 + 32 * c, ov);
         }
       }
-      // P row into the 128-byte-swizzled K-major tile: keys 64 c2 .. 64 c2 + 63 in
-      // box c2, 16-byte chunk cc of the row at position cc ^ (r % 8).
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const int c2 = ch >> 3, cc = ch & 7;
-        uint4* dst = reinterpret_cast<uint4*>(prow + c2 * kAtBox + ((cc ^ (r & 7)) << 4));
-        *dst = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
-      fence_proxy_async_smem();  // the MMA reads P through the async proxy
-      tc_fence_before();         // order the O stores before the MMA thread's next products
-      mbar_arrive(p_ready);
+      // this half of the P row: keys 64 half + 2c, 2c + 1 in column 32 half + c of
+      // P buffer j & 1
+      tmem_st_32x32b_x32(lane_base + kAtPCol + static_cast<uint32_t>(j & 1) * 64 + 32 * half, pk);
+      tmem_st_wait();
+      tc_fence_before();  // order the TMEM stores before the MMA thread's next products
+      mbar_arrive(&p_ready[j & 1]);
     }
     if (!ok) *abort_flag = 1;
-    // epilogue: O / l, rounded to bf16, one 256-byte row per thread
+    // the row's total weight: both halves' sums
+    if (active) {
+      float* xl = xchg;  // the last block's reads finished before its closing pair barrier
+      xl[half * 128 + r] = l_run;
+      named_bar_sync(1 + q, 64);
+      l_run += xl[(half ^ 1) * 128 + r];
+    }
+    // epilogue: O / l, rounded to bf16 (or the fp32 part of a key split)
     bool have_o = ok && nblk > 0 && active;
     if (have_o) {
       const uint64_t limit = p.timeout_ns + 20000ull * static_cast<uint64_t>(nblk + 1);
-      have_o = mbar_wait(o_ready, static_cast<uint32_t>(nblk - 1) & 1u, limit, abort_flag);
-      have_o = __all_sync(0xFFFFFFFFu, have_o);
+      have_o = mbar_wait(&pv_done[(nblk - 1) & 1], (static_cast<uint32_t>(nblk - 1) >> 1) & 1u, limit, abort_flag);
+      have_o = !bar_sync_or(1 + q, 64, !have_o);
       if (!have_o) {
         if (!*abort_flag) record_error(p.err, kDevTimeoutTmemFull, nblk);
         *abort_flag = 1;
@@ -369,18 +402,17 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
     grid_dependency_wait();
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    uint16_t* orow = p.O + static_cast<int64_t>(b * p.Sq + i) * p.ldo + h * kAttnHeadDim;
     const bool store = active && i < p.Sq && !*abort_flag;
     if (p.n_splits > 1) {
       // normalised fp32 part and the log2-sum-exp of this split's scores
-      const int64_t prow = (static_cast<int64_t>(split) * p.B * p.Sq + b * p.Sq + i) * p.H + h;
-      if (store) p.part_lse[prow] = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
-      float* po = p.part_o + prow * kAttnHeadDim;
+      const int64_t prw = (static_cast<int64_t>(split) * p.B * p.Sq + b * p.Sq + i) * p.H + h;
+      if (store && half == 0) p.part_lse[prw] = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+      float* po = p.part_o + prw * kAttnHeadDim + col0;
 #pragma unroll 1
-      for (int c = 0; c < 4 && active; ++c) {
+      for (int c = 0; c < 2 && active; ++c) {
         uint32_t ov[32];
         if (have_o) {
-          tmem_ld_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
+          tmem_ld_32x32b_x32(lane_base + kAtOCol + col0 + 32 * c, ov);
           tmem_ld_wait(ov);
         } else {
 #pragma unroll
@@ -394,26 +426,28 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                             __uint_as_float(ov[4 * g + 2]) * inv, __uint_as_float(ov[4 * g + 3]) * inv);
         }
       }
-    }
+    } else {
+      uint16_t* orow = p.O + static_cast<int64_t>(b * p.Sq + i) * p.ldo + h * kAttnHeadDim + col0;
 #pragma unroll 1
-    for (int c = 0; c < 4 && active && p.n_splits == 1; ++c) {
-      uint32_t ov[32];
-      if (have_o) {
-        tmem_ld_32x32b_x32(lane_base + kAtOCol + 32 * c, ov);
-        tmem_ld_wait(ov);
-      } else {
+      for (int c = 0; c < 2 && active; ++c) {
+        uint32_t ov[32];
+        if (have_o) {
+          tmem_ld_32x32b_x32(lane_base + kAtOCol + col0 + 32 * c, ov);
+          tmem_ld_wait(ov);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ov[e] = 0u;
-      }
-      if (store) {
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+        if (store) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(ov[8 * g + 0]) * inv, __uint_as_float(ov[8 * g + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(ov[8 * g + 2]) * inv, __uint_as_float(ov[8 * g + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(ov[8 * g + 4]) * inv, __uint_as_float(ov[8 * g + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(ov[8 * g + 6]) * inv, __uint_as_float(ov[8 * g + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * g) = v;
+          for (int g = 0; g < 4; ++g) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ov[8 * g + 0]) * inv, __uint_as_float(ov[8 * g + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(ov[8 * g + 2]) * inv, __uint_as_float(ov[8 * g + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(ov[8 * g + 4]) * inv, __uint_as_float(ov[8 * g + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(ov[8 * g + 6]) * inv, __uint_as_float(ov[8 * g + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * g) = v;
+          }
         }
       }
     }

@@ -273,6 +273,19 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]^T, bf16 inputs, fp32 accumulator, one CTA: A
+// is read from TMEM (row m in lane m, two consecutive k per 32-bit column, the
+// lower k in the low half).
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= (A . SFA) . (B . SFB)^T for packed FP4 (E2M1) operands with one
 // E4M3 scale per 16 elements of K (kind::mxf4nvf4, scale_vec::4X), fp32 D, one
 // CTA, K = 64 per instruction.  Scale row r of A is read from TMEM lane r, column

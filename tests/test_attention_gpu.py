@@ -191,3 +191,10 @@ def test_workload_sampled(name):
         sub = (slice(None), slice(i, i + 1), heads)
         kv = (slice(None), slice(0, n), heads // (w.H // w.Hkv))
         assert_close(got[sub], Qb[sub], Kb[kv], Vb[kv], False, label=f"{name} row {i}")
+
+
+@pytest.mark.parametrize("scale", [-0.08, 0.0, 0.3])
+def test_negative_zero_and_large_scales(scale):
+    Qb, Kb, Vb = seeded(1, 200, 2, 500), seeded(1, 260, 2, 501), seeded(1, 260, 2, 502)
+    got = run(Qb, Kb, Vb, True, scale=scale)
+    assert_close(got, Qb, Kb, Vb, True, scale=scale, label=f"scale {scale}")
