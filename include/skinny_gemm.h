@@ -230,6 +230,16 @@ SG_API int gemm_nvfp4(const void *A, const void *SFA, const void *B, const void 
                       int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                       float alpha, sg_stream_t stream);
 
+/* gemm_nvfp4 with the kernel named: SG_PATH_GEMM (one CTA per 128 x 256 tile),
+ * SG_PATH_GEMM_PAIR (a cluster of two CTAs per 256 x 256 tile, tcgen05
+ * cta_group::2) or SG_PATH_AUTO (gemm_nvfp4's choice: the one-CTA kernel).  Any
+ * other path: SG_ERR_INVALID_ARG.  The two kernels add the fp32 products in
+ * different orders, so their results may differ in the last bits; each gives the
+ * same bits on every run. */
+SG_API int gemm_nvfp4_path(const void *A, const void *SFA, const void *B, const void *SFB, void *C,
+                           int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                           float alpha, int path, sg_stream_t stream);
+
 /* Bytes of a scale-atom buffer for `rows` rows and K elements of K (-1 if negative). */
 SG_API int64_t nvfp4_scale_bytes(int64_t rows, int64_t K);
 
@@ -407,9 +417,12 @@ SG_API int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t ent
  * counts outputs (each from one gate and one up weight row). */
 SG_API int sg_plan_swiglu(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_plan_info *out);
 
-/* The plan gemm_nvfp4 uses: 128 x 256 tiles, 256 of K per stage, whole tiles
- * round-robin over one CTA per SM (tile_k counts fp4 elements). */
-SG_API int sg_plan_nvfp4(int64_t M, int64_t N, int64_t K, int32_t num_sms, sg_plan_info *out);
+/* The plan gemm_nvfp4_path uses for `path` (SG_PATH_AUTO, SG_PATH_GEMM or
+ * SG_PATH_GEMM_PAIR): whole tiles round-robin, 256 of K per stage (tile_k counts
+ * fp4 elements); 128 x 256 tiles over one CTA per SM (SG_PATH_GEMM), or 256 x 256
+ * tiles over clusters of two CTAs (SG_PATH_GEMM_PAIR; `grid` counts clusters).
+ * SG_PATH_AUTO takes the one-CTA kernel.  num_sms >= 2. */
+SG_API int sg_plan_nvfp4(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t path, sg_plan_info *out);
 
 /*
  * sg_plan_item -- work item `index` of CTA `cta` under a tcgen05 plan from sg_plan:

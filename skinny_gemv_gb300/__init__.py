@@ -111,7 +111,9 @@ def load(build_if_missing: bool = False):
     lib.nvfp4_scale_bytes.restype = i64
     lib.nvfp4_pack_scales.argtypes = [p, i64, i64, i64, p, p]
     lib.nvfp4_pack_scales.restype = ctypes.c_int
-    lib.sg_plan_nvfp4.argtypes = [i64, i64, i64, i32, ctypes.POINTER(PlanInfo)]
+    lib.sg_plan_nvfp4.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.gemm_nvfp4_path.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, p]
+    lib.gemm_nvfp4_path.restype = ctypes.c_int
     lib.attention_bf16.argtypes = [p, p, p, p] + [i64] * 10 + [ctypes.c_int, ctypes.c_float, p]
     lib.attention_bf16.restype = ctypes.c_int
     lib.sg_plan_nvfp4.restype = ctypes.c_int
@@ -308,7 +310,8 @@ def nvfp4_pack_scales(plain, K: int | None = None, atoms=None, stream=None):
     return atoms
 
 
-def gemm_nvfp4(A, SFA, B, SFB, K: int | None = None, C=None, alpha: float = 1.0, stream=None):
+def gemm_nvfp4(A, SFA, B, SFB, K: int | None = None, C=None, alpha: float = 1.0, stream=None,
+               path: int = PATH_AUTO):
     """C[M, N] (fp16) = alpha * (A . SFA) @ (B . SFB)^T for packed E2M1 operands
     (uint8 [M, >= K/2] and [N, >= K/2]) and their E4M3 scale atoms (from
     nvfp4_pack_scales)."""
@@ -329,9 +332,9 @@ def gemm_nvfp4(A, SFA, B, SFB, K: int | None = None, C=None, alpha: float = 1.0,
         raise ValueError(f"C must be a float16 CUDA tensor of shape {(M, N)}")
     ldc = max(C.stride(0), N)
     with torch.cuda.device(A.device):
-        st = load().gemm_nvfp4(a_ptr, SFA.data_ptr(), b_ptr, SFB.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc,
-                               float(alpha), _stream_handle(stream))
-    _check(st, "gemm_nvfp4")
+        st = load().gemm_nvfp4_path(a_ptr, SFA.data_ptr(), b_ptr, SFB.data_ptr(), C.data_ptr(), M, N, K, lda, ldb,
+                                    ldc, float(alpha), int(path), _stream_handle(stream))
+    _check(st, "gemm_nvfp4_path")
     return C
 
 
@@ -420,9 +423,9 @@ def plan(M: int, N: int, K: int, num_sms: int, entry: int = 0) -> dict:
     return d
 
 
-def plan_nvfp4(M: int, N: int, K: int, num_sms: int) -> dict:
+def plan_nvfp4(M: int, N: int, K: int, num_sms: int, path: int = PATH_AUTO) -> dict:
     info = PlanInfo()
-    _check(load().sg_plan_nvfp4(M, N, K, num_sms, ctypes.byref(info)), "sg_plan_nvfp4")
+    _check(load().sg_plan_nvfp4(M, N, K, num_sms, path, ctypes.byref(info)), "sg_plan_nvfp4")
     d = info.as_dict()
     d["_struct"] = info
     return d

@@ -574,36 +574,50 @@ int run_batched(DeviceState& d, int dev, const void* A, int64_t M, int64_t K, in
 
 // NVFP4 plan: 128 x 256 tiles, 256 of K per stage, whole tiles round-robin over
 // one CTA per SM in a grouped raster.
-void plan_nvfp4(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o) {
+// NVFP4 kernel choice: the one-CTA kernel unless the pairs are asked for (they
+// measured slower at every size tried: 64.6 against 39.6 us at 4096^3).
+bool nvfp4_pair(int64_t, int path) { return path == SG_PATH_GEMM_PAIR; }
+
+void plan_nvfp4(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
-  o->path = SG_PATH_GEMM;
-  o->tile_m = kF4TileM;
+  o->path = pair ? SG_PATH_GEMM_PAIR : SG_PATH_GEMM;
+  o->tile_m = pair ? 2 * kF4TileM : kF4TileM;
   o->tile_n = kF4TileN;
   o->tile_k = kF4StageK;
-  o->stages = kF4Stages;
-  o->cluster_size = 1;
+  o->stages = pair ? 5 : kF4Stages;
+  o->cluster_size = pair ? 2 : 1;
   o->ctas_per_sm = 1;
   Schedule s{};
-  s.tiles_m = static_cast<int32_t>(ceil_div(M, kF4TileM));
+  s.tiles_m = static_cast<int32_t>(ceil_div(M, o->tile_m));
   s.tiles_n = static_cast<int32_t>(ceil_div(N, kF4TileN));
   s.k_steps = static_cast<int32_t>(ceil_div(K, kF4StageK));
   s.group_m = std::max<int32_t>(1, std::min<int32_t>(s.tiles_m, 8));
   const int64_t T = static_cast<int64_t>(s.tiles_m) * s.tiles_n;
-  s.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(T, sms)));
+  const int64_t units = pair ? sms / 2 : sms;  // clusters or CTAs
+  s.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(T, units)));
   s.dp_tiles = static_cast<int32_t>(T);
   fill_sched(o, s);
   o->split_k = 0;
-  o->wave_efficiency = wave_efficiency(T, sms);
+  o->wave_efficiency = wave_efficiency(T, units);
 }
 
 int run_nvfp4(DeviceState& d, int dev, const void* A, const void* SFA, const void* B, const void* SFB, void* C,
               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, float alpha,
-              cudaStream_t stream) {
+              bool pair, cudaStream_t stream) {
   sg_plan_info plan;
-  plan_nvfp4(M, N, K, d.sm_count, &plan);
-  CUtensorMap ta, tb;
+  plan_nvfp4(M, N, K, d.sm_count, pair, &plan);
+  const int64_t kc = ceil_div(K, 64);
+  CUtensorMap ta, tb, tsa, tsb;
   int st = make_map(&ta, A, M, K / 2, lda, kF4TileM, 128, CU_TENSOR_MAP_SWIZZLE_128B, dev, 1);
-  if (st == SG_OK) st = make_map(&tb, B, N, K / 2, ldb, kF4TileN, 128, CU_TENSOR_MAP_SWIZZLE_128B, dev, 1);
+  if (st == SG_OK)
+    st = make_map(&tb, B, N, K / 2, ldb, pair ? kF4TileN / 2 : kF4TileN, 128, CU_TENSOR_MAP_SWIZZLE_128B, dev, 1);
+  if (pair) {
+    // scale atoms as rows of 256 bytes, 8 rows (4 atoms, one stage) per box
+    if (st == SG_OK)
+      st = make_map(&tsa, SFA, 2 * ceil_div(M, 128) * kc, 256, 256, 8, 256, CU_TENSOR_MAP_SWIZZLE_NONE, dev, 1);
+    if (st == SG_OK)
+      st = make_map(&tsb, SFB, 2 * ceil_div(N, 128) * kc, 256, 256, 8, 256, CU_TENSOR_MAP_SWIZZLE_NONE, dev, 1);
+  }
   if (st != SG_OK) return st;
   F4Params p{};
   p.M = static_cast<int32_t>(M);
@@ -619,7 +633,7 @@ int run_nvfp4(DeviceState& d, int dev, const void* A, const void* SFA, const voi
   p.sched = sched_from_plan(plan);
   p.err = d.err;
   p.timeout_ns = g_timeout_ns.load();
-  const cudaError_t e = launch_f4_gemm(ta, tb, p, stream);
+  const cudaError_t e = pair ? launch_f4_gemm_pair(ta, tb, tsa, tsb, p, stream) : launch_f4_gemm(ta, tb, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
@@ -816,8 +830,9 @@ int nvfp4_pack_scales(const void* plain, int64_t rows, int64_t K, int64_t ld, vo
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
-int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int64_t M, int64_t N,
-               int64_t K, int64_t lda, int64_t ldb, int64_t ldc, float alpha, sg_stream_t stream) {
+int gemm_nvfp4_path(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldc, float alpha, int path, sg_stream_t stream) {
+  if (path != SG_PATH_AUTO && path != SG_PATH_GEMM && path != SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return SG_ERR_INVALID_ARG;
   if (K % 16 != 0) return SG_ERR_INVALID_ARG;  // whole 16-element scale blocks
   if (M == 0 || N == 0) return SG_OK;
@@ -835,12 +850,18 @@ int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, v
   if (K == 0) return empty_sum(C, M, N, ldc, nullptr, 0, s);  // +0.0 in fp16 is all zero bits
   st = ensure_workspace(*d, s);
   if (st != SG_OK) return st;
-  return run_nvfp4(*d, dev, A, SFA, B, SFB, C, M, N, K, lda, ldb, ldc, alpha, s);
+  return run_nvfp4(*d, dev, A, SFA, B, SFB, C, M, N, K, lda, ldb, ldc, alpha, nvfp4_pair(M, path), s);
 }
 
-int sg_plan_nvfp4(int64_t M, int64_t N, int64_t K, int32_t num_sms, sg_plan_info* out) {
-  if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
-  plan_nvfp4(M, N, K, num_sms, out);
+int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int64_t M, int64_t N,
+               int64_t K, int64_t lda, int64_t ldb, int64_t ldc, float alpha, sg_stream_t stream) {
+  return gemm_nvfp4_path(A, SFA, B, SFB, C, M, N, K, lda, ldb, ldc, alpha, SG_PATH_AUTO, stream);
+}
+
+int sg_plan_nvfp4(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t path, sg_plan_info* out) {
+  if (!out || M < 0 || N < 0 || K < 0 || num_sms < 2) return SG_ERR_INVALID_ARG;
+  if (path != SG_PATH_AUTO && path != SG_PATH_GEMM && path != SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
+  plan_nvfp4(M, N, K, num_sms, nvfp4_pair(M, path), out);
   return SG_OK;
 }
 

@@ -172,6 +172,12 @@ struct F4Params {
 
 cudaError_t launch_f4_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const F4Params& p, cudaStream_t stream);
 
+// Paired form: clusters of two CTAs, 256 x 256 tiles (p.sched counts pair tiles
+// and clusters); tmB in 128-row boxes; tmSFA / tmSFB view the scale atoms as rows
+// of 256 bytes in boxes of 8 rows (4 atoms).
+cudaError_t launch_f4_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                               const CUtensorMap& tmSFB, const F4Params& p, cudaStream_t stream);
+
 // Plain row-major scales (rows x K/16 bytes, pitch ld) to scale atoms; padding
 // bytes (rows past `rows`, blocks past K/16) are written as 0.
 cudaError_t launch_f4_pack_scales(const uint8_t* plain, int64_t rows, int64_t K, int64_t ld, uint8_t* atoms,

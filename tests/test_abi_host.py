@@ -321,14 +321,29 @@ def test_nvfp4_scale_bytes(lib):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 8192, 8192), (300, 500, 1040), (1, 1, 16),
                                    (128, 256, 256), (16384, 16384, 16384)])
-def test_nvfp4_plan_covers_every_tile_once(lib, M, N, K):
-    info = sg.plan_nvfp4(M, N, K, 152)
-    assert (info["tile_m"], info["tile_n"], info["tile_k"]) == (128, 256, 256)
-    assert info["tiles_m"] == -(-M // 128) and info["tiles_n"] == -(-N // 256) and info["k_steps"] == -(-K // 256)
+@pytest.mark.parametrize("path", [sg.PATH_GEMM, sg.PATH_GEMM_PAIR])
+def test_nvfp4_plan_covers_every_tile_once(lib, M, N, K, path):
+    info = sg.plan_nvfp4(M, N, K, 152, path)
+    pair = path == sg.PATH_GEMM_PAIR
+    tm = 256 if pair else 128
+    assert (info["tile_m"], info["tile_n"], info["tile_k"]) == (tm, 256, 256)
+    assert info["cluster_size"] == (2 if pair else 1)
+    assert info["tiles_m"] == -(-M // tm) and info["tiles_n"] == -(-N // 256) and info["k_steps"] == -(-K // 256)
     T = info["tiles_m"] * info["tiles_n"]
-    assert info["grid"] == min(T, 152) and info["sk_tiles"] == 0 and info["dp_tiles"] == T
+    units = 76 if pair else 152
+    assert info["grid"] == min(T, units) and info["sk_tiles"] == 0 and info["dp_tiles"] == T
     items = _check_plan_coverage(info)
     assert all(k0 == 0 and k1 == info["k_steps"] for row in items for (_, k0, k1, *_) in row)
+
+
+def test_nvfp4_auto_path_is_the_one_cta_kernel(lib):
+    assert sg.plan_nvfp4(255, 4096, 4096, 152)["path"] == sg.PATH_GEMM
+    assert sg.plan_nvfp4(8192, 8192, 8192, 152)["path"] == sg.PATH_GEMM
+    assert sg.plan_nvfp4(8192, 64, 64, 152, sg.PATH_GEMM_PAIR)["path"] == sg.PATH_GEMM_PAIR
+    with pytest.raises(sg.SgError):
+        sg.plan_nvfp4(256, 256, 256, 152, sg.PATH_CUDA_CORE)
+    assert lib.gemm_nvfp4_path(16, 16, 16, 16, 16, 8, 8, 32, 16, 16, 8, 1.0, sg.PATH_CUDA_CORE, None) == \
+        sg.SG_ERR_INVALID_ARG
 
 
 # ------------------------------------------------------------------ attention

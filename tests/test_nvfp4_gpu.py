@@ -46,7 +46,7 @@ def dev(a: np.ndarray):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def run(A, SA, B, SB, M, N, K, alpha=1.0, ldc=None, lda=None, ldb=None):
+def run(A, SA, B, SB, M, N, K, alpha=1.0, ldc=None, lda=None, ldb=None, path=0):
     """Packs the scales with the library and runs gemm_nvfp4; returns fp64 [M, N].
     Row pitches default to K/2 rounded up to 16 bytes (the TMA stride rule)."""
     pitch = -(-(K // 2) // 16) * 16
@@ -59,7 +59,7 @@ def run(A, SA, B, SB, M, N, K, alpha=1.0, ldc=None, lda=None, ldb=None):
     ldc = -(-N // 8) * 8 if ldc is None else ldc
     Cfull = torch.full((M, ldc), float("nan"), dtype=torch.float16, device="cuda")
     C = Cfull[:, :N]
-    sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K, C=C, alpha=alpha)
+    sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K, C=C, alpha=alpha, path=path)
     torch.cuda.synchronize()
     st, detail = sg.check_device_errors()
     assert st == 0, detail
@@ -118,33 +118,40 @@ def _single_block(M, N, K, m_blk, seed):
     return A, SA, B, SB
 
 
+PATHS = [sg.PATH_GEMM, sg.PATH_GEMM_PAIR]  # one CTA per 128 x 256 tile; CTA pairs per 256 x 256 tile
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M,N,K,blk", [(128, 256, 256, 0), (128, 256, 256, 7), (130, 300, 512, 21),
-                                       (256, 512, 1024, 63), (77, 129, 64, 3), (300, 260, 1040, 64)])
-def test_exact_single_block(M, N, K, blk):
+                                       (256, 512, 1024, 63), (77, 129, 64, 3), (300, 260, 1040, 64),
+                                       (512, 256, 256, 2), (700, 520, 768, 40)])
+def test_exact_single_block(M, N, K, blk, path):
     A, SA, B, SB = _single_block(M, N, K, blk, 100 + blk)
     ref = oracle.gemm_nvfp4(A, SA, B, SB, K)
     assert np.array_equal(ref.astype(np.float16).astype(np.float64), ref)  # exact in fp16
-    got = run(A, SA, B, SB, M, N, K)
+    got = run(A, SA, B, SB, M, N, K, path=path)
     bad = np.argwhere(got != ref)
     assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:3].tolist()}"
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (512, 512, 512), (300, 500, 1040), (1, 256, 4096),
                                    (129, 1, 256), (1000, 700, 2048), (256, 1024, 16), (640, 640, 4096)])
-def test_parity_seeded(M, N, K):
+@pytest.mark.parametrize("path", PATHS)
+def test_parity_seeded(M, N, K, path):
     A, B = syn.nvfp4_codes(M, K, 1000 + M), syn.nvfp4_codes(N, K, 2000 + N)
     SA, SB = syn.nvfp4_scales(M, K, 3000 + M), syn.nvfp4_scales(N, K, 4000 + N)
     ref = oracle.gemm_nvfp4(A, SA, B, SB, K)
-    got = run(A, SA, B, SB, M, N, K)
-    assert_close(got, ref, K, product_rms(A, SA, B, SB, K), f"{M}x{N}x{K}")
+    got = run(A, SA, B, SB, M, N, K, path=path)
+    assert_close(got, ref, K, product_rms(A, SA, B, SB, K), f"{M}x{N}x{K} path {path}")
 
 
-def test_alpha_and_pitches():
-    M, N, K = 200, 300, 768
+@pytest.mark.parametrize("path", PATHS)
+def test_alpha_and_pitches(path):
+    M, N, K = 300, 300, 768
     A, B = syn.nvfp4_codes(M, K, 11), syn.nvfp4_codes(N, K, 12)
     SA, SB = syn.nvfp4_scales(M, K, 13), syn.nvfp4_scales(N, K, 14)
     ref = oracle.gemm_nvfp4(A, SA, B, SB, K, alpha=-0.375)
-    got = run(A, SA, B, SB, M, N, K, alpha=-0.375, ldc=320, lda=400, ldb=416)
+    got = run(A, SA, B, SB, M, N, K, alpha=-0.375, ldc=320, lda=400, ldb=416, path=path)
     assert_close(got, ref, K, 0.375 * product_rms(A, SA, B, SB, K), "alpha, pitches")
 
 
@@ -157,14 +164,15 @@ def test_zero_k_and_empty():
     assert (C == 0).all()
 
 
-def test_deterministic():
+@pytest.mark.parametrize("path", PATHS)
+def test_deterministic(path):
     M, N, K = 700, 900, 2048
     A, B = syn.nvfp4_codes(M, K, 21), syn.nvfp4_codes(N, K, 22)
     SA, SB = syn.nvfp4_scales(M, K, 23), syn.nvfp4_scales(N, K, 24)
     Ad, Bd = dev(A), dev(B)
     SAd, SBd = sg.nvfp4_pack_scales(dev(SA), K), sg.nvfp4_pack_scales(dev(SB), K)
-    c1 = sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K).clone()
-    c2 = sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K)
+    c1 = sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K, path=path).clone()
+    c2 = sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K, path=path)
     torch.cuda.synchronize()
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
 
