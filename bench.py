@@ -17,7 +17,9 @@ before.  The JSON line (printed by rank 0) carries:
                        the K back-to-back launches / K) against the measured
                        bf16 peak
   e2e                  the same metric with host buffers: each step copies A and
-                       B from pinned host memory, calls gemm_bf16 and copies C back
+                       B from pinned host memory, calls gemm_bf16 and copies C back;
+                       consecutive steps overlap (uploads of A and B, GEMM and
+                       download on four streams, two sets of device buffers)
   cpu_baseline         the fp64 oracle on a bounded row sample, on the host cores
   rows                 the other workloads (2048^3, the 7B MLP projections,
                        8192^3, the decode shapes M = 1, 2, 16, 64) and the
@@ -449,38 +451,70 @@ def sanity_gate(torch, sg, w, A, B, C, stream):
 
 
 def measure_e2e(torch, sg, w, A0, B0, stream, args, dist, world):
-    """Host buffers in, host buffer out: per step H2D of A and B from pinned memory,
-    gemm_bf16, D2H of C into pinned memory."""
+    """Host buffers in, host buffer out: every step copies A and B from pinned
+    memory to the device, runs gemm_bf16 and copies C back into pinned memory.
+    Steps are pipelined as a serving loop would run them: step i's uploads (A and
+    B on two streams), its GEMM (the bench stream) and its download (a fourth
+    stream) each
+    wait only for what they need, over two sets of device buffers, so step i + 1's
+    uploads overlap step i's GEMM and download.  The timed region runs from before
+    the first upload to after the last download."""
     M, N, K = w.M, w.N, w.K
     hA = A0.cpu().pin_memory()
     hB = B0.cpu().pin_memory()
-    hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    dA = torch.empty_like(A0)
-    dB = torch.empty_like(B0)
-    dC = torch.empty((M, N), dtype=torch.bfloat16, device=A0.device)
+    hC = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dA = [torch.empty_like(A0) for _ in range(2)]
+    dB = [torch.empty_like(B0) for _ in range(2)]
+    dC = [torch.empty((M, N), dtype=torch.bfloat16, device=A0.device) for _ in range(2)]
+    up = torch.cuda.Stream(A0.device)
+    up2 = torch.cuda.Stream(A0.device)  # A and B upload side by side (two copy engines)
+    down = torch.cuda.Stream(A0.device)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("up", "up2", "gemm", "down")}
+    used = [False, False]
 
-    def step():
-        with torch.cuda.stream(stream):
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            sg.gemm_bf16(dA, dB, dC, stream=stream)
-            hC.copy_(dC, non_blocking=True)
+    def step(i):
+        b = i % 2
+        if used[b]:  # buffer set b: its previous GEMM read dA/dB, its previous download read dC
+            up.wait_event(ev["gemm"][b])
+            up2.wait_event(ev["gemm"][b])
+        with torch.cuda.stream(up):
+            dA[b].copy_(hA, non_blocking=True)
+        with torch.cuda.stream(up2):
+            dB[b].copy_(hB, non_blocking=True)
+        ev["up"][b].record(up)
+        ev["up2"][b].record(up2)
+        stream.wait_event(ev["up"][b])
+        stream.wait_event(ev["up2"][b])
+        if used[b]:
+            stream.wait_event(ev["down"][b])
+        sg.gemm_bf16(dA[b], dB[b], dC[b], stream=stream)
+        ev["gemm"][b].record(stream)
+        down.wait_event(ev["gemm"][b])
+        with torch.cuda.stream(down):
+            hC[b].copy_(dC[b], non_blocking=True)
+        ev["down"][b].record(down)
+        used[b] = True
 
     steps = max(3, min(args.steps, 50))
-    for _ in range(3):
-        step()
-    stream.synchronize()
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
     barrier(dist)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(steps):
-        step()
+    up.wait_event(t0)
+    up2.wait_event(t0)
+    down.wait_event(t0)
+    for i in range(steps):
+        step(3 + i)
+    stream.wait_event(ev["down"][(3 + steps - 1) % 2])
     t1.record(stream)
     t1.synchronize()
     ms = max_over_ranks(dist, t0.elapsed_time(t1)) / steps
     return {"value": tflops(M, N, K, ms / 1e3) * world, "unit": "TFLOPS", "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N}
+            "steps": steps, "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N,
+            "pipelined": "uploads (A, B), GEMM and download of consecutive steps overlap on four streams"}
 
 
 ENTRIES = {"auto": None, "cuda_core": 1, "tensor_core": 2}

@@ -40,3 +40,52 @@ def test_capture_and_replay(M, N, K, fn):
         torch.cuda.synchronize()
         assert_close(to_bits(C), ref, K, f"replay {fn} {M}x{N}x{K}")
         Cbuf.view(torch.int16).fill_(0x7FC0)
+
+
+def _capture(call):
+    """Runs `call` once outside capture (first-call set-up), then captures it."""
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    return g
+
+
+@pytest.mark.parametrize("B,Sq,Sk,H,causal", [(1, 300, 300, 4, True), (1, 1, 2000, 8, True)])
+def test_attention_capture_and_replay(B, Sq, Sk, H, causal):
+    """Prefill and the key-split decode path (attention kernel plus combine kernel)."""
+    Qb = syn.matrix(B * Sq, H * 128, "normal", 61).reshape(B, Sq, H, 128)
+    Kb = syn.matrix(B * Sk, H * 128, "normal", 62).reshape(B, Sk, H, 128)
+    Vb = syn.matrix(B * Sk, H * 128, "normal", 63).reshape(B, Sk, H, 128)
+    dev = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in (Qb, Kb, Vb)]
+    O = torch.empty((B, Sq, H, 128), dtype=torch.bfloat16, device="cuda")
+    g = _capture(lambda: sg.attention_bf16(*dev, O=O, causal=causal))
+    ref = oracle.attention(Qb, Kb, Vb, causal=causal)
+    W = oracle.attention(Qb, Kb, np.abs(oracle._bf16_tensor(Vb)), causal=causal)
+    for _ in range(2):
+        O.view(torch.int16).fill_(0x7FC0)
+        g.replay()
+        torch.cuda.synchronize()
+        got = oracle._bf16_tensor(O.cpu().view(torch.int16).numpy().view(np.uint16))
+        assert np.all(np.abs(got - ref) <= 4e-3 * (np.abs(ref) + W)), "replayed attention"
+
+
+def test_nvfp4_capture_and_replay():
+    M, N, K = 512, 768, 1024
+    A, B = syn.nvfp4_codes(M, K, 71), syn.nvfp4_codes(N, K, 72)
+    SA, SB = syn.nvfp4_scales(M, K, 73), syn.nvfp4_scales(N, K, 74)
+    Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    SAd = sg.nvfp4_pack_scales(torch.from_numpy(SA).cuda(), K)
+    SBd = sg.nvfp4_pack_scales(torch.from_numpy(SB).cuda(), K)
+    C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    g = _capture(lambda: sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K, C=C))
+    C.fill_(float("nan"))
+    torch.cuda.synchronize()
+    direct = sg.gemm_nvfp4(Ad, SAd, Bd, SBd, K=K).clone()
+    C.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), direct.view(torch.int16))  # deterministic kernel: same bits
