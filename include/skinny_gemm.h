@@ -73,7 +73,7 @@ typedef enum {
 } sg_path;
 
 /*
- * gemm_bf16 -- C = A . B^T for any M, N, K (the spec entry point).
+ * gemm_bf16 -- C = A . B^T for any M, N, K (the main entry point).
  *
  * M > 64 runs the persistent tcgen05 GEMM: 128 x 256 output tiles, a TMA-fed
  * ring of 128-byte-swizzled shared-memory stages, warp-specialised producer /

@@ -1,6 +1,6 @@
 """Parity of the projection with its residual add, gemm_bf16_residual:
 C = A . B^T + R, against the fp64 oracle (oracle.gemm_residual) within the
-the benchmark spec's tolerance, on every kernel (CUDA-core and tcgen05 skinny paths,
+GEMM parity tolerance (tests/_parity.py), on every kernel (CUDA-core and tcgen05 skinny paths,
 both GEMMs), ragged shapes, a padded residual, Stream-K tiles, in place (R = C),
 the 7B-model down projection, K = 0 and argument errors."""
 import numpy as np

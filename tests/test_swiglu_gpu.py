@@ -1,6 +1,6 @@
 """Parity of the fused gate/up projection with its SwiGLU epilogue,
 gemm_bf16_swiglu: C = silu(A . Wg^T) * (A . Wu^T), against the fp64 oracle
-(oracle.swiglu), within the benchmark spec's tolerance (tests/_parity.py).  The fp32
+(oracle.swiglu), within the GEMM parity tolerance (tests/_parity.py).  The fp32
 accumulators, the fp32 SiLU and product and the bf16 rounding of the output
 keep the GPU's error near the output rounding; the tolerance is the GEMM's.
 
