@@ -195,10 +195,15 @@ def tensor_peak(peaks: dict, timed_ms: float):
     return peaks["bf16_tflops"], "bf16_tflops"
 
 
+# The sources that define the headline GEMM kernel (its translation unit and the
+# headers it includes); recorded DRAM traffic is valid while these are unchanged.
+GEMM_KERNEL_SOURCES = ("sg_gemm_tcgen05.cu", "sg_internal.h", "sg_ptx.cuh", "sg_sched.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "skinny_gemv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in GEMM_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
