@@ -365,9 +365,11 @@ SG_API void sg_set_wait_timeout_ns(uint64_t ns);
 
 /*
  * sg_debug_inject_missing_tx -- failure injection for tests of the bounded
- * waits.  The next tcgen05 GEMM launch on any device (gemm_bf16 with M > 64)
- * arms the first pipeline stage of every CTA with `bytes` more than its copies
- * deliver, so the MMA issuer's wait can never complete: the kernel gives up
+ * waits.  The next launch on any device of the tcgen05 GEMM (gemm_bf16 with
+ * M > 64), the one-CTA NVFP4 GEMM or the attention kernel arms the first
+ * pipeline stage (the first K tile, for attention) of every CTA with `bytes`
+ * more than its copies deliver, so the MMA issuer's wait can never complete:
+ * the kernel gives up
  * after the wait bound (sg_set_wait_timeout_ns), records the timeout, unwinds
  * and exits, and sg_check_device_errors then returns SG_ERR_TIMEOUT.  The
  * output of that launch is undefined.  bytes = 0 cancels a pending injection.

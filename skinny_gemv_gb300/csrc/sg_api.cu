@@ -23,7 +23,7 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
-std::atomic<uint32_t> g_inject_missing_tx{0};  // consumed by the next tcgen05 GEMM launch
+std::atomic<uint32_t> g_inject_missing_tx{0};  // consumed by the next tcgen05 GEMM, one-CTA NVFP4 or attention launch
 
 int cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -633,6 +633,7 @@ int run_nvfp4(DeviceState& d, int dev, const void* A, const void* SFA, const voi
   p.sched = sched_from_plan(plan);
   p.err = d.err;
   p.timeout_ns = g_timeout_ns.load();
+  if (!pair) p.inject_extra_tx = g_inject_missing_tx.exchange(0);
   const cudaError_t e = pair ? launch_f4_gemm_pair(ta, tb, tsa, tsb, p, stream) : launch_f4_gemm(ta, tb, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
@@ -714,6 +715,7 @@ int run_attention(DeviceState& d, int dev, const void* Q, const void* K, const v
   p.q_tiles = static_cast<int32_t>(ceil_div(Sq, kAttnTile));
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.inject_extra_tx = g_inject_missing_tx.exchange(0);
   p.O = static_cast<uint16_t*>(O);
   p.ldo = ldo;
   p.err = d.err;

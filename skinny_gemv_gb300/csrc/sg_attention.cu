@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         uint8_t* st = smem + kAtKvOff + s * kAtStageBytes;
         const int32_t ky = b * p.Sk + (j_begin + j) * kAttnTile;
         const int32_t kx = kvh * kAttnHeadDim;
-        mbar_arrive_expect_tx(&k_full[s], 2u * kAtBox);
+        mbar_arrive_expect_tx(&k_full[s], 2u * kAtBox + (j == 0 ? p.inject_extra_tx : 0u));  // + injection
         tma_load_2d(st, &tmK, kx, ky, &k_full[s]);
         tma_load_2d(st + kAtBox, &tmK, kx + 64, ky, &k_full[s]);
         mbar_arrive_expect_tx(&v_full[s], 2u * kAtBox);

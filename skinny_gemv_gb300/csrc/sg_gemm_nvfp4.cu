@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           const uint32_t sf_bytes = static_cast<uint32_t>(nch * kF4AtomBytes);
           int nrb = 0;                                // B row blocks that exist
           for (int rb = 0; rb < 2; ++rb) nrb += (2 * tn + rb < p.rb_n) ? 1 : 0;
-          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(kF4ABytes + kF4BBytes) + (1u + nrb) * sf_bytes);
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(kF4ABytes + kF4BBytes) + (1u + nrb) * sf_bytes +
+                                              (it == 0 ? p.inject_extra_tx : 0u));  // + failure injection only
           uint8_t* st = smem + s * kF4StageBytes;
           tma_load_2d(st, &tmA, ks * 128, tm * kF4TileM, &full[s]);
           tma_load_2d(st + kF4ABytes, &tmB, ks * 128, tn * kF4TileN, &full[s]);

@@ -168,6 +168,7 @@ struct F4Params {
   Schedule sched;        // whole tiles, round-robin
   DeviceError* err;
   uint64_t timeout_ns;
+  uint32_t inject_extra_tx;  // failure injection (one-CTA kernel): extra bytes expected on the first stage
 };
 
 cudaError_t launch_f4_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const F4Params& p, cudaStream_t stream);
@@ -209,6 +210,7 @@ struct AttnParams {
   float* part_lse;
   DeviceError* err;
   uint64_t timeout_ns;
+  uint32_t inject_extra_tx;  // failure injection: extra bytes expected on the first K tile
 };
 
 // Merges the n_splits partial results of a split launch into O (bf16).
