@@ -180,8 +180,8 @@ SG_API int gemm_bf16_residual_path(const void *A, const void *B, const void *R, 
  * (the pages' "next" step: amortise the ~2 us a launch costs a decode step).  A is
  * M x K (lda); B[i] is N[i] x K (ldb[i]); C[i] is M x N[i] (ldc[i]); count <= 8; the
  * arrays are host arrays of device pointers and sizes.  path: SG_PATH_AUTO (the
- * CUDA-core stream for M <= 2, else tcgen05), SG_PATH_CUDA_CORE or
- * SG_PATH_TENSOR_CORE.  Each C_i is exactly what gemv_bf16 gives for (A, B_i)
+ * CUDA-core stream for M = 1, else tcgen05), SG_PATH_CUDA_CORE (each matrix
+ * gets its own run of CTAs, in proportion to its rows) or SG_PATH_TENSOR_CORE.  Each C_i is exactly what gemv_bf16 gives for (A, B_i)
  * with the same kernel, up to the order of the fp32 sums.  Errors as gemv_bf16
  * for each matrix, plus SG_ERR_INVALID_ARG for count outside 1..8 or null arrays.
  */

@@ -22,6 +22,7 @@
 // bf16 and resets the counter.  Nothing needs clearing between calls, and a call
 // is one launch (spark-kernels, "the decode kernel": split K only when the strips
 // are too few).
+#include <algorithm>
 #include <cuda_bf16.h>
 
 #include "sg_internal.h"
@@ -51,20 +52,69 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
-// Weight row and output location of output row n (of the N rows): in a batched
-// launch, row n - row_begin[i] of matrix i.
-__device__ __forceinline__ const uint16_t* weight_row(const CcParams& p, int n) {
-  if (p.nbatch == 0) return p.B + static_cast<int64_t>(n) * p.ldb;
+// The rows [lo, hi) of the N output rows that one CTA computes, and its weights.
+// In a batched launch the host gives every matrix its own run of CTAs
+// (cta_begin), so a CTA's rows all belong to one matrix i: row n is row
+// n - first of that matrix (first = row_begin[i]).  The matrix is looked up once
+// per CTA (and again for the stores, rather than held in registers throughout).
+__device__ __forceinline__ int cta_batch(const CcParams& p) {
   int i = 0;
-  while (i + 1 < p.nbatch && n >= p.row_begin[i + 1]) ++i;
-  return p.Bs[i] + static_cast<int64_t>(n - p.row_begin[i]) * p.ldbs[i];
+#pragma unroll
+  for (int j = 1; j < kMaxBatch; ++j)
+    if (j < p.nbatch && static_cast<int>(blockIdx.x) >= p.cta_begin[j]) i = j;
+  return i;
 }
 
-__device__ __forceinline__ uint16_t* output_at(const CcParams& p, int m, int n) {
-  if (p.nbatch == 0) return p.C + static_cast<int64_t>(m) * p.ldc + n;
-  int i = 0;
-  while (i + 1 < p.nbatch && n >= p.row_begin[i + 1]) ++i;
-  return p.Cs[i] + static_cast<int64_t>(m) * p.ldcs[i] + (n - p.row_begin[i]);
+struct CtaRows {
+  const uint16_t* b;
+  int64_t ldb;
+  int first, lo, hi;
+};
+
+template <bool BATCHED>
+__device__ __forceinline__ CtaRows cta_rows(const CcParams& p) {
+  CtaRows t;
+  if constexpr (!BATCHED) {
+    t.b = p.B;
+    t.ldb = p.ldb;
+    t.first = 0;
+    t.lo = static_cast<int>((static_cast<int64_t>(blockIdx.x) * p.N) / p.grid_rows);
+    t.hi = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * p.N) / p.grid_rows);
+    return t;
+  }
+  const int i = cta_batch(p);
+  const int64_t ctas = p.cta_begin[i + 1] - p.cta_begin[i];
+  const int64_t b = static_cast<int64_t>(blockIdx.x) - p.cta_begin[i];
+  const int64_t rows = p.row_begin[i + 1] - p.row_begin[i];
+  t.b = p.Bs[i];
+  t.ldb = p.ldbs[i];
+  t.first = p.row_begin[i];
+  t.lo = t.first + static_cast<int>((b * rows) / ctas);
+  t.hi = t.first + static_cast<int>(((b + 1) * rows) / ctas);
+  return t;
+}
+
+__device__ __forceinline__ const uint16_t* weight_row(const CtaRows& t, int n) {
+  return t.b + static_cast<int64_t>(n - t.first) * t.ldb;
+}
+
+// Where this CTA's outputs go: output row n, activation row m at
+// out + m * ldc + (n - first).
+struct CtaOut {
+  uint16_t* out;
+  int64_t ldc;
+  int first;
+  __device__ __forceinline__ uint16_t* at(int64_t m, int64_t n) const { return out + m * ldc + (n - first); }
+};
+
+template <bool BATCHED>
+__device__ __forceinline__ CtaOut cta_out(const CcParams& p) {
+  if constexpr (!BATCHED) {
+    return {p.C, p.ldc, 0};
+  } else {
+    const int i = cta_batch(p);
+    return {p.Cs[i], p.ldcs[i], p.row_begin[i]};
+  }
 }
 
 // The residual R[m, n] as fp32 (0 without one); R may be C itself.
@@ -106,14 +156,15 @@ struct Butterfly {
 // vectors per lane per row in flight.  GATED: the CTA's rows are outputs n, each
 // from weight row n of B (gate) and of B2 (up); a pass takes R / 2 outputs, their
 // gate and up rows sharing each paired FMA, and the result is silu(gate) * up.
-template <int MT, int R, int U, bool GATED>
+template <int MT, int R, int U, bool GATED, bool BATCHED>
 __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParams p) {
   extern __shared__ float red[];  // [rows of this CTA (x 2 gated)][MT][kCcWarps]
   constexpr int kRowStep = GATED ? R / 2 : R;  // output rows per pass
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int row_lo = static_cast<int>((static_cast<int64_t>(blockIdx.x) * p.N) / p.grid_rows);
-  const int row_hi = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * p.N) / p.grid_rows);
+  const CtaRows rows_of = cta_rows<BATCHED>(p);
+  const int row_lo = rows_of.lo;
+  const int row_hi = rows_of.hi;
   const int slice = blockIdx.y;
   const int kb = slice * p.k_slice;
   const int ke = min(p.K, kb + p.k_slice);
@@ -128,7 +179,7 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     const int r = lane;
     const int n = row_lo + (GATED ? r / 2 : r);
     if (n < row_hi) {
-      const uint16_t* row = GATED ? ((r & 1) ? p.B2 : p.B) + static_cast<int64_t>(n) * p.ldb : weight_row(p, n);
+      const uint16_t* row = GATED ? ((r & 1) ? p.B2 : p.B) + static_cast<int64_t>(n) * p.ldb : weight_row(rows_of, n);
       bulk_prefetch_l2(row + 8 * v_lo, static_cast<uint32_t>(v_hi - v_lo) * 16u);
     }
   }
@@ -167,7 +218,7 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
         brow[r] = ((r & 1) ? p.B2 : p.B) + static_cast<int64_t>(row_ok[r] ? r0 + r / 2 : r0) * p.ldb;
       } else {
         row_ok[r] = r0 + r < row_hi;
-        brow[r] = weight_row(p, row_ok[r] ? r0 + r : r0);
+        brow[r] = weight_row(rows_of, row_ok[r] ? r0 + r : r0);
       }
     }
     for (int v = v_lo + lane; v < v_hi; v += 32 * U) {
@@ -269,8 +320,9 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
     }
     if (p.split_k == 1) {
       const int64_t n = row_lo + r;
+      const CtaOut o = cta_out<BATCHED>(p);
       const float res = (!GATED && p.R != nullptr) ? rres[j] : 0.f;  // prefetched at the start
-      *reinterpret_cast<__nv_bfloat16*>(output_at(p, m, static_cast<int>(n))) =
+      *reinterpret_cast<__nv_bfloat16*>(o.at(m, n)) =
           __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0] + res);
     } else {
 #pragma unroll
@@ -290,6 +342,7 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
   __syncthreads();
   if (!is_last) return;
   __threadfence();
+  const CtaOut o = cta_out<BATCHED>(p);
   for (int e = threadIdx.x; e < rows * p.M; e += blockDim.x) {
     const int r = e / p.M, m = e % p.M;
     const int n = row_lo + r;
@@ -302,17 +355,26 @@ __global__ void __launch_bounds__(kCcWarps * 32, 2) cc_gemv_kernel(const CcParam
         s[gu] = (sl == 0) ? x : s[gu] + x;
       }
     }
-    *reinterpret_cast<__nv_bfloat16*>(output_at(p, m, n)) =
+    *reinterpret_cast<__nv_bfloat16*>(o.at(m, n)) =
         __float2bfloat16_rn(GATED ? silu_mul(s[0], s[kPlanes - 1]) : s[0] + residual(p, m, n));
   }
   if (threadIdx.x == 0) atomicExch(&p.counters[blockIdx.x], 0u);
 }
 
-template <int MT, int R, int U, bool GATED>
+template <int MT, int R, int U, bool GATED, bool BATCHED = false>
 cudaError_t launch_one(const CcParams& p, cudaStream_t stream) {
-  const int rows_max = (p.N + p.grid_rows - 1) / p.grid_rows;
+  int rows_max = (p.N + p.grid_rows - 1) / p.grid_rows;
+  if (p.nbatch > 0) {  // the largest row block of any matrix's run of CTAs
+    rows_max = 0;
+    for (int i = 0; i < p.nbatch; ++i) {
+      const int rows = p.row_begin[i + 1] - p.row_begin[i];
+      const int ctas = p.cta_begin[i + 1] - p.cta_begin[i];
+      if (ctas < 1) return cudaErrorInvalidValue;
+      rows_max = std::max(rows_max, (rows + ctas - 1) / ctas);
+    }
+  }
   const size_t smem = static_cast<size_t>(rows_max) * (GATED ? 2 : 1) * MT * kCcWarps * sizeof(float);
-  auto kern = cc_gemv_kernel<MT, R, U, GATED>;
+  auto kern = cc_gemv_kernel<MT, R, U, GATED, BATCHED>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -343,6 +405,13 @@ cudaError_t launch_cc_gemv(const CcParams& p, cudaStream_t stream) {
     if (p.M <= 2) return launch_one<2, 8, 2, true>(p, stream);
     if (p.M <= 4) return launch_one<4, 4, 2, true>(p, stream);
     if (p.M <= 8) return launch_one<8, 2, 2, true>(p, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (p.nbatch > 0) {
+    if (p.M <= 1) return launch_one<1, 8, 2, false, true>(p, stream);
+    if (p.M <= 2) return launch_one<2, 8, 2, false, true>(p, stream);
+    if (p.M <= 4) return launch_one<4, 4, 2, false, true>(p, stream);
+    if (p.M <= 8) return launch_one<8, 2, 2, false, true>(p, stream);
     return cudaErrorInvalidValue;
   }
   if (p.M <= 1) return launch_one<1, 8, 2, false>(p, stream);

@@ -130,9 +130,12 @@ struct CcParams {
   const uint16_t* R;     // non-null: residual added to the result (R[m * ldr + n], may be C)
   int64_t ldr;
   // Batched launch (nbatch > 0): output rows [row_begin[i], row_begin[i + 1]) of the
-  // N rows belong to matrix i (weights Bs[i], ldbs[i]; outputs Cs[i], ldcs[i]).
+  // N rows belong to matrix i (weights Bs[i], ldbs[i]; outputs Cs[i], ldcs[i]) and
+  // are split over CTAs [cta_begin[i], cta_begin[i + 1]) (at least one each;
+  // cta_begin[nbatch] = grid_rows).
   int32_t nbatch;
   int32_t row_begin[kMaxBatch + 1];
+  int32_t cta_begin[kMaxBatch + 1];
   const uint16_t* Bs[kMaxBatch];
   uint16_t* Cs[kMaxBatch];
   int64_t ldbs[kMaxBatch];
