@@ -278,9 +278,18 @@ SG_API int nvfp4_pack_scales(const void *plain, int64_t rows, int64_t K, int64_t
  * per-device workspace is allocated on a first call).  K and V must be finite:
  * keys past seq_k inside a tile are masked, but their values are multiplied by 0.
  *
+ * Kernels: the tcgen05 kernel above, or, for a decode step whose query rows per
+ * key/value head (seq_q * heads / kv_heads) are at most 4, a CUDA-core kernel
+ * that streams K and V once with plain 16-byte loads, each CTA taking one key
+ * range of one (batch, kv head) for all of that head's query rows; key ranges
+ * are merged from fp32 partials (log2-sum-exp weights), as the tcgen05 kernel's
+ * key splits are.  attention_bf16 picks the CUDA-core kernel for 1, 3 or 4 rows
+ * (measured faster there; 2 rows run faster on the tcgen05 kernel).
+ *
  * Arithmetic: scores and the softmax in fp32 (exp2 of log2-scaled scores), the
- * weights rounded to bf16 for the P V product, fp32 accumulation, one bf16
- * rounding of O (nearest even).  Results are the same on every run.
+ * weights rounded to bf16 for the tcgen05 kernel's P V product (kept in fp32 by
+ * the CUDA-core kernel), fp32 accumulation, one bf16 rounding of O (nearest
+ * even).  Results are the same on every run.
  *
  * Requirements: head_dim = 128; heads a multiple of kv_heads; ldq, ldo >= heads *
  * head_dim and ldk, ldv >= kv_heads * head_dim, all multiples of 8; pointers
@@ -294,6 +303,15 @@ SG_API int nvfp4_pack_scales(const void *plain, int64_t rows, int64_t K, int64_t
 SG_API int attention_bf16(const void *Q, const void *K, const void *V, void *O, int64_t batch, int64_t seq_q,
                           int64_t seq_k, int64_t heads, int64_t kv_heads, int64_t head_dim, int64_t ldq,
                           int64_t ldk, int64_t ldv, int64_t ldo, int causal, float scale, sg_stream_t stream);
+
+/* attention_bf16 with the kernel named: SG_PATH_AUTO (attention_bf16's choice),
+ * SG_PATH_TENSOR_CORE (the tcgen05 kernel, any shape) or SG_PATH_CUDA_CORE (the
+ * decode kernel; SG_ERR_INVALID_ARG unless seq_q * heads / kv_heads <= 4).  Any
+ * other path: SG_ERR_INVALID_ARG.  Otherwise as attention_bf16. */
+SG_API int attention_bf16_path(const void *Q, const void *K, const void *V, void *O, int64_t batch,
+                               int64_t seq_q, int64_t seq_k, int64_t heads, int64_t kv_heads, int64_t head_dim,
+                               int64_t ldq, int64_t ldk, int64_t ldv, int64_t ldo, int causal, float scale,
+                               int path, sg_stream_t stream);
 
 /*
  * gemv_bf16_noalloc -- gemv_bf16 on the CUDA-core kernel (SG_PATH_CUDA_CORE),

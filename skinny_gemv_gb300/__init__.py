@@ -116,6 +116,8 @@ def load(build_if_missing: bool = False):
     lib.gemm_nvfp4_path.restype = ctypes.c_int
     lib.attention_bf16.argtypes = [p, p, p, p] + [i64] * 10 + [ctypes.c_int, ctypes.c_float, p]
     lib.attention_bf16.restype = ctypes.c_int
+    lib.attention_bf16_path.argtypes = [p, p, p, p] + [i64] * 10 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, p]
+    lib.attention_bf16_path.restype = ctypes.c_int
     lib.sg_plan_nvfp4.restype = ctypes.c_int
     lib.sg_status_string.argtypes = [ctypes.c_int]
     lib.sg_status_string.restype = ctypes.c_char_p
@@ -351,9 +353,12 @@ def _tokens_heads(t, name: str):
     return t.data_ptr(), max(t.stride(1), H * D)
 
 
-def attention_bf16(Q, K, V, O=None, causal: bool = False, scale: float | None = None, stream=None):
+def attention_bf16(Q, K, V, O=None, causal: bool = False, scale: float | None = None, stream=None,
+                   path: int = PATH_AUTO):
     """O = softmax(scale Q K^T, causal mask) V per head for Q [B, Sq, H, 128] and
-    K, V [B, Sk, Hkv, 128] (bfloat16); returns O [B, Sq, H, 128]."""
+    K, V [B, Sk, Hkv, 128] (bfloat16); returns O [B, Sq, H, 128].  ``path``:
+    PATH_AUTO, PATH_TENSOR_CORE (the tcgen05 kernel) or PATH_CUDA_CORE (the
+    decode kernel, Sq x H / Hkv <= 4)."""
     torch = _torch()
     q_ptr, ldq = _tokens_heads(Q, "Q")
     k_ptr, ldk = _tokens_heads(K, "K")
@@ -369,9 +374,9 @@ def attention_bf16(Q, K, V, O=None, causal: bool = False, scale: float | None = 
     o_ptr, ldo = _tokens_heads(O, "O")
     scale = D ** -0.5 if scale is None else float(scale)
     with torch.cuda.device(Q.device):
-        st = load().attention_bf16(q_ptr, k_ptr, v_ptr, o_ptr, Bt, Sq, Sk, H, Hkv, D, ldq, ldk, ldv, ldo,
-                                   1 if causal else 0, scale, _stream_handle(stream))
-    _check(st, "attention_bf16")
+        st = load().attention_bf16_path(q_ptr, k_ptr, v_ptr, o_ptr, Bt, Sq, Sk, H, Hkv, D, ldq, ldk, ldv, ldo,
+                                        1 if causal else 0, scale, path, _stream_handle(stream))
+    _check(st, "attention_bf16_path")
     return O
 
 

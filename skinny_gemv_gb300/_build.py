@@ -17,7 +17,7 @@ LIB_NAME = "libskinny_gemm.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["sg_api.cu", "sg_gemm_tcgen05.cu", "sg_gemm_nvfp4.cu", "sg_attention.cu", "sg_gemv_cuda_core.cu", "sg_microbench.cu",
+SOURCES = ["sg_api.cu", "sg_gemm_tcgen05.cu", "sg_gemm_nvfp4.cu", "sg_attention.cu", "sg_attention_decode.cu", "sg_gemv_cuda_core.cu", "sg_microbench.cu",
            "sg_noalloc.cu"]
 HEADERS = ["sg_ptx.cuh", "sg_sched.cuh", "sg_internal.h"]
 

@@ -723,9 +723,66 @@ void attn_splits(int64_t B, int64_t Sq, int64_t Sk, int64_t H, int causal, int s
   *split_blocks = static_cast<int32_t>(bps);
 }
 
+// Key splits of the decode kernel: enough (batch, kv head, split) CTAs to fill the
+// resident slots (two per SM, one with more than two rows), at most 32 splits (the
+// combine kernel's lanes) of at least 128 keys, within the partials workspace.
+// Each split's keys are a multiple of 32 (one key per lane group and warp).
+void attn_decode_splits(int64_t B, int64_t Sq, int64_t Sk, int64_t H, int64_t Hkv, int64_t rows, int sms,
+                        int32_t* n_splits, int32_t* keys_per_split) {
+  const int64_t slots = (rows > 2 ? 1 : 2) * static_cast<int64_t>(sms);
+  const int64_t units = B * Hkv;
+  int64_t n = units >= slots ? 1 : slots / units;
+  n = std::min<int64_t>({n, 32, std::max<int64_t>(1, ceil_div(Sk, 128))});
+  const int64_t per_split_bytes = B * Sq * H * (kAttnHeadDim + 1) * 4 + 256;
+  while (n > 1 && n * per_split_bytes > static_cast<int64_t>(kPartialBytes)) --n;
+  const int64_t kps = ceil_div(ceil_div(Sk, n), 32) * 32;
+  *keys_per_split = static_cast<int32_t>(kps);
+  *n_splits = static_cast<int32_t>(ceil_div(Sk, kps));
+}
+
+// The decode kernel takes a launch whose query rows per kv head (Sq x H / Hkv) fit
+// its registers.
+bool attn_decode_fits(int64_t Sq, int64_t H, int64_t Hkv) { return Sq * (H / Hkv) <= kAttnDecodeMaxRows; }
+
+// attention_bf16's choice of the decode kernel, by measurement against a
+// 4096-key cache (32 query heads): one row per kv head 16.1 us against 17.1 (32
+// kv heads), four rows 13.5 against 14.5 (8 kv heads; 45.6 against 68.2 at batch
+// 8); two rows 18.1 against 17.5, so two rows stay on the tcgen05 kernel.
+bool attn_decode_auto(int64_t Sq, int64_t H, int64_t Hkv) {
+  return attn_decode_fits(Sq, H, Hkv) && Sq * (H / Hkv) != 2;
+}
+
 int run_attention(DeviceState& d, int dev, const void* Q, const void* K, const void* V, void* O, int64_t B,
                   int64_t Sq, int64_t Sk, int64_t H, int64_t Hkv, int64_t ldq, int64_t ldk, int64_t ldv,
-                  int64_t ldo, int causal, float scale, cudaStream_t stream) {
+                  int64_t ldo, int causal, float scale, int path, cudaStream_t stream) {
+  if (path == SG_PATH_CUDA_CORE) {
+    AttnParams p{};
+    p.B = static_cast<int32_t>(B);
+    p.Sq = static_cast<int32_t>(Sq);
+    p.Sk = static_cast<int32_t>(Sk);
+    p.H = static_cast<int32_t>(H);
+    p.Hkv = static_cast<int32_t>(Hkv);
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.O = static_cast<uint16_t*>(O);
+    p.ldo = ldo;
+    p.err = d.err;
+    p.timeout_ns = g_timeout_ns.load();
+    AttnDecodeArgs a{};
+    a.Q = static_cast<const uint16_t*>(Q);
+    a.K = static_cast<const uint16_t*>(K);
+    a.V = static_cast<const uint16_t*>(V);
+    a.ldq = ldq;
+    a.ldk = ldk;
+    a.ldv = ldv;
+    a.rows = static_cast<int32_t>(Sq * (H / Hkv));
+    attn_decode_splits(B, Sq, Sk, H, Hkv, a.rows, d.sm_count, &p.n_splits, &a.keys_per_split);
+    p.part_lse = d.partials;
+    p.part_o = d.partials + ceil_div(static_cast<int64_t>(p.n_splits) * B * Sq * H, 64) * 64;
+    cudaError_t e = launch_attn_decode(p, a, stream);
+    if (e == cudaSuccess && p.n_splits > 1) e = launch_attn_combine(p, stream);
+    return e == cudaSuccess ? SG_OK : cuda_fail(e);
+  }
   CUtensorMap tq, tk, tv;
   int st = make_map(&tq, Q, B * Sq, H * kAttnHeadDim, ldq, kAttnTile, 64, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tk, K, B * Sk, Hkv * kAttnHeadDim, ldk, kAttnTile, 64, CU_TENSOR_MAP_SWIZZLE_128B, dev);
@@ -968,10 +1025,19 @@ const char* sg_status_string(int status) {
 int attention_bf16(const void* Q, const void* K, const void* V, void* O, int64_t batch, int64_t seq_q,
                    int64_t seq_k, int64_t heads, int64_t kv_heads, int64_t head_dim, int64_t ldq, int64_t ldk,
                    int64_t ldv, int64_t ldo, int causal, float scale, sg_stream_t stream) {
+  return attention_bf16_path(Q, K, V, O, batch, seq_q, seq_k, heads, kv_heads, head_dim, ldq, ldk, ldv, ldo, causal,
+                             scale, SG_PATH_AUTO, stream);
+}
+
+int attention_bf16_path(const void* Q, const void* K, const void* V, void* O, int64_t batch, int64_t seq_q,
+                        int64_t seq_k, int64_t heads, int64_t kv_heads, int64_t head_dim, int64_t ldq, int64_t ldk,
+                        int64_t ldv, int64_t ldo, int causal, float scale, int path, sg_stream_t stream) {
+  if (path != SG_PATH_AUTO && path != SG_PATH_TENSOR_CORE && path != SG_PATH_CUDA_CORE) return SG_ERR_INVALID_ARG;
   if (batch < 0 || seq_q < 0 || seq_k < 0 || heads < 0 || kv_heads < 0) return SG_ERR_INVALID_ARG;
   if (head_dim != kAttnHeadDim || !std::isfinite(scale)) return SG_ERR_INVALID_ARG;
   if (batch == 0 || seq_q == 0 || heads == 0) return SG_OK;
   if (kv_heads == 0 || heads % kv_heads != 0) return SG_ERR_INVALID_ARG;
+  if (path == SG_PATH_CUDA_CORE && !attn_decode_fits(seq_q, heads, kv_heads)) return SG_ERR_INVALID_ARG;
   // every row index and grid size in int32
   const int64_t tiles = ceil_div(seq_q, kAttnTile) * heads * batch;
   if (batch * seq_q > INT32_MAX || batch * seq_k > INT32_MAX || heads * head_dim > INT32_MAX || tiles > INT32_MAX)
@@ -995,8 +1061,9 @@ int attention_bf16(const void* Q, const void* K, const void* V, void* O, int64_t
   }
   st = ensure_workspace(*d, s);
   if (st != SG_OK) return st;
+  if (path == SG_PATH_AUTO) path = attn_decode_auto(seq_q, heads, kv_heads) ? SG_PATH_CUDA_CORE : SG_PATH_TENSOR_CORE;
   return run_attention(*d, dev, Q, K, V, O, batch, seq_q, seq_k, heads, kv_heads, ldq, ldk, ldv, ldo, causal,
-                       scale, s);
+                       scale, path, s);
 }
 
 int sg_last_cuda_error(void) { return g_last_cuda_error; }

@@ -481,15 +481,29 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   float tot = w;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+  // Eight splits' loads are issued together, then summed in split order (one
+  // load per iteration would put n_splits memory latencies in a row).  A split
+  // of zero weight (no visible key, or past n_splits: lanes there hold w = 0) is
+  // not read: its part may be stale.
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int sp = 0; sp < p.n_splits; ++sp) {
-    const float ws = __shfl_sync(0xFFFFFFFFu, w, sp);
-    if (ws == 0.f) continue;
-    const float4 v = *reinterpret_cast<const float4*>(p.part_o + (sp * split_stride + unit) * kAttnHeadDim + 4 * lane);
-    acc.x += ws * v.x;
-    acc.y += ws * v.y;
-    acc.z += ws * v.z;
-    acc.w += ws * v.w;
+  for (int sp0 = 0; sp0 < p.n_splits; sp0 += 8) {
+    float ws[8];
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int sp = sp0 + u;  // < 32: n_splits <= 32
+      ws[u] = __shfl_sync(0xFFFFFFFFu, w, sp);
+      v[u] = (sp < p.n_splits && ws[u] != 0.f)
+                 ? *reinterpret_cast<const float4*>(p.part_o + (sp * split_stride + unit) * kAttnHeadDim + 4 * lane)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      acc.x += ws[u] * v[u].x;
+      acc.y += ws[u] * v[u].y;
+      acc.z += ws[u] * v[u].z;
+      acc.w += ws[u] * v[u].w;
+    }
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
   uint2 out;

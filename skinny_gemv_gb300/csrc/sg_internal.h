@@ -216,6 +216,22 @@ struct AttnParams {
   uint32_t inject_extra_tx;  // failure injection: extra bytes expected on the first K tile
 };
 
+// Decode attention on CUDA cores (sg_attention_decode.cu): CTA (b, kv head g,
+// split s) takes the rows = Sq x H / Hkv query rows of heads g H / Hkv .. and keys
+// [s keys_per_split, (s + 1) keys_per_split); Q, K and V are read directly (row
+// pitches ldq, ldk, ldv elements, 16-byte aligned).  With n_splits > 1 it writes
+// the same partials as the tensor-core kernel for launch_attn_combine.
+constexpr int kAttnDecodeMaxRows = 4;
+struct AttnDecodeArgs {
+  const uint16_t* Q;
+  const uint16_t* K;
+  const uint16_t* V;
+  int64_t ldq, ldk, ldv;
+  int32_t rows;
+  int32_t keys_per_split;
+};
+cudaError_t launch_attn_decode(const AttnParams& p, const AttnDecodeArgs& a, cudaStream_t stream);
+
 // Merges the n_splits partial results of a split launch into O (bf16).
 cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream);
 

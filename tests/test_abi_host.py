@@ -365,6 +365,18 @@ def test_attention_argument_errors_before_any_cuda_call(lib, args, code):
     assert lib.attention_bf16(*args[:14], args[14], args[15], None) == code
 
 
+def test_attention_path_errors_before_any_cuda_call(lib):
+    # (Q, K, V, O, batch, seq_q, seq_k, heads, kv_heads, head_dim, ldq, ldk, ldv, ldo, causal, scale, path)
+    ok = (16, 16, 16, 16, 1, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1)
+    for bad_path in (sg.PATH_GEMM, sg.PATH_GEMM_PAIR, 7, -1):
+        assert lib.attention_bf16_path(*ok, bad_path, None) == sg.SG_ERR_INVALID_ARG
+    # the decode kernel holds at most four query rows per kv head: 8 queries x 1 head
+    assert lib.attention_bf16_path(*ok, sg.PATH_CUDA_CORE, None) == sg.SG_ERR_INVALID_ARG
+    # 1 query x 8 heads per kv head (grouped): 8 rows
+    grouped = (16, 16, 16, 16, 1, 1, 8, 8, 1, 128, 1024, 128, 128, 1024, 1, 0.1)
+    assert lib.attention_bf16_path(*grouped, sg.PATH_CUDA_CORE, None) == sg.SG_ERR_INVALID_ARG
+
+
 def test_attention_empty_is_noop(lib):
     # no batch, no queries or no heads: nothing to do, nothing dereferenced
     assert lib.attention_bf16(None, None, None, None, 0, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1, None) == sg.SG_OK

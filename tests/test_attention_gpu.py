@@ -45,8 +45,8 @@ def bf16(x: np.ndarray) -> np.ndarray:
     return syn.f64_to_bf16_bits(np.asarray(x, dtype=np.float64))
 
 
-def run(Qb, Kb, Vb, causal, scale=None, O=None):
-    O = sg.attention_bf16(to_dev(Qb), to_dev(Kb), to_dev(Vb), O=O, causal=causal, scale=scale)
+def run(Qb, Kb, Vb, causal, scale=None, O=None, path=sg.PATH_AUTO):
+    O = sg.attention_bf16(to_dev(Qb), to_dev(Kb), to_dev(Vb), O=O, causal=causal, scale=scale, path=path)
     torch.cuda.synchronize()
     st, detail = sg.check_device_errors()
     assert st == 0, detail
@@ -71,14 +71,20 @@ def seeded(B, S, H, seed):
 
 
 @pytest.mark.parametrize("Sq,Sk,causal", [(128, 128, True), (300, 300, True), (200, 333, False), (5, 260, True),
-                                          (130, 70, True), (1, 1, True)])
+                                          (130, 70, True), (1, 1, True), (2, 700, True), (1, 4096, False)])
 def test_zero_queries_average_values(Sq, Sk, causal):
     rng = np.random.default_rng(Sq * 1000 + Sk)
     B, H = 2, 2
     Qb = np.zeros((B, Sq, H, D), dtype=np.uint16)
     Kb = bf16(rng.standard_normal((B, Sk, H, D)))
     Vb = bf16(rng.integers(-8, 9, size=(B, Sk, H, D)).astype(np.float64))
-    got = run(Qb, Kb, Vb, causal)
+    # H = Hkv: one query row per kv head and query, so the decode kernel takes Sq <= 4
+    paths = [sg.PATH_TENSOR_CORE] + ([sg.PATH_CUDA_CORE] if Sq <= 4 else [])
+    for path in paths:
+        _zero_queries_check(run(Qb, Kb, Vb, causal, path=path), Qb, Kb, Vb, causal)
+
+
+def _zero_queries_check(got, Qb, Kb, Vb, causal):
     ref = oracle.attention(Qb, Kb, Vb, causal=causal)
     # every weight is exactly 1: O is the mean of small integers, rounded to bf16 (one
     # bf16 step); a key split merges per-split means with fp32 weights from
@@ -117,6 +123,48 @@ def test_grouped_heads_read_their_kv_head():
     got = run(Qb, Kb, Vb, causal=False)
     for h in range(H):
         assert np.all(got[:, :, h] == 10.0 * (h // (H // Hkv)) + 1.0), h
+
+
+def test_grouped_heads_decode_kernel():
+    # one query per head, four query heads per kv head: the decode kernel's rows
+    rng = np.random.default_rng(18)
+    B, Sq, Sk, H, Hkv = 2, 1, 130, 8, 2
+    Qb = bf16(rng.standard_normal((B, Sq, H, D)))
+    Kb = bf16(rng.standard_normal((B, Sk, Hkv, D)))
+    Vb = bf16(np.broadcast_to(np.arange(Hkv, dtype=np.float64)[None, None, :, None] * 10 + 1.0, (B, Sk, Hkv, D)))
+    got = run(Qb, Kb, Vb, causal=True, path=sg.PATH_CUDA_CORE)
+    for h in range(H):
+        assert np.all(got[:, :, h] == 10.0 * (h // (H // Hkv)) + 1.0), h
+
+
+DECODE_CASES = [
+    (1, 1, 4096, 32, 32, True),   # the decode workload's shape
+    (2, 1, 777, 8, 2, True),      # grouped heads: four query rows per kv head
+    (3, 2, 300, 4, 4, True),      # two queries: the first sees one key fewer
+    (1, 4, 129, 2, 2, True),      # four causal queries
+    (2, 3, 50, 1, 1, False),      # three rows, few keys
+    (1, 1, 31, 4, 2, True),       # fewer keys than one step of the kernel
+    (1, 3, 2, 2, 2, True),        # more queries than keys: the first row sees nothing
+]
+
+
+@pytest.mark.parametrize("B,Sq,Sk,H,Hkv,causal", DECODE_CASES)
+def test_decode_kernel_parity(B, Sq, Sk, H, Hkv, causal):
+    # both kernels on the decode shapes (AUTO takes the CUDA-core one)
+    seed = 9500 + B * 131 + Sq * 7 + Sk
+    Qb, Kb, Vb = seeded(B, Sq, H, seed), seeded(B, Sk, Hkv, seed + 1), seeded(B, Sk, Hkv, seed + 2)
+    for path in (sg.PATH_CUDA_CORE, sg.PATH_TENSOR_CORE, sg.PATH_AUTO):
+        got = run(Qb, Kb, Vb, causal, path=path)
+        assert_close(got, Qb, Kb, Vb, causal, label=f"path {path} {(B, Sq, Sk, H, Hkv, causal)}")
+        if causal and Sq > Sk:
+            assert np.all(got[:, : Sq - Sk] == 0.0)
+
+
+def test_decode_kernel_rejects_many_rows():
+    Q = torch.zeros((1, 5, 2, D), dtype=torch.bfloat16, device="cuda")
+    K = torch.zeros((1, 9, 2, D), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(RuntimeError):
+        sg.attention_bf16(Q, K, K, causal=True, path=sg.PATH_CUDA_CORE)
 
 
 @pytest.mark.parametrize("B,Sq,Sk,H,Hkv,causal", [

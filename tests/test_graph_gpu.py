@@ -54,15 +54,18 @@ def _capture(call):
     return g
 
 
-@pytest.mark.parametrize("B,Sq,Sk,H,causal", [(1, 300, 300, 4, True), (1, 1, 2000, 8, True)])
-def test_attention_capture_and_replay(B, Sq, Sk, H, causal):
-    """Prefill and the key-split decode path (attention kernel plus combine kernel)."""
+@pytest.mark.parametrize("B,Sq,Sk,H,causal,path", [(1, 300, 300, 4, True, sg.PATH_AUTO),
+                                                   (1, 1, 2000, 8, True, sg.PATH_AUTO),
+                                                   (1, 1, 2000, 8, True, sg.PATH_TENSOR_CORE)])
+def test_attention_capture_and_replay(B, Sq, Sk, H, causal, path):
+    """Prefill, and the key-split decode step on the CUDA-core decode kernel (AUTO)
+    and on the tcgen05 kernel, each with the combine kernel."""
     Qb = syn.matrix(B * Sq, H * 128, "normal", 61).reshape(B, Sq, H, 128)
     Kb = syn.matrix(B * Sk, H * 128, "normal", 62).reshape(B, Sk, H, 128)
     Vb = syn.matrix(B * Sk, H * 128, "normal", 63).reshape(B, Sk, H, 128)
     dev = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in (Qb, Kb, Vb)]
     O = torch.empty((B, Sq, H, 128), dtype=torch.bfloat16, device="cuda")
-    g = _capture(lambda: sg.attention_bf16(*dev, O=O, causal=causal))
+    g = _capture(lambda: sg.attention_bf16(*dev, O=O, causal=causal, path=path))
     ref = oracle.attention(Qb, Kb, Vb, causal=causal)
     W = oracle.attention(Qb, Kb, np.abs(oracle._bf16_tensor(Vb)), causal=causal)
     for _ in range(2):
