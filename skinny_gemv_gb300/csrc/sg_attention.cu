@@ -468,6 +468,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int64_t rows = static_cast<int64_t>(p.B) * p.Sq * p.H;
+  // The next launch may start its set-up (and its early L2 reads) at once: it
+  // waits for this grid's completion before it touches memory.
+  grid_launch_dependents();
   grid_dependency_wait();
   if (unit >= rows) return;
   const int64_t row = unit / p.H;  // b * Sq + i

@@ -80,6 +80,20 @@ __global__ void __launch_bounds__(kDecThreads, RT >= 4 ? 1 : 2) attn_decode_kern
   const int ka = split * a.keys_per_split;
   const int kb = min(p.Sk, ka + a.keys_per_split);
 
+  // The first round's K and V rows (256 bytes each), pulled into L2 while the
+  // previous launch may still be finishing: a hint only (L2 is the point of
+  // coherence, so the loads after the wait see that launch's writes).
+  if (dg == 0) {
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int j = ka + kKeysPerStep * c + 4 * warp + kg;
+      if (j < kb) {
+        const int64_t kvr = static_cast<int64_t>(b) * p.Sk + j;
+        bulk_prefetch_l2(a.K + kvr * a.ldk + g * kAttnHeadDim, kAttnHeadDim * 2);
+        bulk_prefetch_l2(a.V + kvr * a.ldv + g * kAttnHeadDim, kAttnHeadDim * 2);
+      }
+    }
+  }
   grid_dependency_wait();  // Q, K and V may come from the previous kernel
 
   // this lane's 16 dims of each query row (bf16 pairs), and each row's last visible key
