@@ -348,9 +348,21 @@ def _tokens_heads(t, name: str):
         raise ValueError(f"{name} must be a 4-D [batch, seq, heads, head_dim] bfloat16 CUDA tensor, "
                          f"got {t.dtype} {tuple(t.shape)} {t.device}")
     Bt, S, H, D = t.shape
-    if (D > 1 and t.stride(3) != 1) or (H > 1 and t.stride(2) != D) or (Bt > 1 and S > 0 and t.stride(0) != S * t.stride(1)):
-        raise ValueError(f"{name} must have dense heads x head_dim rows and batches of whole rows")
-    return t.data_ptr(), max(t.stride(1), H * D)
+    if (D > 1 and t.stride(3) != 1) or (H > 1 and t.stride(2) != D):
+        raise ValueError(f"{name} must have dense heads x head_dim rows")
+    # token row b * S + i at pitch ld; with one token per sequence the rows are
+    # the batches (a size-1 dimension's stride says nothing about memory)
+    if S > 1:
+        ld = t.stride(1)
+        if Bt > 1 and t.stride(0) != S * ld:
+            raise ValueError(f"{name} must have batches of whole rows")
+    elif Bt > 1:
+        ld = t.stride(0)
+    else:
+        ld = H * D
+    if ld < H * D:  # overlapping or broadcast rows: not a token-major layout
+        raise ValueError(f"{name} token rows overlap (pitch {ld} < {H * D} elements)")
+    return t.data_ptr(), ld
 
 
 def attention_bf16(Q, K, V, O=None, causal: bool = False, scale: float | None = None, stream=None,

@@ -382,3 +382,35 @@ def test_attention_empty_is_noop(lib):
     assert lib.attention_bf16(None, None, None, None, 0, 8, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1, None) == sg.SG_OK
     assert lib.attention_bf16(None, None, None, None, 1, 0, 8, 2, 2, 128, 256, 256, 256, 256, 1, 0.1, None) == sg.SG_OK
     assert lib.attention_bf16(None, None, None, None, 1, 8, 8, 0, 0, 128, 256, 256, 256, 256, 1, 0.1, None) == sg.SG_OK
+
+
+class _Rows:
+    """A stand-in for a [B, S, heads, 128] bf16 CUDA tensor: the binding's token
+    pitch logic reads only its shape and strides."""
+
+    def __init__(self, shape, strides):
+        import torch
+        self.shape, self._strides, self.dtype, self.is_cuda = shape, strides, torch.bfloat16, True
+
+    def dim(self):
+        return 4
+
+    def stride(self, i):
+        return self._strides[i]
+
+    def data_ptr(self):
+        return 0
+
+
+def test_attention_token_pitch():
+    H, D = 6, 128
+    # one token per sequence: the rows are the batches, whatever the size-1 stride says
+    assert sg._tokens_heads(_Rows((2, 1, H, D), (776, 768, 128, 1)), "Q") == (0, 776)
+    assert sg._tokens_heads(_Rows((2, 5, H, D), (5 * 776, 776, 128, 1)), "Q") == (0, 776)
+    assert sg._tokens_heads(_Rows((1, 1, H, D), (768, 768, 128, 1)), "Q") == (0, 768)
+    with pytest.raises(ValueError):  # broadcast rows
+        sg._tokens_heads(_Rows((1, 5, H, D), (0, 0, 128, 1)), "K")
+    with pytest.raises(ValueError):  # batches that are not whole runs of rows
+        sg._tokens_heads(_Rows((2, 5, H, D), (776, 776, 128, 1)), "K")
+    with pytest.raises(ValueError):  # heads not dense
+        sg._tokens_heads(_Rows((1, 5, H, D), (5 * 1024, 1024, 136, 1)), "V")

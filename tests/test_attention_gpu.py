@@ -246,3 +246,30 @@ def test_negative_zero_and_large_scales(scale):
     Qb, Kb, Vb = seeded(1, 200, 2, 500), seeded(1, 260, 2, 501), seeded(1, 260, 2, 502)
     got = run(Qb, Kb, Vb, True, scale=scale)
     assert_close(got, Qb, Kb, Vb, True, scale=scale, label=f"scale {scale}")
+
+
+def test_decode_kernel_pitches_scales_and_reruns():
+    # the decode kernel (three query rows per kv head) on NaN-padded token rows:
+    # padding must be neither read nor written; any finite scale; identical reruns
+    rng = np.random.default_rng(11)
+    B, Sq, Sk, H, Hkv = 2, 1, 190, 6, 2
+    Qb = bf16(rng.standard_normal((B, Sq, H, D)))
+    Kb, Vb = (bf16(rng.standard_normal((B, Sk, Hkv, D))) for _ in range(2))
+
+    def padded(x, heads, extra):
+        buf = torch.full((x.shape[0], x.shape[1], heads * D + extra), float("nan"), dtype=torch.bfloat16,
+                         device="cuda")
+        buf[:, :, :heads * D] = to_dev(x).reshape(x.shape[0], x.shape[1], heads * D)
+        return buf[:, :, :heads * D].unflatten(2, (heads, D))
+    Qd, Kd, Vd = padded(Qb, H, 8), padded(Kb, Hkv, 64), padded(Vb, Hkv, 16)
+    for scale in (0.05, -0.08, 0.0, 0.3):
+        Obuf = torch.full((B, Sq, H * D + 24), float("nan"), dtype=torch.bfloat16, device="cuda")
+        Od = Obuf[:, :, :H * D].unflatten(2, (H, D))
+        sg.attention_bf16(Qd, Kd, Vd, O=Od, causal=True, scale=scale, path=sg.PATH_CUDA_CORE)
+        torch.cuda.synchronize()
+        got = oracle._bf16_tensor(from_dev(Od.contiguous()))
+        assert_close(got, Qb, Kb, Vb, True, scale=scale, label=f"decode kernel, pitched, scale {scale}")
+        assert torch.isnan(Obuf[:, :, H * D:]).all(), "padding columns of O were written"
+        again = sg.attention_bf16(Qd, Kd, Vd, causal=True, scale=scale, path=sg.PATH_CUDA_CORE)
+        torch.cuda.synchronize()
+        assert torch.equal(again.view(torch.int16), Od.contiguous().view(torch.int16)), "rerun differs"
