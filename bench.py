@@ -21,10 +21,19 @@ before.  The JSON line (printed by rank 0) carries:
                        consecutive steps overlap (uploads of A and B, GEMM and
                        download on four streams, two sets of device buffers)
   cpu_baseline         the fp64 oracle on a bounded row sample, on the host cores
-  rows                 the other workloads (2048^3, the 7B MLP projections,
-                       8192^3, the decode shapes M = 1, 2, 16, 64) and the
-                       measured tcgen05 peak / copy / read roofs
+  rows                 every bf16 config (512^3 ... 16384^3, the 7B MLP
+                       projections, the decode shapes M = 1, 2, 16, 64 on every
+                       skinny entry) and the fused, batched, NVFP4 and attention
+                       workloads: per-launch graph-replay median over 8 rounds
+                       in rotated arm order (cuBLAS through torch.matmul is an
+                       arm, for context), single-launch median of 100, wave
+                       efficiency of the plan
+  microbench           the measured tcgen05 peak / copy / read roofs
+  oracle_rows          the fp64 oracle's seconds per config (full up to the MLP
+                       shapes; sampled 128 x 128 and extrapolated beyond)
   clocks               nvidia-smi SM clock samples taken during the timed region
+  summary              (last, compact) per config: graph and single-launch us,
+                       throughput, fraction of the measured roof; oracle seconds
 
 --impl reference times the oracle itself (the reference arm): each step is the
 fp64 oracle on a 64-row sample of the same 4096^3 workload, on the host cores.
@@ -385,16 +394,20 @@ def run_ours(args, world, rank, local):
     rows = []
     micro = {}
     cpu = None
+    oracle_rows = []
     if rank == 0 and not args.quick:
         rows = measure_rows(torch, sg, syn, stream, l2, peaks, args)
         micro = measure_micro(torch, sg, stream)
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(syn, w)
+        if not args.quick:
+            oracle_rows = oracle_table(syn)
 
     if rank != 0:
         return 0
     plan = sg.plan(M, N, K, info["sm_count"], 0)
     peak, peak_key = tensor_peak(peaks, total_ms)
+    clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -424,12 +437,22 @@ def run_ours(args, world, rank, local):
         },
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "clocks": sampler.summary(),
+        "clocks": clocks,
         "gpu_launches": args.steps,
         "correctness": check,
         "rows": rows,
         "microbench": micro,
+        "oracle_rows": oracle_rows,
     }
+    if micro:
+        # against the card's own tcgen05 loop (the metric's "measured tcgen05 peak"),
+        # with the clock each was measured at
+        line["roofline"]["frac_of_tcgen05_loop"] = achieved / micro["tcgen05_peak_tflops"]
+        line["roofline"]["tcgen05_loop"] = {"tflops": micro["tcgen05_peak_tflops"],
+                                            "sm_mhz": micro["tcgen05_peak_sm_mhz"],
+                                            "timed_region_sm_mhz": clocks.get("sm_mhz")}
+    if rows:
+        line["summary"] = summary(rows, oracle_rows)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -524,16 +547,77 @@ def measure_e2e(torch, sg, w, A0, B0, stream, args, dist, world):
 
 ENTRIES = {"auto": None, "cuda_core": 1, "tensor_core": 2}
 
+# Rows' timing protocol (gemm3 benchmarks page, "Methodology"; spark-kernels, "how
+# things are measured"): every arm of a workload (our entries, and cuBLAS through
+# torch.matmul for context) is captured as one CUDA graph of ROUND_LAUNCHES
+# launches over the rotating inputs; ROUNDS rounds replay the arms in rotated
+# order and each arm's per-launch time is the median over the rounds.  Beside it,
+# SINGLE_LAUNCHES launches are timed one by one (events around each) and their
+# median is the single-launch time, which includes the launch gap.
+ROUNDS = 8
+ROUND_LAUNCHES = 20
+SINGLE_LAUNCHES = 100
+
+
+def time_arms(torch, stream, arms, warmup: int = 5, rounds: int = ROUNDS, per_round: int = ROUND_LAUNCHES,
+              singles: int = SINGLE_LAUNCHES):
+    """arms: list of (label, fns), each fns a list of zero-argument launches on
+    `stream` (called in rotation).  Returns {label: {"graph_us", "single_us",
+    "graph_ms_total"}}: the median per-launch time of graph replay over `rounds`
+    rounds in rotated arm order, and the median of `singles` one-launch event
+    timings."""
+    graphs = {}
+    for label, fns in arms:
+        for i in range(warmup):
+            fns[i % len(fns)]()
+        stream.synchronize()
+        graphs[label] = build_graphs(torch, stream, fns, per_round, offset=warmup)
+        replay_ms(torch, stream, graphs[label])  # uploads the graph
+    per = {label: [] for label, _ in arms}
+    labels = [label for label, _ in arms]
+    for r in range(rounds):
+        k = r % len(labels)
+        for label in labels[k:] + labels[:k]:
+            per[label].append(replay_ms(torch, stream, graphs[label]) / per_round)
+    out = {}
+    for label, fns in arms:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(singles)]
+        with torch.cuda.stream(stream):
+            for i, (e0, e1) in enumerate(ev):
+                e0.record(stream)
+                fns[i % len(fns)]()
+                e1.record(stream)
+        stream.synchronize()
+        single = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        out[label] = {"graph_us": statistics.median(per[label]) * 1e3, "single_us": single * 1e3,
+                      "graph_ms_total": sum(per[label]) * per_round}
+    del graphs
+    return out
+
+
+def _tensor_row(row, flops, t, peaks):
+    row["tflops"] = flops / (row["us"] / 1e6) / 1e12
+    rpeak, rkey = tensor_peak(peaks, t["graph_ms_total"])
+    row["frac_of_peak"] = row["tflops"] / rpeak
+    row["peak"] = rkey
+
+
+def _hbm_row(row, byts, peaks):
+    row["gbs"] = byts / (row["us"] / 1e6) / 1e9
+    row["frac_of_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+
 
 def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=None):
-    """Other workloads of the pages, timed the same way (inputs rotated past L2).
-    Inputs are drawn on the device from seeded generators with the workloads'
-    distributions; the parity tests check these shapes on the host generator's inputs.
-    `names` limits the workloads and `entries` the skinny entries (auto, cuda_core,
-    tensor_core) that are timed."""
+    """Other workloads of the pages, timed with the rows' protocol (inputs rotated
+    past L2).  Inputs are drawn on the device from seeded generators with the
+    workloads' distributions; the parity tests check these shapes on the host
+    generator's inputs.  `names` limits the workloads and `entries` the skinny
+    entries (auto, cuda_core, tensor_core) that are timed."""
     out = []
     gen = torch.Generator(device=stream.device)
-    steps = 20 if args.quick else 100
+    rounds = 3 if args.quick else ROUNDS
+    singles = 20 if args.quick else SINGLE_LAUNCHES
+    sms = sg.device_query()["sm_count"]
 
     def draw(rows, cols, dist, seed):
         gen.manual_seed(seed)
@@ -544,10 +628,14 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
             t = torch.randn((rows, cols), generator=gen, device=stream.device, dtype=torch.float32) * sigma
         return t.to(torch.bfloat16)
 
+    def timed(arms):
+        return time_arms(torch, stream, arms, rounds=rounds, singles=singles)
+
     if names is None:
         # decode rows first: right after seconds of power-capped GEMMs the
         # memory-bound rows measured up to 2 us slower per launch
-        names = [n for n in syn.WORKLOADS if n.startswith("dec")] + ["sq2048", "mlp_up", "mlp_down", "sq8192"]
+        names = [n for n in syn.WORKLOADS if n.startswith("dec")]
+        names += ["sq512", "sq2048", "sq4096", "mlp_up", "mlp_down", "sq8192", "sq16384"]
         names += list(syn.GATED_WORKLOADS) + list(syn.RESIDUAL_WORKLOADS) + list(syn.BATCHED_WORKLOADS)
         names += ["fp4_sq4096", "fp4_sq8192", "fp4_sq16384"]
         names += ["attn_causal_4096", "attn_4096", "attn_decode_4096"]
@@ -567,6 +655,7 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
             As = copies(A, nrot) if w.M > 64 else [A] * nrot
             Bs = copies(B, nrot)
             C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=stream.device)
+            Cb = torch.empty_like(C)
         stream.synchronize()
         paths = [("gemm_bf16", None)]
         if w.M <= 64:
@@ -575,26 +664,34 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         if entries is not None:
             keep = {ENTRIES[e] for e in entries}
             paths = [(label, path) for label, path in paths if path in keep]
+        arms = []
         for label, path in paths:
             if path is None:
                 fns = [(lambda a=a, b=b: sg.gemm_bf16(a, b, C, stream=stream)) for a, b in zip(As, Bs)]
             else:
                 fns = [(lambda a=a, b=b, p=path: sg.gemv_bf16(a, b, C, stream=stream, path=p))
                        for a, b in zip(As, Bs)]
-            total = time_launches(torch, stream, fns, steps, 5)
-            med = total / steps  # ms per launch, graph replay back to back
-            row = {"workload": name, "entry": label, "M": w.M, "N": w.N, "K": w.K, "us": med * 1e3}
+            arms.append((label, fns))
+        if entries is None:  # cuBLAS (torch.matmul) on the same inputs, for context only
+            def mm(a, b):
+                with torch.cuda.stream(stream):
+                    torch.matmul(a, b.t(), out=Cb)
+            arms.append(("cublas", [(lambda a=a, b=b: mm(a, b)) for a, b in zip(As, Bs)]))
+        t = timed(arms)
+        plan = sg.plan(w.M, w.N, w.K, sms, 0)
+        for label, path in paths:
+            row = {"workload": name, "entry": label, "M": w.M, "N": w.N, "K": w.K, "us": t[label]["graph_us"],
+                   "single_us": t[label]["single_us"]}
+            if label == "gemm_bf16":
+                row["wave_efficiency"] = plan["wave_efficiency"]
+                if "cublas" in t:
+                    row["cublas_us"] = t["cublas"]["graph_us"]
             if w.M > 64:
-                row["tflops"] = tflops(w.M, w.N, w.K, med / 1e3)
-                rpeak, rkey = tensor_peak(peaks, total)
-                row["frac_of_peak"] = row["tflops"] / rpeak
-                row["peak"] = rkey
+                _tensor_row(row, w.flops, t[label], peaks)
             else:
-                gbs = decode_bytes(w.M, w.N, w.K) / (med / 1e3) / 1e9
-                row["gbs"] = gbs
-                row["frac_of_hbm"] = gbs / peaks["hbm_gbs"]
+                _hbm_row(row, w.decode_bytes, peaks)
             out.append(row)
-        del As, Bs, A, B, C
+        del As, Bs, A, B, C, Cb
         torch.cuda.empty_cache()
     for name in gated_names:
         g = syn.GATED_WORKLOADS[name]
@@ -610,17 +707,13 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         stream.synchronize()
         fns = [(lambda a=a, wg=wg, wu=wu: sg.gemm_bf16_swiglu(a, wg, wu, C, stream=stream))
                for a, wg, wu in zip(As, Gs, Us)]
-        total = time_launches(torch, stream, fns, steps, 5)
-        med = total / steps
-        row = {"workload": name, "entry": "gemm_bf16_swiglu", "M": w.M, "N": w.N, "K": w.K, "us": med * 1e3}
+        t = timed([("gemm_bf16_swiglu", fns)])["gemm_bf16_swiglu"]
+        row = {"workload": name, "entry": "gemm_bf16_swiglu", "M": w.M, "N": w.N, "K": w.K, "us": t["graph_us"],
+               "single_us": t["single_us"]}
         if w.M > 64:
-            row["tflops"] = g.flops / (med / 1e3) / 1e12
-            rpeak, rkey = tensor_peak(peaks, total)
-            row["frac_of_peak"] = row["tflops"] / rpeak
-            row["peak"] = rkey
+            _tensor_row(row, g.flops, t, peaks)
         else:
-            row["gbs"] = g.decode_bytes / (med / 1e3) / 1e9
-            row["frac_of_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+            _hbm_row(row, g.decode_bytes, peaks)
         out.append(row)
         del As, Gs, Us, A, Wg, Wu, C
         torch.cuda.empty_cache()
@@ -637,17 +730,13 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
             C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=stream.device)
         stream.synchronize()
         fns = [(lambda a=a, b=b, r=r: sg.gemm_bf16_residual(a, b, r, C, stream=stream)) for a, b, r in zip(As, Bs, Rs)]
-        total = time_launches(torch, stream, fns, steps, 5)
-        med = total / steps
-        row = {"workload": name, "entry": "gemm_bf16_residual", "M": w.M, "N": w.N, "K": w.K, "us": med * 1e3}
+        t = timed([("gemm_bf16_residual", fns)])["gemm_bf16_residual"]
+        row = {"workload": name, "entry": "gemm_bf16_residual", "M": w.M, "N": w.N, "K": w.K, "us": t["graph_us"],
+               "single_us": t["single_us"]}
         if w.M > 64:
-            row["tflops"] = rw.flops / (med / 1e3) / 1e12
-            rpeak, rkey = tensor_peak(peaks, total)
-            row["frac_of_peak"] = row["tflops"] / rpeak
-            row["peak"] = rkey
+            _tensor_row(row, rw.flops, t, peaks)
         else:
-            row["gbs"] = rw.decode_bytes / (med / 1e3) / 1e9
-            row["frac_of_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+            _hbm_row(row, rw.decode_bytes, peaks)
         out.append(row)
         del As, Bs, Rs, A, B, R, C
         torch.cuda.empty_cache()
@@ -661,11 +750,11 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
             Cs = [torch.empty((bw.M, n), dtype=torch.bfloat16, device=stream.device) for n in bw.Ns]
         stream.synchronize()
         fns = [(lambda ws=ws: sg.gemv_bf16_batched(A, ws, Cs, stream=stream)) for ws in sets]
-        total = time_launches(torch, stream, fns, steps, 5)
-        med = total / steps
-        gbs = bw.decode_bytes / (med / 1e3) / 1e9
-        out.append({"workload": name, "entry": "gemv_bf16_batched", "M": bw.M, "N": list(bw.Ns), "K": bw.K,
-                    "us": med * 1e3, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]})
+        t = timed([("gemv_bf16_batched", fns)])["gemv_bf16_batched"]
+        row = {"workload": name, "entry": "gemv_bf16_batched", "M": bw.M, "N": list(bw.Ns), "K": bw.K,
+               "us": t["graph_us"], "single_us": t["single_us"]}
+        _hbm_row(row, bw.decode_bytes, peaks)
+        out.append(row)
         del sets, Ws, A, Cs
         torch.cuda.empty_cache()
     for name in fp4_names:
@@ -689,11 +778,10 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         stream.synchronize()
         fns = [(lambda a=a, sa=sa, b=b, sb=sb: sg.gemm_nvfp4(a, sa, b, sb, K=fw.K, C=C, alpha=fw.alpha, stream=stream))
                for a, sa, b, sb in sets]
-        total = time_launches(torch, stream, fns, steps, 5)
-        med = total / steps
-        row = {"workload": name, "entry": "gemm_nvfp4", "M": fw.M, "N": fw.N, "K": fw.K, "us": med * 1e3,
-               "tflops": fw.flops / (med / 1e3) / 1e12}
-        rpeak, rkey = tensor_peak(peaks, total)
+        t = timed([("gemm_nvfp4", fns)])["gemm_nvfp4"]
+        row = {"workload": name, "entry": "gemm_nvfp4", "M": fw.M, "N": fw.N, "K": fw.K, "us": t["graph_us"],
+               "single_us": t["single_us"], "tflops": fw.flops / (t["graph_us"] / 1e6) / 1e12}
+        rpeak, rkey = tensor_peak(peaks, t["graph_ms_total"])
         # FP4 roof: the measured bf16 roof times the nominal dense FP4 / bf16 ratio (13.5 / 2.25)
         row["frac_of_peak"] = row["tflops"] / (FP4_PER_BF16 * rpeak)
         row["peak"] = f"{FP4_PER_BF16:g} x {rkey}"
@@ -715,22 +803,16 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
         stream.synchronize()
         fns = [(lambda q=q, k=k, v=v, o=o: sg.attention_bf16(q, k, v, O=o, causal=aw.causal, stream=stream))
                for q, k, v, o in sets]
-        total = time_launches(torch, stream, fns, steps, 5)
-        med = total / steps
+        t = timed([("attention_bf16", fns)])["attention_bf16"]
         row = {"workload": name, "entry": "attention_bf16", "B": aw.B, "Sq": aw.Sq, "Sk": aw.Sk, "H": aw.H,
-               "Hkv": aw.Hkv, "D": aw.D, "causal": aw.causal, "us": med * 1e3}
+               "Hkv": aw.Hkv, "D": aw.D, "causal": aw.causal, "us": t["graph_us"], "single_us": t["single_us"]}
         if aw.Sq >= 128:  # prefill: tensor-bound, FLOPs over the visible pairs
-            row["tflops"] = aw.flops / (med / 1e3) / 1e12
-            rpeak, rkey = tensor_peak(peaks, total)
-            row["frac_of_peak"] = row["tflops"] / rpeak
-            row["peak"] = rkey
+            _tensor_row(row, aw.flops, t, peaks)
         else:  # decode: K and V streamed once
-            byts = aw.kv_bytes + 2 * 2 * aw.B * aw.Sq * aw.H * aw.D
-            row["gbs"] = byts / (med / 1e3) / 1e9
-            row["frac_of_hbm"] = row["gbs"] / peaks["hbm_gbs"]
+            _hbm_row(row, aw.kv_bytes + 2 * 2 * aw.B * aw.Sq * aw.H * aw.D, peaks)
         # torch's own scaled_dot_product_attention on the same inputs, for context
         q0, k0, v0, _ = sets[0]
-        tq, tk, tv = (t.transpose(1, 2) for t in (q0, k0, v0))
+        tq, tk, tv = (t_.transpose(1, 2) for t_ in (q0, k0, v0))
         sdpa_causal = aw.causal and aw.Sq == aw.Sk
         if aw.causal and aw.Sq != aw.Sk and aw.Sq != 1:
             sdpa_causal = None  # bottom-right causal has no plain sdpa flag
@@ -738,7 +820,8 @@ def measure_rows(torch, sg, syn, stream, l2, peaks, args, names=None, entries=No
             try:
                 with torch.cuda.stream(stream):
                     tfn = [lambda: torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=sdpa_causal)]
-                    row["torch_sdpa_us"] = time_launches(torch, stream, tfn, min(steps, 50), 3) / min(steps, 50) * 1e3
+                    row["torch_sdpa_us"] = time_launches(torch, stream, tfn, min(ROUND_LAUNCHES * rounds, 50), 3) \
+                        / min(ROUND_LAUNCHES * rounds, 50) * 1e3
             except RuntimeError as e:  # a comparison only: never fail the bench on it
                 row["torch_sdpa_us"] = None
                 row["torch_sdpa_error"] = str(e).splitlines()[0][:120]
@@ -759,6 +842,71 @@ def measure_micro(torch, sg, stream):
     del src, dst
     torch.cuda.empty_cache()
     return {"tcgen05_peak_tflops": tf, "tcgen05_peak_sm_mhz": mhz, "copy_gbs": copy, "read_gbs": read}
+
+
+def oracle_table(syn):
+    """The fp64 oracle timed on every bf16 GEMM config, on the host cores: the
+    full oracle up to the MLP shapes and for decode, the sampled oracle (the
+    128 x 128 row/column intersections the parity tests check) at 8192^3 and
+    16384^3, with the full oracle's time extrapolated from it (its cost is
+    proportional to the outputs it computes)."""
+    import numpy as np
+
+    import oracle
+    out = []
+    decode_b = {}
+    for name, w in syn.WORKLOADS.items():
+        if w.oracle == "full":
+            A = w.a()
+            if name.startswith("dec"):
+                # the four decode rows of a shape share one draw of its weights:
+                # the oracle's time does not depend on the values
+                key = (w.N, w.K)
+                if key not in decode_b:
+                    decode_b[key] = w.b()
+                B = decode_b[key]
+            else:
+                B = w.b()
+            t = time.perf_counter()
+            _, used = oracle.gemm(A, B, return_threads=True)
+            dt = time.perf_counter() - t
+            out.append({"workload": name, "mode": "full", "s": dt, "gflops": w.flops / dt / 1e9, "cores": used})
+        else:
+            rows = syn.sample_indices(w.M, 128, 1)
+            cols = syn.sample_indices(w.N, 128, 2)
+            A = syn.matrix_rows(rows, w.K, w.dist_a, w.seed_a)
+            B = syn.matrix_rows(cols, w.K, w.dist_b, w.seed_b)
+            t = time.perf_counter()
+            _, used = oracle.gemm_sampled(A, B, np.arange(128), np.arange(128), return_threads=True)
+            dt = time.perf_counter() - t
+            flops = 2 * 128 * 128 * w.K
+            out.append({"workload": name, "mode": "sampled 128x128", "s": dt, "gflops": flops / dt / 1e9,
+                        "cores": used, "full_s_extrapolated": dt * (w.M * w.N) / (128 * 128)})
+        del A, B
+    return out
+
+
+SUMMARY_WORKLOADS = ("sq512", "sq2048", "sq4096", "mlp_up", "mlp_down", "sq8192", "sq16384",
+                     "dec1_up", "dec2_up", "dec16_up", "dec64_up", "dec1_down", "dec2_down", "dec16_down", "dec64_down")
+
+
+def summary(rows, oracle_rows):
+    """A compact digest of the configs, printed last in the line: per config the
+    graph-replay and single-launch microseconds, the throughput and its fraction
+    of the measured roof, and the oracle's seconds."""
+    out = {"cols": "us graph, us single, TFLOP/s or GB/s, frac of measured roof"}
+    by = {(r["workload"], r["entry"]): r for r in rows}
+    for name in SUMMARY_WORKLOADS:
+        r = by.get((name, "gemm_bf16"))
+        if r is None:
+            continue
+        thr = r.get("tflops", r.get("gbs"))
+        frac = r.get("frac_of_peak", r.get("frac_of_hbm"))
+        out[name] = [round(r["us"], 2), round(r.get("single_us", float("nan")), 2), round(thr, 1 if thr > 100 else 2),
+                     round(frac, 3)]
+    if oracle_rows:
+        out["oracle_s"] = {o["workload"]: round(o.get("full_s_extrapolated", o["s"]), 3) for o in oracle_rows}
+    return out
 
 
 def cpu_baseline(syn, w):

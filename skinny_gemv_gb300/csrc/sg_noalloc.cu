@@ -110,8 +110,11 @@ extern "C" int gemv_bf16_noalloc(const void* A, const void* B, void* C, int64_t 
     const int64_t mb = std::min<int64_t>(8, M - m0);
     const sg_plan_info& plan = plans[b];
     if (plan.split_k > 1) {
-      // The array keeps the previous call's contents: the arrival counters this
-      // launch uses must start at zero.
+      // The array keeps the previous call's contents.  A kernel that runs to the
+      // end leaves its counters at zero, but one that never finished (its launch
+      // failed part-way, or its stream was torn down) would leave a count behind
+      // that the next call's slices would miscount, so each call clears the
+      // counters it uses instead of trusting the last call to have done so.
       e = cudaMemsetAsync(counters, 0, static_cast<size_t>(plan.tiles_m) * sizeof(uint32_t), s);
       if (e != cudaSuccess) {
         set_last_cuda_error(static_cast<int>(e));
@@ -133,6 +136,7 @@ extern "C" int gemv_bf16_noalloc(const void* A, const void* B, void* C, int64_t 
     p.k_slice = plan.k_steps;
     p.partials = partials;
     p.counters = counters;
+    p.prewait = plan.prefetch_steps;
     e = launch_cc_gemv(p, s);
     if (e != cudaSuccess) {
       set_last_cuda_error(static_cast<int>(e));

@@ -121,6 +121,16 @@ def matrix(rows: int, cols: int, dist: str, seed: int, ld: int | None = None,
     return out
 
 
+def matrix_rows(row_idx, cols: int, dist: str, seed: int) -> np.ndarray:
+    """Rows ``row_idx`` of ``matrix(rows, cols, dist, seed)`` without drawing the
+    others (element (r, c) is draw r*cols + c; ``cols`` even for normal draws)."""
+    row_idx = np.asarray(row_idx, dtype=np.int64)
+    out = np.empty((row_idx.size, cols), dtype=np.uint16)
+    for i, r in enumerate(row_idx):
+        out[i] = f64_to_bf16_bits(draws(dist, seed, int(r) * cols, cols))
+    return out
+
+
 def small_int_matrix(rows: int, cols: int, lo: int, hi: int, seed: int) -> np.ndarray:
     """Integers in [lo, hi] stored as bf16 (exact for |v| <= 256)."""
     u = uniform01(seed, 0, rows * cols)

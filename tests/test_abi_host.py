@@ -250,6 +250,38 @@ def test_cuda_core_plan(lib, N, K):
     assert bounds[0] == 0 and bounds[-1] == N and all(x < y for x, y in zip(bounds, bounds[1:]))
 
 
+def _header_define(name):
+    with open(os.path.join(os.path.dirname(GOLDEN), "..", "include", "skinny_gemm.h")) as f:
+        for line in f:
+            if line.startswith(f"#define {name} "):
+                return eval(line.split(None, 2)[2].replace("u", ""))  # "(1u << 20)" / "4096u"
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("sms", [152, 148, 160, 132])
+def test_cuda_core_split_fits_the_noalloc_array(lib, sms):
+    # gemv_bf16_noalloc keeps the CUDA-core kernel's split-K partials and counters
+    # in a fixed array.  The planner splits K only when there are fewer than
+    # 2 x SMs row blocks (N < 2 SMs), with at most ceil(2 SMs / N) slices, so the
+    # partials stay below (2 SMs / N + 1) * 8 rows * N * 4 B < 128 * SMs bytes and
+    # the counters at N < 2 SMs: far inside the array for any of these parts.
+    part_bytes = _header_define("SG_NOALLOC_PARTIAL_BYTES")
+    counters = _header_define("SG_NOALLOC_COUNTERS")
+    assert part_bytes == 1 << 20 and counters == 4096
+    worst = 0
+    for M in range(1, 9):
+        for N in list(range(1, 2 * sms + 2)) + [4096, 11008]:
+            for K in (2048, 11008, 1 << 16, 1 << 22):
+                info = sg.plan(M, N, K, sms, sg.PATH_CUDA_CORE)
+                if info["split_k"] > 1:
+                    assert N < 2 * sms
+                    need = info["split_k"] * M * N * 4
+                    worst = max(worst, need)
+                    assert need < 128 * sms <= part_bytes, (M, N, K, info)
+                    assert info["tiles_m"] <= counters, (M, N, K, info)
+    assert worst > 0  # some plans do split
+
+
 def test_plan_rejects_bad_arguments(lib):
     out = sg.PlanInfo()
     assert lib.sg_plan(-1, 8, 8, 152, 0, ctypes.byref(out)) == sg.SG_ERR_INVALID_ARG

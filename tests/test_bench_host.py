@@ -87,3 +87,22 @@ def test_tensor_peak_follows_the_timed_region():
     assert bench.tensor_peak(peaks, 10.0) == (1883.7, "bf16_tflops")
     assert bench.tensor_peak(peaks, 400.0) == (1707.5, "bf16_tflops_sustained")
     assert bench.tensor_peak({"bf16_tflops": 1.0, "bf16_tflops_sustained": None}, 400.0) == (1.0, "bf16_tflops")
+
+
+def test_summary_fits_the_tail_of_the_line():
+    # The bench line ends with a compact digest of every config (graph and
+    # single-launch times, throughput, fraction of the roof, oracle seconds), so a
+    # reader that keeps only the last ~1.5 KB of the line still has all of them.
+    rows = []
+    for n in bench.SUMMARY_WORKLOADS:
+        r = {"workload": n, "entry": "gemm_bf16", "us": 12345.678, "single_us": 12399.1}
+        if n.startswith("dec"):
+            r.update(gbs=6123.456, frac_of_hbm=0.904567)
+        else:
+            r.update(tflops=1888.888, frac_of_peak=0.99999)
+        rows.append(r)
+    orows = [{"workload": n, "s": 1.0, "full_s_extrapolated": 123456.789} for n in bench.SUMMARY_WORKLOADS]
+    s = bench.summary(rows, orows)
+    assert all(n in s for n in bench.SUMMARY_WORKLOADS)
+    text = json.dumps({"summary": s})
+    assert len(text) < 1400, len(text)

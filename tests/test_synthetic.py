@@ -69,3 +69,10 @@ def test_sample_indices():
     s = syn.sample_indices(16384, 128, 7)
     assert s.size == 128 and np.all(np.diff(s) > 0) and s[-1] < 16384
     assert np.array_equal(s, syn.sample_indices(16384, 128, 7))
+
+
+def test_matrix_rows_equal_the_full_matrix_rows():
+    for dist in ("uniform", "normal:0.02"):
+        full = syn.matrix(37, 50, dist, 99)
+        idx = np.array([0, 3, 17, 36])
+        assert np.array_equal(syn.matrix_rows(idx, 50, dist, 99), full[idx])
