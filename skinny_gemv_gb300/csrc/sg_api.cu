@@ -279,14 +279,17 @@ void plan_tc_swiglu(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan
 
 int skinny_bn(int64_t M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
 
-// Swapped skinny plan: 64-row weight tiles, two CTAs per SM.  When every tile
+// Swapped skinny plan: 128-row (M <= 16) or 64-row weight tiles, two CTAs per SM.  When every tile
 // fits in the resident slots, each tile is cut into split_k equal k pieces, one
 // CTA per piece, and all CTAs run at once (split mode); past that, a persistent
 // grid of two CTAs per SM walks the tiles with a Stream-K remainder.
-// Weight rows per tile.  128-row tiles would halve the activation bytes each
-// weight byte brings along, but measured slower at every M <= 64 on the 7B-model
-// decode shapes (fewer, longer-latency stages and larger partial sums).
-int skinny_rows(int64_t) { return 64; }
+// Weight rows per tile.  Each tile's MMAs are thin (N = 16 to 64 activation
+// rows), and a thin tcgen05.mma costs about the same whatever its N, so wider
+// weight tiles mean fewer MMAs for the same bytes.  128-row tiles pay at M <= 16
+// (11008 x 4096 weights 18.3 -> 17.6 us, 4096 x 11008 18.8 -> 18.6 us); at M = 64
+// they hold only three stages and split K nine ways with 32 KB partial sums
+// (20.3 -> 21.9 us and 21.5 -> 27.1 us), so 64-row tiles stay there.
+int skinny_rows(int64_t M) { return M <= 16 ? 128 : 64; }
 
 void plan_tc_skinny(int64_t M, int64_t N, int64_t K, int sms, sg_plan_info* o, bool gated = false) {
   std::memset(o, 0, sizeof *o);

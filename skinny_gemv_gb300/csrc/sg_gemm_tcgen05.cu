@@ -956,6 +956,14 @@ cudaError_t launch_tc_skinny(int bn, int rows, const CUtensorMap& tmW, const CUt
       default: return cudaErrorInvalidValue;
     }
   }
+  if (rows == 128) {
+    switch (bn) {
+      case 16: return launch_skinny<16, 128>(tmW, tmX, tmC, p, stream, tmR, batch);
+      case 32: return launch_skinny<32, 128>(tmW, tmX, tmC, p, stream, tmR, batch);
+      case 64: return launch_skinny<64, 128>(tmW, tmX, tmC, p, stream, tmR, batch);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   return cudaErrorInvalidValue;
 }
 

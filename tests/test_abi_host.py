@@ -193,7 +193,7 @@ def test_skinny_tensor_core_plan(lib, M, N, K):
     info = sg.plan(M, N, K, 152, sg.PATH_TENSOR_CORE)
     assert info["path"] == sg.PATH_TENSOR_CORE
     assert info["tile_n"] == (16 if M <= 16 else 32 if M <= 32 else 64)
-    rows = 64
+    rows = 128 if M <= 16 else 64  # wider weight tiles (fewer thin MMAs) up to 16 activation rows
     assert info["tile_m"] == rows and info["tiles_n"] == 1 and info["tiles_m"] == -(-N // rows)
     assert info["ctas_per_sm"] == 2 and info["tile_k"] == (128 if rows == 64 else 64)
     assert info["k_steps"] == -(-K // info["tile_k"])
@@ -218,8 +218,9 @@ def test_skinny_tensor_core_plan(lib, M, N, K):
 def test_prefetch_only_on_skinny_paths(lib):
     assert sg.plan(4096, 4096, 4096, 152, 0)["prefetch_steps"] == 0
     assert sg.plan(128, 4096, 4096, 152, 0)["prefetch_steps"] == 0
-    assert sg.plan(16, 11008, 4096, 152, 0)["prefetch_steps"] == 0  # 172 CTAs on 304 slots
-    assert sg.plan(16, 4096, 11008, 152, 0)["prefetch_steps"] == 8  # 64 tiles x 4 pieces
+    assert sg.plan(64, 11008, 4096, 152, 0)["prefetch_steps"] == 0  # 172 CTAs on 304 slots
+    assert sg.plan(64, 4096, 11008, 152, 0)["prefetch_steps"] == 8  # 64 tiles x 4 pieces
+    assert sg.plan(16, 11008, 4096, 152, 0)["prefetch_steps"] == 8  # 86 tiles x 3 pieces
     assert sg.plan(1, 11008, 4096, 152, 0)["prefetch_steps"] == 1
 
 
