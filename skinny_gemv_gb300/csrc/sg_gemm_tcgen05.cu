@@ -152,14 +152,19 @@ __device__ __forceinline__ void add_residual_32(float* v, const uint16_t* R, int
 
 // One warp writes 32 rows x 32 fp32 columns (lane = row) to C as bf16 (round to
 // nearest even): 64-byte-swizzled staging in one of two 2 KB buffers, then a TMA
-// store clipped at M and N.
+// store clipped at M and N.  With `own` set, the chunk goes through that 2 KB
+// buffer instead, one that no earlier store of the warp uses, so nothing is waited for.
 __device__ __forceinline__ void store_rows_32x32(const CUtensorMap* tmC, const float* v, int col0, int row0,
-                                                 uint8_t* staging, uint32_t& count, int lane, int M, int N) {
+                                                 uint8_t* staging, uint32_t& count, int lane, int M, int N,
+                                                 uint8_t* own = nullptr) {
   constexpr int kBuf = 32 * 64;
   const uint32_t buf = count & 1u;
-  if (lane == 0) bulk_wait_group_read<1>();  // buffer `buf` no longer read by TMA
-  __syncwarp();
-  const uint32_t base = smem_u32(staging + buf * kBuf) + lane * 64;
+  if (own == nullptr) {
+    if (lane == 0) bulk_wait_group_read<1>();  // buffer `buf` no longer read by TMA
+    __syncwarp();
+  }
+  uint8_t* const dst = own != nullptr ? own : staging + buf * kBuf;
+  const uint32_t base = smem_u32(dst) + lane * 64;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t phys = static_cast<uint32_t>(c) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u);
@@ -169,7 +174,7 @@ __device__ __forceinline__ void store_rows_32x32(const CUtensorMap* tmC, const f
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (row0 < M && col0 < N) tma_store_2d(tmC, staging + buf * kBuf, col0, row0);
+    if (row0 < M && col0 < N) tma_store_2d_hint(tmC, dst, col0, row0, policy_evict_first());
     bulk_commit_group();
   }
   ++count;
@@ -392,12 +397,27 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // This thread's loop sets the pace of the tensor pipe: per k-step it waits
+    // for the stage, issues the MMAs and commits, and whatever else it does per
+    // step adds to the step's time (measured: one extra global store per step cost
+    // ~40 of ~560 cycles).  So the items' k-ranges are decoded before the wait
+    // for the previous launch, the descriptors are advanced by additions, and, in
+    // the GEMM, the next stage's barrier is tested while this step's last MMA is
+    // queued.  (The swapped kernel waits on its weight stream instead; there the
+    // test measured 4% slower at M = 64.)
+    const KRanges kr(sched, unit);
     grid_dependency_wait();
     if (lane == 0 && rank == 0) {
-      uint32_t it = 0;
+      uint32_t s = 0, ph = 0;  // ring stage and the parity of its current phase
       bool ok = true;
+      bool ready = false;      // the next stage's full barrier was seen complete
+      // Descriptors of stage 0's first A and B boxes.  A byte offset d moves the
+      // address field by d / 16, without carry: shared memory ends below 256 KB.
+      const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + L::kAOff));
+      const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + L::kBOff));
       for (int i = 0; i < nitems && ok; ++i) {
-        const WorkItem w = get_item(sched, unit, i);
+        int32_t k0, k1;
+        kr.range(i, k0, k1);
         const uint32_t b = static_cast<uint32_t>(i) & 1u;
         const uint32_t use = static_cast<uint32_t>(i) >> 1;
         if (!mbar_wait(&tmem_empty[b], (use & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
@@ -407,34 +427,37 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * L::kAccCols;
-        for (int ks = w.k0; ks < w.k1; ++ks, ++it) {
-          const uint32_t s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, p.timeout_ns, abort_flag)) {
+        uint32_t acc = 0u;  // the item's first MMA overwrites the accumulator
+        for (int ks = k0; ks < k1; ++ks) {
+          if (!ready && !mbar_wait(&full[s], ph, p.timeout_ns, abort_flag)) {
             if (!*abort_flag) record_error(p.err, kDevTimeoutFull, s);
             *abort_flag = 1;
             ok = false;
             break;
           }
+          ready = false;
           tc_fence_after();
+          const uint32_t s_next = (s + 1 == STAGES) ? 0u : s + 1;
+          const uint32_t ph_next = (s + 1 == STAGES) ? ph ^ 1u : ph;
           const int nsub = min(KSUB, kboxes - ks * KSUB);
+          const uint64_t a_st = a_desc0 + s * static_cast<uint32_t>(L::kABytes / 16);
+          const uint64_t b_st = b_desc0 + s * static_cast<uint32_t>(L::kBBytes / 16);
           for (int j = 0; j < nsub; ++j) {
-            const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes + j * L::kAMats * L::kASub);
-            const uint32_t b_addr = smem_u32(smem + L::kBOff + s * L::kBBytes + j * L::kBSub);
+            const uint64_t ad = a_st + static_cast<uint32_t>(j * (L::kAMats * L::kASub / 16));
+            const uint64_t bd = b_st + static_cast<uint32_t>(j * (L::kBSub / 16));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-              // +32 bytes per 16 bf16 of K inside the 128-byte swizzle row
-              const uint32_t acc = (ks > w.k0 || j > 0 || kk > 0) ? 1u : 0u;
+              if (!SWAP && kk == kBK / 16 - 1 && j == nsub - 1 && ks + 1 < k1)
+                ready = mbar_test_wait(&full[s_next], ph_next);
+              // +32 bytes (2 in the address field) per 16 bf16 of K inside the 128-byte swizzle row
               if constexpr (PAIR) {
-                tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32),
-                                 kIdesc, acc);
+                tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, kIdesc, acc);
               } else {
-                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), kIdesc,
-                            acc);
+                tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, kIdesc, acc);
                 if constexpr (SWAP && GATED)  // the up weights into the up accumulator
-                  tc_mma_bf16(d_tmem + BN, smem_desc_sw128(a_addr + L::kASub + kk * 32),
-                              smem_desc_sw128(b_addr + kk * 32), kIdesc, acc);
+                  tc_mma_bf16(d_tmem + BN, ad + L::kASub / 16 + 2 * kk, bd + 2 * kk, kIdesc, acc);
               }
+              acc = 1u;
             }
           }
           // the stage is free (in both CTAs) once these MMAs have read it
@@ -442,6 +465,8 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
             tc_commit_pair_multicast(&empty[s], 0x3);
           else
             tc_commit(&empty[s]);
+          s = s_next;
+          ph = ph_next;
         }
         if (!ok) break;
         if constexpr (PAIR)
@@ -483,13 +508,20 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
     // overwrite with their outputs.
     const bool swap_resid = SWAP && !GATED && p.R != nullptr;
 
+    // The CTA's last item, when a whole tile: its MMAs have read the copy ring
+    // for the last time, so each chunk is staged in a 2 KB buffer of its own
+    // carved from the ring (kOutCols / 32 per warp), and the stores of the
+    // launch's tail do not wait for one another.
+    uint8_t* last_staging = nullptr;
+    static_assert(SWAP || L::kEpiWarps * (kOutCols / 32) * 2048 <= L::kRingBytes, "last tile staged in the ring");
     // Writes one chunk of kChunk fp32 columns (per thread: one row) to C.
     auto emit_chunk = [&](float* v, int tm, int tn, int j) {
       if constexpr (!SWAP) {
         const int col0 = tn * kOutCols + j * 32;
         const int row0 = tm * kTileRows + static_cast<int>(rank) * kBM + q * 32;
         if (!GATED && p.R != nullptr) add_residual_32(v, p.R, p.ldr, row0 + lane, col0, p.M, p.N);
-        store_rows_32x32(&tmC, v, col0, row0, staging, store_count, lane, p.M, p.N);
+        store_rows_32x32(&tmC, v, col0, row0, staging, store_count, lane, p.M, p.N,
+                         last_staging != nullptr ? last_staging + j * 2048 : nullptr);
       } else {
         // D[n][m]: this thread's row is weight row n, its columns activation rows
         // m; the staging tile is C's layout (row m, 64 consecutive n), so a warp's
@@ -589,6 +621,8 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + b * L::kAccCols;
       float v[L::kChunk];
+      if (!SWAP && w.npieces == 1 && i == nitems - 1)
+        last_staging = smem + L::kAOff + ew * (kOutCols / 32) * 2048;
       if (GATED && w.npieces == 1) {
         // Whole gated tile: output chunk j combines accumulator columns j * kChunk
         // (gate) and kOutCols + j * kChunk (up) of this thread's row.

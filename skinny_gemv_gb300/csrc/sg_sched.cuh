@@ -96,6 +96,42 @@ SG_HD int32_t sk_count(const Schedule& s, int32_t c) {
   return u1 > u0 ? (u1 - 1) / s.k_steps - u0 / s.k_steps + 1 : 0;
 }
 
+// The k-step ranges [k0, k1) of CTA c's work items in get_item's order, for a
+// role that needs nothing else (the MMA issuer): the divisions are done once per
+// CTA, so an item boundary costs none.
+struct KRanges {
+  int32_t nsk = 0, u0 = 0, u1 = 0, t0 = 0, k_steps = 0, split_k0 = 0, split_k1 = 0;
+  bool split = false;
+  SG_HD KRanges(const Schedule& s, int32_t c) : k_steps(s.k_steps) {
+    if (s.split > 0) {
+      split = true;
+      const int32_t pc = c % s.split;
+      split_k0 = (s.k_steps * pc) / s.split;
+      split_k1 = (s.k_steps * (pc + 1)) / s.split;
+      return;
+    }
+    nsk = sk_count(s, c);
+    if (nsk > 0) {
+      u0 = sk_range_begin(s, c);
+      u1 = sk_range_begin(s, c + 1);
+      t0 = u0 / s.k_steps;
+    }
+  }
+  SG_HD void range(int32_t i, int32_t& k0, int32_t& k1) const {
+    if (split) {
+      k0 = split_k0;
+      k1 = split_k1;
+    } else if (i >= nsk) {
+      k0 = 0;
+      k1 = k_steps;
+    } else {
+      const int32_t tb = (t0 + i) * k_steps, te = tb + k_steps;
+      k0 = (u0 > tb ? u0 : tb) - tb;
+      k1 = (u1 < te ? u1 : te) - tb;
+    }
+  }
+};
+
 // Number of work items of CTA c.
 SG_HD int32_t item_count(const Schedule& s, int32_t c) {
   if (s.split > 0) return c < s.tiles_m * s.tiles_n * s.split ? 1 : 0;
