@@ -216,18 +216,29 @@ Schedule sched_from_plan(const sg_plan_info& o) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Single-CTA tiles are 128 columns wide when the 128 x 128 tiles fit in one wave
+// of SMs, else 256.  Such a GEMM then spreads over up to twice as many SMs, each
+// with half the MMA work per k-step, and splits K less often.  Measured
+// (graph-timed): 512^3 6.4 -> 5.3 us, 1024^3 9.5 -> 8.0 us, 1536^3 12.4 -> 11.2 us,
+// 128 x 4096 x 4096 83.3 -> 26.4 us, 512 x 4096 x 4096 38.8 -> 22.4 us,
+// 128 x 11008 x 4096 56.8 -> 22.7 us; past one wave they lose (1792^3 14.0 -> 19.9 us).
+bool narrow_tiles(int64_t M, int64_t N, int sms) {
+  return ceil_div(M, kBM) * ceil_div(N, kGemmNarrowBN) <= static_cast<int64_t>(sms);
+}
+
 // tcgen05 GEMM plan.  pair: 256 x 256 tiles on clusters of two CTAs (the
-// schedule counts clusters); else 128 x 256 tiles, one CTA each.
+// schedule counts clusters); else 128 x 256 or 128 x 128 tiles, one CTA each.
 void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_info* o) {
   std::memset(o, 0, sizeof *o);
+  const bool narrow = !pair && narrow_tiles(M, N, sms);
   o->path = pair ? SG_PATH_GEMM_PAIR : SG_PATH_GEMM;
   o->tile_m = pair ? 2 * kBM : kBM;
-  o->tile_n = kGemmBN;
+  o->tile_n = narrow ? kGemmNarrowBN : kGemmBN;
   o->tile_k = kBK;
-  o->stages = pair ? kPairStages : kGemmStages;
+  o->stages = pair ? kPairStages : (narrow ? kGemmNarrowStages : kGemmStages);
   o->cluster_size = pair ? 2 : 1;
   const int32_t units = pair ? std::max(1, sms / 2) : sms;
-  const int32_t tm = static_cast<int32_t>(ceil_div(M, o->tile_m)), tn = static_cast<int32_t>(ceil_div(N, kGemmBN));
+  const int32_t tm = static_cast<int32_t>(ceil_div(M, o->tile_m)), tn = static_cast<int32_t>(ceil_div(N, o->tile_n));
   const int32_t ks = static_cast<int32_t>(ceil_div(K, kBK));
   // Raster groups of 8 tile rows: a wave of 76 pair tiles then spans ~8 rows x
   // ~10 columns of tiles, the fewest A and B bytes per wave (measured: MLP
@@ -240,7 +251,9 @@ void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_i
   o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, units);
 }
 
-bool auto_pair(int64_t M) { return M >= 2 * kBM; }
+// The automatic GEMM kernel for M > 64: CTA pairs from M = 256, except where
+// 128 x 128 single-CTA tiles fit in one wave (above).
+bool auto_pair(int64_t M, int64_t N, int sms) { return M >= 2 * kBM && !narrow_tiles(M, N, sms); }
 
 // Most Stream-K pieces any CTA of the schedule runs.
 int32_t max_sk_items(const Schedule& s) {
@@ -404,7 +417,7 @@ int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, 
   sg_plan_info plan;
   plan_tc_gemm(M, N, K, d.sm_count, pair, &plan);
   CUtensorMap ta, tb, tc;
-  const uint32_t b_rows = pair ? kGemmBN / 2 : kGemmBN;  // B rows each CTA loads per tile
+  const uint32_t b_rows = pair ? kGemmBN / 2 : static_cast<uint32_t>(plan.tile_n);  // B rows each CTA loads per tile
   int st = make_map(&ta, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tb, B, N, K, ldb, b_rows, kBK, CU_TENSOR_MAP_SWIZZLE_128B, dev);
   if (st == SG_OK) st = make_map(&tc, C, M, N, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, dev);
@@ -414,7 +427,9 @@ int run_tc_gemm(DeviceState& d, int dev, const void* A, const void* B, void* C, 
   p.inject_extra_tx = g_inject_missing_tx.exchange(0);
   p.R = static_cast<const uint16_t*>(R);
   p.ldr = ldr;
-  cudaError_t e = pair ? launch_tc_gemm_pair(ta, tb, tc, p, stream) : launch_tc_gemm(ta, tb, tc, p, stream);
+  cudaError_t e = pair                              ? launch_tc_gemm_pair(ta, tb, tc, p, stream)
+                  : plan.tile_n == kGemmNarrowBN ? launch_tc_gemm_narrow(ta, tb, tc, p, stream)
+                                                 : launch_tc_gemm(ta, tb, tc, p, stream);
   return e == cudaSuccess ? SG_OK : cuda_fail(e);
 }
 
@@ -708,7 +723,7 @@ int gemm_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N, i
   if (K == 0) return empty_sum(C, M, N, ldc, R, ldr, s);
   st = ensure_workspace(*d, s);
   if (st != SG_OK) return st;
-  const bool pair = path == SG_PATH_GEMM_PAIR || (path == SG_PATH_AUTO && auto_pair(M));
+  const bool pair = path == SG_PATH_GEMM_PAIR || (path == SG_PATH_AUTO && auto_pair(M, N, d->sm_count));
   return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, pair, s, R, ldr);
 }
 
@@ -1111,7 +1126,8 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_
   if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
   if (entry < SG_PATH_AUTO || entry > SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
   if (entry == SG_PATH_GEMM || entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && M > 64)) {
-    plan_tc_gemm(M, N, K, num_sms, entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && auto_pair(M)), out);
+    plan_tc_gemm(M, N, K, num_sms, entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && auto_pair(M, N, num_sms)),
+                 out);
     return SG_OK;
   }
   if (M > 64) return SG_ERR_INVALID_ARG;

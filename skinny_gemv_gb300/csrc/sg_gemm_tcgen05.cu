@@ -942,6 +942,11 @@ cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   return launch_variant<kGemmBN, kGemmStages, 0, 1, false>(tmA, tmB, tmC, p, stream);
 }
 
+cudaError_t launch_tc_gemm_narrow(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                  const TcParams& p, cudaStream_t stream) {
+  return launch_variant<kGemmNarrowBN, kGemmNarrowStages, 0, 1, false>(tmA, tmB, tmC, p, stream);
+}
+
 cudaError_t launch_tc_gemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmG, const CUtensorMap& tmU,
                                   const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
   return launch_variant<kGemmBN, kGemmStages, 0, 1, false, true>(tmA, tmG, tmC, p, stream, &tmU);

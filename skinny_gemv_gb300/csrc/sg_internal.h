@@ -18,6 +18,10 @@ constexpr int kMaxBatch = 8;
 constexpr int kBM = 128;  // MMA M (tile rows; weight rows on the swapped path)
 constexpr int kBK = 64;   // bf16 per k-step: one 128-byte swizzle row
 constexpr int kGemmBN = 256;
+// Single-CTA tiles 128 columns wide, for GEMMs whose 128 x 128 tiles fit in one wave
+// (six 32 KB stages).
+constexpr int kGemmNarrowBN = 128;
+constexpr int kGemmNarrowStages = 6;
 constexpr int kGemmStages = 4;
 constexpr int kPairStages = 6;  // paired tiles: 32 KB per stage per CTA
 // Stream-K pieces per CTA that the GEMM's fixup warps take (more fall back to
@@ -84,6 +88,8 @@ struct TcBatchMaps {
 
 // Non-swapped GEMM: A-operand = A (rows M), B-operand = B (rows N), BN = 256.
 cudaError_t launch_tc_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                           const TcParams& p, cudaStream_t stream);
+cudaError_t launch_tc_gemm_narrow(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const TcParams& p, cudaStream_t stream);
 
 // Gated GEMM: C = silu(A . G^T) * (A . U^T); each 128 x 256 B tile is 128 rows of

@@ -164,8 +164,11 @@ def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms, path):
     assert info["path"] == path and info["cluster_size"] == (2 if pair else 1)
     tm = 256 if pair else 128
     units = sms // 2 if pair else sms
-    assert info["tile_m"] == tm and info["tile_n"] == 256 and info["tile_k"] == 64
-    assert info["tiles_m"] == -(-M // tm) and info["tiles_n"] == -(-N // 256)
+    # single-CTA tiles are 128 wide when the 128 x 128 tiles fit in one wave
+    tn = 128 if not pair and -(-M // 128) * -(-N // 128) <= sms else 256
+    assert info["tile_m"] == tm and info["tile_n"] == tn and info["tile_k"] == 64
+    assert info["stages"] == (6 if pair or tn == 128 else 4)
+    assert info["tiles_m"] == -(-M // tm) and info["tiles_n"] == -(-N // tn)
     assert info["grid"] <= units
     T = info["tiles_m"] * info["tiles_n"]
     assert info["dp_tiles"] + info["sk_tiles"] == T
@@ -181,10 +184,19 @@ def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms, path):
 
 
 def test_auto_gemm_kernel_choice(lib):
-    assert sg.plan(128, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM
-    assert sg.plan(255, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM
-    assert sg.plan(256, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM_PAIR
+    # 128 x 128 single-CTA tiles wherever they fit in one wave of SMs
+    for M, N in [(128, 4096), (255, 4096), (256, 4096), (512, 4096), (512, 512), (1536, 1536), (128, 19456)]:
+        info = sg.plan(M, N, 4096, 152, 0)
+        assert info["path"] == sg.PATH_GEMM and info["tile_n"] == 128, (M, N)
+    # past one wave: 128 x 256 single tiles below M = 256, CTA pairs from there
+    assert sg.plan(128, 32768, 4096, 152, 0)["path"] == sg.PATH_GEMM
+    assert sg.plan(128, 32768, 4096, 152, 0)["tile_n"] == 256
+    assert sg.plan(255, 32768, 4096, 152, 0)["path"] == sg.PATH_GEMM
+    assert sg.plan(256, 32768, 4096, 152, 0)["path"] == sg.PATH_GEMM_PAIR
+    assert sg.plan(1792, 1792, 1792, 152, 0)["path"] == sg.PATH_GEMM_PAIR
     assert sg.plan(4096, 4096, 4096, 152, 0)["grid"] == 76
+    # the rule follows the SM count: 1536^3 is 144 tiles of 128 x 128
+    assert sg.plan(1536, 1536, 1536, 132, 0)["path"] == sg.PATH_GEMM_PAIR
 
 
 @pytest.mark.parametrize("M", [1, 2, 9, 16, 17, 33, 64])

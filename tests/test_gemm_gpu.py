@@ -123,6 +123,21 @@ def test_deterministic_across_runs(M, N, K, path):
         assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 4096, 4096), (384, 512, 8192), (300, 1000, 2048)])
+def test_narrow_tiles_with_stream_k(M, N, K):
+    # 128 x 128 single-CTA tiles, chosen automatically when they fit in one wave;
+    # these shapes also split K, so Stream-K partials of the narrow tiles are summed
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    info = sg.plan(M, N, K, sms, sg.PATH_AUTO)
+    assert info["path"] == sg.PATH_GEMM and info["tile_n"] == 128 and info["sk_tiles"] > 0, info
+    A = syn.matrix(M, K, "normal:1", 7000 + M)
+    B = syn.matrix(N, K, "normal:0.02", 7100 + N)
+    got = _run(A, B, M, N, K)
+    assert_close(got, oracle.gemm(A, B), K, f"narrow {M}x{N}x{K}")
+    again = _run(A, B, M, N, K)
+    assert np.array_equal(got, again), "narrow tiles: not the same bits on a rerun"
+
+
 def test_zero_k_and_empty():
     s = torch.cuda.current_stream().cuda_stream
     C = torch.full((100, 72), 3.0, dtype=torch.bfloat16, device="cuda")

@@ -60,6 +60,16 @@ def test_padded_residual_and_in_place():
     assert_close(_run(A[:16], B, R[:16], 16, N, K, inplace=True)[:, :N], ref[:16], K, "skinny in place")
 
 
+def test_narrow_stream_k_tiles():
+    # 128 x 128 single-CTA tiles split along K: the residual is added once, after the partials
+    M, N, K = 384, 512, 8192
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    info = sg.plan(M, N, K, sms, sg.PATH_GEMM)
+    assert info["tile_n"] == 128 and info["sk_tiles"] > 0, info
+    A, B, R = _inputs(M, N, K, 1331)
+    assert_close(_run(A, B, R, M, N, K, sg.PATH_GEMM), oracle.gemm_residual(A, B, R), K, "narrow stream-k residual")
+
+
 @pytest.mark.parametrize("path", [sg.PATH_GEMM, sg.PATH_GEMM_PAIR])
 def test_stream_k_tiles(path):
     M, N, K = 4096, 4096, 4096
