@@ -208,7 +208,7 @@ Schedule sched_from_plan(const sg_plan_info& o) {
   s.sk_tiles = o.sk_tiles;
   s.sk_units = o.sk_units;
   s.group_m = o.group_m;
-  s.split = o.path == SG_PATH_TENSOR_CORE ? o.split_k : 0;
+  s.split = (o.path == SG_PATH_TENSOR_CORE || o.path == SG_PATH_GEMM || o.path == SG_PATH_GEMM_PAIR) ? o.split_k : 0;
   s.sk_q = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units / s.grid) : 0;
   s.sk_r = s.sk_units > 0 ? static_cast<int32_t>(s.sk_units % s.grid) : 0;
   return s;
@@ -244,11 +244,28 @@ void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_i
   // ~10 columns of tiles, the fewest A and B bytes per wave (measured: MLP
   // 4096 x 11008 x 4096 204.6 -> 199.5 us and 4096 x 4096 x 11008 210.1 -> 202.1 us
   // against groups of 4; 4096^3 and 8192^3 unchanged within noise).
-  const Schedule s = make_schedule(tm, tn, ks, units, 4, std::min<int32_t>(tm, 8), false);
-  fill_sched(o, s);
+  Schedule s = make_schedule(tm, tn, ks, units, 4, std::min<int32_t>(tm, 8), false);
   o->split_k = 0;
+  const int64_t T = static_cast<int64_t>(tm) * tn;
+  if (T < units && s.sk_tiles == T && s.dp_tiles == 0) {
+    // Fewer tiles than units, and K worth splitting: every tile is cut into
+    // `split` equal k pieces, one per unit (split mode), so each unit runs one
+    // piece and the piece that finishes a tile is its unit's last item, summed
+    // from the idle copy ring.  Stream-K ranges over the same units would cross
+    // tile boundaries, and a piece that finishes a tile in the middle of its
+    // unit's schedule is summed by the fixup warps, at a fraction of the
+    // bandwidth.  Measured with the ring sum: 384 x 512 x 8192 56.3 -> 19.6 us,
+    // 300 x 1000 x 2048 36.1 -> 15.6 us, 256 x 256 x 65536 135 -> 51 us.  At most
+    // kGemmMaxSplit pieces per tile: their 32-column chunks fit the ring together.
+    const int32_t split = std::min<int32_t>(s.grid / static_cast<int32_t>(T), kGemmMaxSplit);
+    if (split >= 2) {
+      s = make_split_schedule(tm, tn, ks, split);
+      o->split_k = split;
+    }
+  }
+  fill_sched(o, s);
   o->ctas_per_sm = 1;
-  o->wave_efficiency = wave_efficiency(static_cast<int64_t>(tm) * tn, units);
+  o->wave_efficiency = wave_efficiency(T, units);
 }
 
 // The automatic GEMM kernel for M > 64: CTA pairs from M = 256, except where

@@ -685,6 +685,12 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
           *sk_last = (before == static_cast<uint32_t>(w.npieces - 1)) ? 1u : 0u;
         }
         named_bar_sync(1, 32 * L::kEpiWarps);
+        // The CTA's last item, when this CTA finishes its tile: the epilogue warps
+        // sum it themselves from the idle copy ring (below), since nothing follows
+        // for them to overlap it with.
+        constexpr int64_t kChunkFloats = static_cast<int64_t>(kQuads) * kSR * 4;  // one piece's 32 columns
+        const bool take_last = !SWAP && !GATED && *sk_last && i == nitems - 1 &&
+                               static_cast<int64_t>(w.npieces) * kChunkFloats * 4 <= L::kRingBytes;
         if (L::kFixupWarps > 0 && i < L::kMaxJobs) {
           // Hand the piece to the fixup warps (the sum, if this piece arrived last,
           // runs there while this epilogue goes on to the next tile).
@@ -692,9 +698,65 @@ __global__ void __launch_bounds__(TcLayout<BN, STAGES, SWAP_ROWS, KSUB, PAIR, GA
             int32_t* job = reinterpret_cast<int32_t*>(smem + L::kJobOff) + 4 * i;
             job[0] = tm;
             job[1] = tn;
-            job[2] = static_cast<int32_t>(*sk_last);
+            job[2] = static_cast<int32_t>(*sk_last && !take_last);
             mbar_arrive(&job_bar[i]);
           }
+          if (!take_last) continue;
+        }
+        if (take_last) {
+          // Chunk j (32 columns) of every piece's partial is bulk-copied into the
+          // ring under fixup_bar's phase j, two chunks' buffers in turn when they
+          // fit, then summed in k order and stored.  The piece's loads in flight
+          // are whole 16 KB chunks instead of one row per thread.
+          __threadfence();
+          float* ring = reinterpret_cast<float*>(smem);
+          constexpr int kNChunks = L::kAccCols / L::kChunk;
+          const int64_t buf_floats = static_cast<int64_t>(w.npieces) * kChunkFloats;
+          const bool two_bufs = 2 * buf_floats * 4 <= L::kRingBytes;
+          auto fetch = [&](int j) {
+            if (epi_tid == 0) {
+              float* dst = ring + ((two_bufs && (j & 1)) ? buf_floats : 0);
+              fence_proxy_async_global();
+              mbar_arrive_expect_tx(fixup_bar, static_cast<uint32_t>(buf_floats * 4));
+              for (int pj = 0; pj < w.npieces; ++pj) {
+                const int64_t sl = piece_slot(sched, w.sk_index, pj);
+                bulk_load(dst + pj * kChunkFloats,
+                          p.partials + (PAIR ? 2 * sl + rank : sl) * kSlotFloats + j * kChunkFloats,
+                          static_cast<uint32_t>(kChunkFloats * 4), fixup_bar);
+              }
+            }
+          };
+          fetch(0);
+          for (int j = 0; j < kNChunks; ++j) {
+            const bool landed = mbar_wait(fixup_bar, static_cast<uint32_t>(j) & 1u, p.timeout_ns, abort_flag);
+            if (!landed && !*abort_flag) record_error(p.err, kDevTimeoutFull, 1000 + i);
+            if (bar_sync_or(1, kEpiThreads, !landed)) {  // every thread is past chunk j - 1
+              *abort_flag = 1;
+              break;
+            }
+            if (two_bufs && j + 1 < kNChunks) fetch(j + 1);
+            const float4* src =
+                reinterpret_cast<const float4*>(ring + ((two_bufs && (j & 1)) ? buf_floats : 0));
+            float acc[L::kChunk];
+            for (int pj = 0; pj < w.npieces; ++pj) {  // k order
+#pragma unroll
+              for (int q4 = 0; q4 < kQuads; ++q4) {
+                const float4 x = src[pj * (kChunkFloats / 4) + q4 * kSR + slot_row];
+                float* a4 = &acc[4 * q4];
+                if (pj == 0) {
+                  a4[0] = x.x; a4[1] = x.y; a4[2] = x.z; a4[3] = x.w;
+                } else {
+                  a4[0] += x.x; a4[1] += x.y; a4[2] += x.z; a4[3] += x.w;
+                }
+              }
+            }
+            emit_chunk(acc, tm, tn, j);
+            if (!two_bufs && j + 1 < kNChunks) {
+              named_bar_sync(1, kEpiThreads);  // the one buffer has been read
+              fetch(j + 1);
+            }
+          }
+          if (epi_tid == 0) atomicExch(&p.counters[counter], 0u);
           continue;
         }
         if constexpr (GATED && !SWAP) {

@@ -22,6 +22,9 @@ constexpr int kGemmBN = 256;
 // (six 32 KB stages).
 constexpr int kGemmNarrowBN = 128;
 constexpr int kGemmNarrowStages = 6;
+// Most k pieces per tile in a GEMM split-mode plan: the pieces' 32-column chunks
+// of fp32 partial sums (16 KB each) must fit the copy ring together.
+constexpr int kGemmMaxSplit = 8;
 constexpr int kGemmStages = 4;
 constexpr int kPairStages = 6;  // paired tiles: 32 KB per stage per CTA
 // Stream-K pieces per CTA that the GEMM's fixup warps take (more fall back to

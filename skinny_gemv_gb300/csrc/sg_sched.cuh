@@ -89,8 +89,9 @@ SG_HD int32_t dp_count(const Schedule& s, int32_t c) {
   return c < s.dp_tiles ? (s.dp_tiles - 1 - c) / s.grid + 1 : 0;
 }
 
-// Number of Stream-K pieces of CTA c.
+// Number of Stream-K pieces of CTA c (split mode: its one piece).
 SG_HD int32_t sk_count(const Schedule& s, int32_t c) {
+  if (s.split > 0) return c < s.tiles_m * s.tiles_n * s.split ? 1 : 0;
   if (s.sk_tiles <= 0) return 0;
   const int32_t u0 = sk_range_begin(s, c), u1 = sk_range_begin(s, c + 1);
   return u1 > u0 ? (u1 - 1) / s.k_steps - u0 / s.k_steps + 1 : 0;

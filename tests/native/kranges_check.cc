@@ -1,5 +1,6 @@
 // Host check of the MMA issuer's item decoding: KRanges must give, for every CTA
-// and item of every schedule below, the k-steps [k0, k1) that get_item gives.
+// and item of every schedule below, the k-steps [k0, k1) that get_item gives; and
+// in split mode the fixup warps' piece count must be the CTA's item count.
 // Prints "ok <items checked>" and exits 0, or the first disagreement and exits 1.
 #include <cstdio>
 #include <initializer_list>
@@ -12,6 +13,11 @@ static bool check(const Schedule& s, long long& n) {
   for (int32_t c = 0; c < s.grid; ++c) {
     const KRanges kr(s, c);
     const int32_t items = item_count(s, c);
+    // split mode: a CTA's one item is its one k piece (the fixup warps count on it)
+    if (s.split > 0 && sk_count(s, c) != items) {
+      std::printf("split mode: sk_count %d != item_count %d (cta %d)\n", sk_count(s, c), items, c);
+      return false;
+    }
     for (int32_t i = 0; i < items; ++i) {
       const WorkItem w = get_item(s, c, i);
       int32_t k0 = -1, k1 = -1;

@@ -117,7 +117,9 @@ def _check_plan_coverage(info):
     KS = info["k_steps"]
     cover = np.zeros((T, KS), dtype=np.int32)
     pieces = {}
-    split_mode = info["path"] == sg.PATH_TENSOR_CORE and info["split_k"] > 0
+    # split mode (the swapped skinny plans, and GEMM plans below one wave): every
+    # tile cut into split_k pieces, one per CTA
+    split_mode = info["path"] in (sg.PATH_TENSOR_CORE, sg.PATH_GEMM, sg.PATH_GEMM_PAIR) and info["split_k"] > 0
     for cta, row in enumerate(items):
         assert len(row) >= 1, f"CTA {cta} has no work"
         n_sk = sum(1 for it in row if it[0] < info["sk_tiles"])
@@ -172,6 +174,8 @@ def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms, path):
     assert info["grid"] <= units
     T = info["tiles_m"] * info["tiles_n"]
     assert info["dp_tiles"] + info["sk_tiles"] == T
+    if info["split_k"] > 0:  # below one wave: every tile in split_k equal pieces, at most 8
+        assert T < units and 2 <= info["split_k"] <= 8 and info["grid"] == T * info["split_k"]
     if T >= units and T % units:
         rem, KS = T % units, info["k_steps"]
         if (units - rem) * KS <= 24 * units:

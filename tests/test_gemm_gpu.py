@@ -32,6 +32,8 @@ def _run(A_bits, B_bits, M, N, K, ldc=None, fill=None, path=sg.PATH_AUTO):
     C = Cfull[:, :N]
     sg.gemm_bf16(A, B, C, path=path)
     torch.cuda.synchronize()
+    st, detail = sg.check_device_errors()  # no bounded wait in any role ran out
+    assert st == sg.SG_OK, detail
     return to_bits(Cfull)[:, :N]
 
 

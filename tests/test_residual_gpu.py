@@ -33,6 +33,8 @@ def _run(A_bits, B_bits, R_bits, M, N, K, path=sg.PATH_AUTO, inplace=False):
         C = torch.empty((M, ld), dtype=torch.bfloat16, device="cuda")[:, :N]
     sg.gemm_bf16_residual(A, B, Rd, C, path=path)
     torch.cuda.synchronize()
+    st, detail = sg.check_device_errors()  # no bounded wait in any role ran out
+    assert st == sg.SG_OK, detail
     return to_bits(C)
 
 

@@ -1,7 +1,8 @@
 """The MMA issuer decodes its work items' k-step ranges with KRanges (once per
 CTA, no division per item) instead of get_item.  A host program built from the
 schedule header checks, over a sweep of tile grids, k-step counts, grid sizes and
-split factors, that both give the same [k0, k1) for every CTA and item."""
+split factors, that both give the same [k0, k1) for every CTA and item, and that
+in split mode sk_count (the fixup warps' job count) is each CTA's item count."""
 import os
 import shutil
 import subprocess
