@@ -25,7 +25,8 @@ before.  The JSON line (printed by rank 0) carries:
                        projections, the decode shapes M = 1, 2, 16, 64 on every
                        skinny entry) and the fused, batched, NVFP4 and attention
                        workloads: per-launch graph-replay median over 8 rounds
-                       in rotated arm order (cuBLAS through torch.matmul is an
+                       of 50-launch graphs, arm order rotated and reversed
+                       between rounds (cuBLAS through torch.matmul is an
                        arm, for context), single-launch median of 100, wave
                        efficiency of the plan
   microbench           the measured tcgen05 peak / copy / read roofs
@@ -553,12 +554,13 @@ ENTRIES = {"auto": None, "cuda_core": 1, "tensor_core": 2}
 # Rows' timing protocol (gemm3 benchmarks page, "Methodology"; spark-kernels, "how
 # things are measured"): every arm of a workload (our entries, and cuBLAS through
 # torch.matmul for context) is captured as one CUDA graph of ROUND_LAUNCHES
-# launches over the rotating inputs; ROUNDS rounds replay the arms in rotated
-# order and each arm's per-launch time is the median over the rounds.  Beside it,
+# launches over the rotating inputs (the page's 50 timed replays per round);
+# ROUNDS rounds replay the arms in an order rotated, and reversed every other
+# round, and each arm's per-launch time is the median over the rounds.  Beside it,
 # SINGLE_LAUNCHES launches are timed one by one (events around each) and their
 # median is the single-launch time, which includes the launch gap.
 ROUNDS = 8
-ROUND_LAUNCHES = 20
+ROUND_LAUNCHES = 50
 SINGLE_LAUNCHES = 100
 COOL_DOWN_S = 1.0  # idle before each compute-bound row
 
@@ -581,7 +583,10 @@ def time_arms(torch, stream, arms, warmup: int = 5, rounds: int = ROUNDS, per_ro
     labels = [label for label, _ in arms]
     for r in range(rounds):
         k = r % len(labels)
-        for label in labels[k:] + labels[:k]:
+        order = labels[k:] + labels[:k]
+        if r % 2:
+            order.reverse()
+        for label in order:
             per[label].append(replay_ms(torch, stream, graphs[label]) / per_round)
     out = {}
     for label, fns in arms:
