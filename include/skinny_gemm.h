@@ -68,17 +68,20 @@ typedef enum {
     SG_PATH_AUTO = 0,        /* library's choice (see gemv_bf16) */
     SG_PATH_CUDA_CORE = 1,   /* fp32 FMA stream over the weights, no tensor cores */
     SG_PATH_TENSOR_CORE = 2, /* tcgen05 with the weight rows on the MMA's M side */
-    SG_PATH_GEMM = 3,        /* tcgen05 GEMM, one CTA per 128 x 256 tile */
+    SG_PATH_GEMM = 3,        /* tcgen05 GEMM, one CTA per 128 x 256 or 128 x 128 tile */
     SG_PATH_GEMM_PAIR = 4    /* tcgen05 GEMM, a 2-CTA cluster per 256 x 256 tile */
 } sg_path;
 
 /*
  * gemm_bf16 -- C = A . B^T for any M, N, K (the main entry point).
  *
- * M > 64 runs the persistent tcgen05 GEMM: 128 x 256 output tiles, a TMA-fed
- * ring of 128-byte-swizzled shared-memory stages, warp-specialised producer /
- * MMA / epilogue roles, fp32 accumulators in tensor memory, a Stream-K tail
- * (spark-kernels, "stream-k proper") and a TMA-store epilogue.  M <= 64 is
+ * M > 64 runs the persistent tcgen05 GEMM: a TMA-fed ring of 128-byte-swizzled
+ * shared-memory stages, warp-specialised producer / MMA / epilogue roles, fp32
+ * accumulators in tensor memory, a Stream-K tail (spark-kernels, "stream-k
+ * proper") and a TMA-store epilogue.  Its tiles are 256 x 256 on clusters of two
+ * CTAs from M = 256, or 128 x 128 on one CTA each when those fit in one wave of
+ * SMs (then K is split into equal pieces, one per CTA, if the tiles still leave
+ * SMs idle), or 128 x 256 on one CTA below M = 256.  M <= 64 is
  * routed to the skinny path exactly as gemv_bf16 would (spark-kernels, "the
  * decode kernel": the decode shapes get their own kernel).
  *
@@ -348,7 +351,8 @@ SG_API int gemv_bf16_noalloc(const void *A, const void *B, void *C,
 
 /*
  * gemm_bf16_path -- gemm_bf16 with the kernel chosen by the caller:
- * SG_PATH_AUTO (gemm_bf16's choice), SG_PATH_GEMM (one CTA per 128 x 256 tile),
+ * SG_PATH_AUTO (gemm_bf16's choice), SG_PATH_GEMM (one CTA per tile: 128 x 128
+ * when those tiles fit in one wave of SMs, else 128 x 256),
  * SG_PATH_GEMM_PAIR (a cluster of two CTAs on two SMs per 256 x 256 tile, each
  * CTA loading half of the A rows and half of the B rows of the tile), or, for
  * M <= 64, SG_PATH_CUDA_CORE / SG_PATH_TENSOR_CORE as in gemv_bf16_path.  Any M
@@ -411,8 +415,9 @@ typedef struct {
     int32_t group_m;    /* raster group height */
     int32_t stages;     /* shared-memory ring depth */
     int32_t split_k;    /* CUDA-core path: K slices per row group; tensor-core skinny
-                           path: k pieces per weight tile, one CTA each, every CTA
-                           resident at once (0: persistent schedule); else 0 */
+                           path and bf16 GEMM paths: k pieces per tile, one CTA (or
+                           cluster) each, every one resident at once (0: persistent
+                           schedule); else 0 */
     int32_t rows_per_cta; /* CUDA-core path: weight rows per CTA */
     double wave_efficiency; /* of one tile per CTA, (ctas/slots)/ceil(ctas/slots) */
     int32_t cluster_size; /* CTAs per schedule unit: 2 for SG_PATH_GEMM_PAIR, else 1 */
