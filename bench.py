@@ -210,13 +210,40 @@ def tensor_peak(peaks: dict, timed_ms: float):
 GEMM_KERNEL_SOURCES = ("sg_gemm_tcgen05.cu", "sg_internal.h", "sg_ptx.cuh", "sg_sched.cuh")
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its comments, whitespace runs collapsed (string and
+    character literals kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and i + 1 < n and text[i + 1] == "/":
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif c == "/" and i + 1 < n and text[i + 1] == "*":
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the GEMM kernel's sources, comments and layout aside: a recorded
+    traffic figure stays valid across comment edits, not across code changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "skinny_gemv_gb300", "csrc")
     for name in GEMM_KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,7 +1,7 @@
 // Persistent tcgen05 GEMM for sm_103a: C[M,N] = A[M,K] . B[N,K]^T, bf16 in,
 // fp32 accumulate in tensor memory, bf16 out.
 //
-// One CTA per SM, 6 warps with fixed roles:
+// One CTA per SM (two on the swapped variant), warps with fixed roles:
 //   warp 0     TMA producer: per k-step waits for a free ring stage, arms its
 //              `full` barrier with the stage's byte count and issues two tiled
 //              cp.async.bulk.tensor loads (A box 64 x 128, B box 64 x BN, 128-byte
@@ -12,9 +12,14 @@
 //              `tmem_full`;
 //   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, Stream-K partials,
 //              fp32 -> bf16 (round to nearest even), 64-byte-swizzled staging and
-//              TMA stores (clipped at M and N), then release the accumulator.
+//              TMA stores (clipped at M and N), then release the accumulator;
+//   warps 6-7  (GEMM variants) sum the fp32 partials of Stream-K tiles that this
+//              CTA finishes in the middle of its schedule.  A CTA's last item is
+//              summed by the epilogue warps from the idle copy ring instead.
 // Two accumulators (2 x BN TMEM columns) let the epilogue of one tile overlap the
-// main loop of the next.
+// main loop of the next.  The single-CTA GEMM comes with BN = 256 or, for GEMMs
+// whose 128 x 128 tiles fit in one wave, BN = 128; below one wave K may be split
+// into equal pieces, one per CTA (split mode of the schedule).
 //
 // This is spark-kernels' variant 5 ("the copies were the problem, not the power":
 // a producer warp with cp.async.bulk.tensor boxes, 128-byte swizzle, a full and an
@@ -30,9 +35,10 @@
 // moves 2/3 of the bytes of the 128 x 256 single-CTA tile for the same FLOPs.
 //
 // The swapped variant (SWAP = true) serves the skinny path: the weights B take
-// the MMA's 128-row M side and the few activation rows of A its N side (16, 32 or
-// 64), so every weight byte is loaded once for all rows; its epilogue writes
-// C[m, n] = D[n, m] with direct coalesced stores.
+// the MMA's M side (64- or 128-row tiles) and the few activation rows of A its N
+// side (16, 32 or 64), so every weight byte is loaded once for all rows; its
+// epilogue writes C[m, n] = D[n, m] into a shared-memory tile in C's layout and
+// stores it with one TMA store.
 #include <cuda_bf16.h>
 
 #include "sg_internal.h"

@@ -106,3 +106,10 @@ def test_summary_fits_the_tail_of_the_line():
     assert all(n in s for n in bench.SUMMARY_WORKLOADS)
     text = json.dumps({"summary": s})
     assert len(text) < 1400, len(text)
+
+
+def test_kernel_hash_ignores_comments_not_code():
+    src = 'int a = 1; // note\n/* block */ asm("x // y"); char q = \'"\';\n'
+    assert bench.strip_c_comments(src) == 'int a = 1; asm("x // y"); char q = \'"\';'
+    assert bench.strip_c_comments(src.replace("// note", "// other words")) == bench.strip_c_comments(src)
+    assert bench.strip_c_comments(src.replace("a = 1", "a = 2")) != bench.strip_c_comments(src)
