@@ -157,7 +157,9 @@ def _check_plan_coverage(info):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (2048, 2048, 2048), (512, 512, 512),
                                    (4096, 11008, 4096), (4096, 4096, 11008), (8192, 8192, 8192),
-                                   (65, 257, 4104), (1000, 3000, 200), (129, 8, 64)])
+                                   (65, 257, 4104), (1000, 3000, 200), (129, 8, 64),
+                                   # below one wave: narrow tiles, K split into equal pieces
+                                   (128, 4096, 4096), (384, 512, 8192), (300, 1000, 2048), (256, 256, 65536)])
 @pytest.mark.parametrize("sms", [148, 152, 170])
 @pytest.mark.parametrize("path", [sg.PATH_GEMM, sg.PATH_GEMM_PAIR])
 def test_gemm_plan_covers_every_unit_once(lib, M, N, K, sms, path):
