@@ -81,7 +81,8 @@ typedef enum {
  * proper") and a TMA-store epilogue.  Its tiles are 256 x 256 on clusters of two
  * CTAs from M = 256, or 128 x 128 on one CTA each when those fit in one wave of
  * SMs (then K is split into equal pieces, one per CTA, if the tiles still leave
- * SMs idle), or 128 x 256 on one CTA below M = 256.  M <= 64 is
+ * SMs idle), or 128 x 256 on one CTA below M = 256 and where at most 32 k-steps
+ * of pair tiles would fall short of a wave.  M <= 64 is
  * routed to the skinny path exactly as gemv_bf16 would (spark-kernels, "the
  * decode kernel": the decode shapes get their own kernel).
  *

@@ -269,8 +269,17 @@ void plan_tc_gemm(int64_t M, int64_t N, int64_t K, int sms, bool pair, sg_plan_i
 }
 
 // The automatic GEMM kernel for M > 64: CTA pairs from M = 256, except where
-// 128 x 128 single-CTA tiles fit in one wave (above).
-bool auto_pair(int64_t M, int64_t N, int sms) { return M >= 2 * kBM && !narrow_tiles(M, N, sms); }
+// 128 x 128 single-CTA tiles fit in one wave (above), or where at most 32 k-steps
+// of 256 x 256 pair tiles fall short of a wave while 128 x 256 single-CTA tiles
+// fit in one: the pairs' set-up then weighs more than their lighter operand
+// traffic (2048^3 16.3 -> 15.8 us, 1792^3 14.35 -> 13.96 us; at 64 k-steps the
+// pairs stay ahead, 1024 x 4096 x 4096 25.3 against 27.5 us).
+bool auto_pair(int64_t M, int64_t N, int64_t K, int sms) {
+  if (M < 2 * kBM || narrow_tiles(M, N, sms)) return false;
+  const bool short_sub_wave = ceil_div(K, kBK) <= 32 && ceil_div(M, 2 * kBM) * ceil_div(N, kGemmBN) < sms / 2 &&
+                              ceil_div(M, kBM) * ceil_div(N, kGemmBN) <= sms;
+  return !short_sub_wave;
+}
 
 // Most Stream-K pieces any CTA of the schedule runs.
 int32_t max_sk_items(const Schedule& s) {
@@ -740,7 +749,7 @@ int gemm_dispatch(const void* A, const void* B, void* C, int64_t M, int64_t N, i
   if (K == 0) return empty_sum(C, M, N, ldc, R, ldr, s);
   st = ensure_workspace(*d, s);
   if (st != SG_OK) return st;
-  const bool pair = path == SG_PATH_GEMM_PAIR || (path == SG_PATH_AUTO && auto_pair(M, N, d->sm_count));
+  const bool pair = path == SG_PATH_GEMM_PAIR || (path == SG_PATH_AUTO && auto_pair(M, N, K, d->sm_count));
   return run_tc_gemm(*d, dev, A, B, C, M, N, K, lda, ldb, ldc, pair, s, R, ldr);
 }
 
@@ -1143,8 +1152,8 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t entry, sg_
   if (!out || M < 0 || N < 0 || K < 0 || num_sms < 1) return SG_ERR_INVALID_ARG;
   if (entry < SG_PATH_AUTO || entry > SG_PATH_GEMM_PAIR) return SG_ERR_INVALID_ARG;
   if (entry == SG_PATH_GEMM || entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && M > 64)) {
-    plan_tc_gemm(M, N, K, num_sms, entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && auto_pair(M, N, num_sms)),
-                 out);
+    plan_tc_gemm(M, N, K, num_sms,
+                 entry == SG_PATH_GEMM_PAIR || (entry == SG_PATH_AUTO && auto_pair(M, N, K, num_sms)), out);
     return SG_OK;
   }
   if (M > 64) return SG_ERR_INVALID_ARG;

@@ -199,10 +199,17 @@ def test_auto_gemm_kernel_choice(lib):
     assert sg.plan(128, 32768, 4096, 152, 0)["tile_n"] == 256
     assert sg.plan(255, 32768, 4096, 152, 0)["path"] == sg.PATH_GEMM
     assert sg.plan(256, 32768, 4096, 152, 0)["path"] == sg.PATH_GEMM_PAIR
-    assert sg.plan(1792, 1792, 1792, 152, 0)["path"] == sg.PATH_GEMM_PAIR
     assert sg.plan(4096, 4096, 4096, 152, 0)["grid"] == 76
-    # the rule follows the SM count: 1536^3 is 144 tiles of 128 x 128
-    assert sg.plan(1536, 1536, 1536, 132, 0)["path"] == sg.PATH_GEMM_PAIR
+    # pair tiles short of a wave at <= 32 k-steps, 128 x 256 single tiles within one: single
+    for M, N, K in [(2048, 2048, 2048), (1792, 1792, 1792), (1024, 4096, 2048)]:
+        info = sg.plan(M, N, K, 152, 0)
+        assert info["path"] == sg.PATH_GEMM and info["tile_n"] == 256, (M, N, K)
+    assert sg.plan(1024, 4096, 4096, 152, 0)["path"] == sg.PATH_GEMM_PAIR  # 64 k-steps: pairs
+    assert sg.plan(2048, 4096, 2048, 152, 0)["path"] == sg.PATH_GEMM_PAIR  # a full wave of pairs
+    # the rules follow the SM count: 1536^3 is 144 tiles of 128 x 128, more than 132
+    # SMs, so 128 x 256 single tiles (36 pair tiles are short of 66 clusters)
+    info = sg.plan(1536, 1536, 1536, 132, 0)
+    assert info["path"] == sg.PATH_GEMM and info["tile_n"] == 256
 
 
 @pytest.mark.parametrize("M", [1, 2, 9, 16, 17, 33, 64])
